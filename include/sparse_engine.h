@@ -1,0 +1,272 @@
+/*
+ * sparse_engine.h -- C ABI of libsparse_engine.so, the GB300 (sm_103a) hot path
+ * of sparse-first KV-cache decoding: Quest page selection, split-K GQA decode
+ * attention over an AttentionView, SnapKV compaction and the H2O step.
+ *
+ * Sources: the SparseEngine pages --
+ *   [tokendh] tokendh.com news article on SparseEngine, sections
+ *             "历史太长,会撑爆什么" (method families; Quest picks pages by the
+ *             query, H2O keeps an accumulated attention score and deletes) and
+ *             "把边界划在'生命周期'上" (per-method cache managers; SnapKV reads
+ *             the last few tokens' attention and physically deletes; H2O
+ *             updates scores each decode step; AttentionView turns every
+ *             method's cache into one format the attention reads);
+ *   [card]    "SparseEngine：稀疏优先推理引擎" (ai-feeds.com paper card),
+ *             section "方法 / 关键模块" (AttentionView exposes the selected
+ *             positions uniformly, so methods need no kernel changes);
+ *   [jetabc]  "长程 agent 把显存撑爆以后" (jetabc.cn explainer), section
+ *             "四、为什么进不了 vLLM 一类的引擎" (fixed-size pages + a table
+ *             mapping tokens to pages).
+ * The pages give no formulas; each entry point states the definition it computes.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer in a struct or argument is a DEVICE pointer unless marked
+ *     "host".  The caller owns and allocates all memory; the library never
+ *     allocates, never frees, and never synchronises the stream.
+ *   - bf16 = IEEE bfloat16 bit patterns (uint16 in memory).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *     Calls are reentrant; the library's only global state is a per-device
+ *     cache of device attributes.
+ *   - Host-side validation failures return a negative status and launch
+ *     nothing.  A failed CUDA launch returns SE_ERR_CUDA.
+ *   - Workspace (`ws`, `ws_bytes`): a caller-provided device buffer, 256-byte
+ *     aligned, of at least the size its *_workspace() function returns.  Its
+ *     first 4 bytes are the DEVICE STATUS WORD (int32): kernels OR in SE_DEV_*
+ *     bits when they meet inconsistent device data (an index outside its
+ *     buffer, a full segment, a wait that ran out of time); the offending
+ *     access is skipped, nothing traps.  The word is sticky: clear it (a
+ *     4-byte memset) to reset; read it after synchronising the stream.
+ *     Calls that share one workspace must not overlap on the GPU.
+ *   - Supported shapes: head_dim in {64, 128}; page size 16; group size
+ *     G = num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}.
+ *   - A "unit" is one (sequence b, KV head h) pair, u = b*num_kv_heads + h.
+ */
+#ifndef SPARSE_ENGINE_H
+#define SPARSE_ENGINE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values) ------------------------------------- */
+#define SE_OK               0
+#define SE_ERR_INVALID_ARG (-1)  /* null pointer, bad size or stride */
+#define SE_ERR_UNSUPPORTED (-2)  /* shape outside the supported set */
+#define SE_ERR_WORKSPACE   (-3)  /* workspace missing, misaligned or too small */
+#define SE_ERR_CUDA        (-4)  /* a CUDA runtime call or launch failed */
+#define SE_ERR_CAPACITY    (-5)  /* an output buffer is too small for the request */
+
+/* ---- device status word bits (workspace bytes 0..3) -------------------- */
+#define SE_DEV_BAD_INDEX   1     /* block-table entry / row / position outside its buffer */
+#define SE_DEV_CAPACITY    2     /* append past the last page or a full segment: dropped */
+#define SE_DEV_BAD_LENGTH  4     /* a device length outside [0, capacity]: clamped */
+#define SE_DEV_TIMEOUT     8     /* an intra-CTA wait ran past its limit; results invalid */
+
+#define SE_PAGE_SIZE 16
+#define SE_MAX_SPLITS 64
+
+typedef void* se_stream_t;       /* cudaStream_t */
+
+/* Paged KV cache with Quest page summaries ([jetabc] paging; [tokendh] the
+ * "summary index" of dynamic-sparse methods).
+ *   k, v   bf16 [num_pages][num_kv_heads][page_size][head_dim]: one (page, head)
+ *          chunk is page_size contiguous rows of head_dim elements.  Viewed as
+ *          [rows][head_dim], a token is row (page*num_kv_heads + h)*16 + slot.
+ *   meta   bf16 [num_pages][num_kv_heads][2][head_dim]: per (page, head) the
+ *          channel-wise min over the page's valid tokens, then the max.
+ *   block_table int32 [batch][max_pages_per_seq]: physical page of each logical
+ *          page (entries past a sequence's pages are never read).
+ *   ctx_len int32 [batch]: tokens held per sequence (se_kv_append increments it). */
+typedef struct se_paged_kv {
+    void* k;
+    void* v;
+    void* meta;
+    const int32_t* block_table;
+    int32_t* ctx_len;
+    int32_t num_pages;
+    int32_t max_pages_per_seq;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t page_size;
+} se_paged_kv;
+
+/* AttentionView ([card] "exposes the selected positions in one format";
+ * [tokendh] AttentionView): for each unit u, the rows it attends, as chunks of
+ * 16 consecutive rows of a row-addressed K/V base ([rows][head_dim] bf16).
+ *   chunk_row int32 [num_units][max_chunks]: first row of each chunk.
+ *   n_tokens  int32 [num_units]: tokens of unit u; chunk c holds
+ *             min(16, n_tokens - 16c) valid rows (only the last may be partial).
+ * Token order = chunk order, then row order within a chunk. */
+typedef struct se_view {
+    int32_t* chunk_row;
+    int32_t* n_tokens;
+    int32_t num_units;
+    int32_t max_chunks;
+} se_view;
+
+/* Per-(sequence, KV head) variable-length cache: the physical home of evicted
+ * caches ([tokendh] SnapKV/H2O delete physically; retained tokens keep their
+ * logical positions, section "聊天记录也能'续命':Chain Cache").
+ *   k, v    bf16 [total_rows][head_dim]
+ *   pos     int32 [total_rows]: logical position of each held row
+ *   score   float [total_rows] or NULL: per-token accumulated score (H2O)
+ *   seg_off int32 [num_units]: first row of unit u's segment
+ *   seg_len int32 [num_units]: rows held
+ *   seq_len int32 [batch]: logical tokens seen per sequence (= next position)
+ *   seg_cap rows available to each segment (seg_off[u] + seg_cap <= total_rows). */
+typedef struct se_varlen_kv {
+    void* k;
+    void* v;
+    int32_t* pos;
+    float* score;
+    const int32_t* seg_off;
+    int32_t* seg_len;
+    int32_t* seq_len;
+    int32_t seg_cap;
+    int32_t total_rows;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} se_varlen_kv;
+
+/* H2O state: a varlen cache whose segments hold at most budget+1 slots, with
+ * scores, plus the slot freed by the last eviction. */
+typedef struct se_h2o_state {
+    se_varlen_kv kv;          /* seg_cap >= budget + 1, score != NULL */
+    int32_t* free_slot;       /* int32 [num_units]: slot of the next token when full */
+    int32_t budget;           /* tokens kept after each step */
+    int32_t recent;           /* newest positions never evicted (1 <= recent <= budget) */
+} se_h2o_state;
+
+/* Decode options (optional; NULL means all defaults). */
+typedef struct se_decode_opts {
+    int32_t out_dtype;        /* 0 = bf16 output (default), 1 = fp32 output */
+    int32_t max_splits;       /* split-K pieces per unit, 1..64 (0 = default 64) */
+    float* logits_out;        /* NULL, or fp32 [num_units][logits_stride][G]:
+                                 scale*q.k of every attended token, view order */
+    int32_t logits_stride;    /* tokens per unit in logits_out */
+    void* ev_kernel_begin;    /* NULL or a cudaEvent_t recorded right before / */
+    void* ev_kernel_end;      /* right after the attention kernel (timing only) */
+} se_decode_opts;
+
+/* ---- library ------------------------------------------------------------ */
+const char* se_status_str(int status);      /* static string, never NULL */
+int se_version(void);                       /* ABI version, currently 1 */
+
+/* ---- workspace sizes (bytes, multiples of 256) --------------------------- */
+size_t se_small_workspace(void);            /* ops that need only the status word */
+size_t se_quest_select_workspace(int batch, int num_kv_heads, int max_pages_per_seq);
+size_t se_sparse_decode_workspace(int num_units, int group_size, int head_dim, int max_splits);
+size_t se_snapkv_workspace(int batch, int num_kv_heads, int num_q_heads, int window, int max_ctx);
+size_t se_h2o_workspace(int batch, int num_kv_heads, int num_q_heads, int head_dim, int seg_cap);
+
+/* ---- page summaries ----------------------------------------------------- */
+/* Rebuilds meta for every valid (page, head) of the first `batch` sequences:
+ * kmin/kmax over tokens [16p, min(16p+16, ctx_len[b])).  Called once after
+ * prefill.  Bad block-table entries set SE_DEV_BAD_INDEX and are skipped.
+ * Workspace: se_small_workspace(). */
+int se_page_meta_build(const se_paged_kv* kv, int batch,
+                       void* ws, size_t ws_bytes, se_stream_t stream);
+
+/* Decode-step append: writes k_new/v_new (bf16 [batch][num_kv_heads][head_dim])
+ * at position ctx_len[b], folds the key into its page's min/max (a page's first
+ * token sets both), then increments ctx_len[b].  block_table[b][ctx_len[b]/16]
+ * must name a page; past max_pages_per_seq: SE_DEV_CAPACITY, token dropped.
+ * Workspace: se_small_workspace(). */
+int se_kv_append(const se_paged_kv* kv, const void* k_new, const void* v_new, int batch,
+                 void* ws, size_t ws_bytes, se_stream_t stream);
+
+/* ---- (a) Quest page selection ([tokendh] Quest picks pages by the query) ----
+ * For unit u = (b, h) with query heads g of KV head h and n = ceil(ctx_len[b]/16):
+ *   U[p] = sum_g sum_d max(q[b,hG+g,d]*kmin[p,h,d], q[b,hG+g,d]*kmax[p,h,d])
+ *   k    = max(1, budget_tokens[b] / 16)   (integer division)
+ *   selected = all pages if n <= k, else the last page n-1 plus the k-1 best of
+ *   pages 0..n-2 under (U desc, page asc); written in ascending order.
+ * q         bf16 [batch][num_q_heads][head_dim]
+ * budget_tokens int32 [batch]
+ * sel_pages int32 [num_units][max_pages_per_seq]: logical page ids (first n_sel[u])
+ * n_sel     int32 [num_units]
+ * view      filled for the paged K/V viewed as rows: chunk c of unit u is page
+ *           block_table[b][sel[c]] of head h; n_tokens counts valid tokens.
+ *           Needs view->num_units == batch*num_kv_heads and
+ *           view->max_chunks >= max_pages_per_seq.
+ * U is evaluated in fp32 as sum_d (Q+[d]*kmax[d] + Q-[d]*kmin[d]) with
+ * Q+ = sum_g max(q_g, 0), Q- = sum_g min(q_g, 0): the same value in exact
+ * arithmetic.  Workspace: se_quest_select_workspace(). */
+int se_quest_select(const se_paged_kv* kv, const void* q, int batch, int num_q_heads,
+                    const int32_t* budget_tokens, int32_t* sel_pages, int32_t* n_sel,
+                    const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);
+
+/* View of whole varlen segments: chunk c of unit u starts at row seg_off[u] + 16c;
+ * n_tokens[u] = seg_len[u].  Needs view->max_chunks >= ceil(seg_cap / 16).
+ * Workspace: se_small_workspace(). */
+int se_view_from_segments(const se_varlen_kv* kv, int batch, const se_view* view,
+                          void* ws, size_t ws_bytes, se_stream_t stream);
+
+/* ---- (b) split-K GQA decode attention over a view ----------------------------
+ * For unit u = (b, h), each query head g of the group, over the view's T tokens t:
+ *   s[g,t] = scale * q[b,hG+g] . k_rows[row(t)]
+ *   out[b,hG+g] = sum_t softmax_t(s[g,:]) v_rows[row(t)];  lse = log sum_t exp(s[g,t])
+ * Each unit is cut into at most max_splits pieces of whole chunks; the pieces are
+ * merged by their log-sum-exp.  T = 0 gives out = 0, lse = -inf.
+ * k_rows, v_rows bf16 [total_rows][head_dim]; q bf16 [batch][num_q_heads][head_dim];
+ * out bf16 or fp32 [batch][num_q_heads][head_dim]; lse fp32 [batch][num_q_heads] or NULL.
+ * A chunk row outside [0, total_rows) sets SE_DEV_BAD_INDEX and counts as empty.
+ * Workspace: se_sparse_decode_workspace(num_units, G, head_dim, max_splits). */
+int se_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
+                     const se_view* view, const void* q, int batch, int num_q_heads,
+                     int num_kv_heads, int head_dim, float scale, const se_decode_opts* opts,
+                     void* out, float* lse, void* ws, size_t ws_bytes, se_stream_t stream);
+
+/* Varlen append for decode over compacted caches: writes k_new/v_new (bf16
+ * [batch][num_kv_heads][head_dim]) at row seg_off[u] + seg_len[u] with
+ * pos = seq_len[b], then increments seg_len[u] and seq_len[b].  A full segment
+ * sets SE_DEV_CAPACITY and drops the token.  Workspace: se_small_workspace(). */
+int se_varlen_append(const se_varlen_kv* kv, const void* k_new, const void* v_new, int batch,
+                     void* ws, size_t ws_bytes, se_stream_t stream);
+
+/* ---- (c) SnapKV compaction ([tokendh] SnapKV: the last few tokens' attention
+ * over the history decides what is kept; the rest is deleted physically) ------------
+ * For unit (b, h), L = ctx_len[b]: window row i = 0..window-1 (position L-window+i,
+ * queries q_win[b][i][hG+g]) attends causally to keys j <= L-window+i and
+ *   A[j] = sum_i sum_g softmax_j(scale * q_win[b,i,hG+g] . k[j]).
+ * Candidates are positions [0, L-recent); their A is max-pooled with the odd window
+ * `pool_kernel` (stride 1, same length, clipped borders); the best `keep` under
+ * (pooled desc, position asc) plus positions [L-recent, L) are kept, ascending.
+ * SnapKV proper uses recent = window; recent > window with pool_kernel 1 seeds H2O.
+ * Output rows seg_off[u] .. seg_off[u]+n_kept-1 of out->k/v, out->pos, out->score
+ * (the unpooled A of each kept token) when non-NULL; seg_len[u] = n_kept;
+ * seq_len[b] = L.  n_kept = min(keep, L-recent) + recent must fit seg_cap.
+ * prefill: paged K/V (meta unused); q_win bf16 [batch][window][num_q_heads][head_dim].
+ * Limits: 1 <= window <= 64, window*G <= 512, 1 <= recent <= L, L <= max_ctx of the
+ * workspace query, pool_kernel odd and <= 63.
+ * Workspace: se_snapkv_workspace(batch, num_kv_heads, num_q_heads, window, max_ctx). */
+int se_snapkv_compact(const se_paged_kv* prefill, const void* q_win, int batch, int num_q_heads,
+                      int window, int pool_kernel, int keep, int recent, float scale,
+                      const se_varlen_kv* out, void* ws, size_t ws_bytes, se_stream_t stream);
+
+/* ---- (d) H2O decode step ([tokendh] H2O: accumulated attention scores updated
+ * every decode step, then a physical deletion) -----------------------------------
+ * For each unit u = (b, h):
+ *   1. the new token (k_new/v_new bf16 [batch][num_kv_heads][head_dim]) goes to slot
+ *      seg_len[u] while seg_len[u] < seg_cap, else to free_slot[u], with
+ *      pos = seq_len[b] and score 0;
+ *   2. decode attention of q (bf16 [batch][num_q_heads][head_dim]) over all held
+ *      tokens -> out (bf16 or fp32 per out_dtype), lse (fp32, NULL allowed);
+ *   3. score[t] += sum_g exp(s[g,t] - lse[g]) for every held token t;
+ *   4. if more than `budget` tokens are held: among tokens whose position is not
+ *      one of the `recent` largest, the last under (score desc, position asc) --
+ *      the lowest score, the higher position on equal scores -- is evicted; its
+ *      slot becomes free_slot[u] and its position goes to evicted_pos[u] (else -1).
+ * seq_len[b] is incremented.  Positions stay unique per unit.
+ * Workspace: se_h2o_workspace(batch, num_kv_heads, num_q_heads, head_dim, seg_cap). */
+int se_h2o_step(const se_h2o_state* st, const void* q, const void* k_new, const void* v_new,
+                int batch, int num_q_heads, float scale, int out_dtype, void* out, float* lse,
+                int32_t* evicted_pos, void* ws, size_t ws_bytes, se_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPARSE_ENGINE_H */
