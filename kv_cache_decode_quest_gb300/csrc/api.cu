@@ -1,0 +1,241 @@
+// C ABI of libsparse_engine: host-side validation, workspace layout and kernel
+// launches.  Every entry point validates its arguments on the host, returns a
+// negative status without launching when they are wrong, and otherwise
+// enqueues its kernels on the caller's stream.
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "cudaTypedefs.h"
+
+namespace se {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+}  // namespace
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+    int v = g_sms[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 1;
+        g_sms[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int head_dim) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode || rows <= 0) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace se
+
+using namespace se;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+bool group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (!ws || !aligned(ws, 256) || ws_bytes < need) return SE_ERR_WORKSPACE;
+    return SE_OK;
+}
+
+int check_paged(const se_paged_kv* kv, bool need_meta) {
+    if (!kv || !kv->k || !kv->v || !kv->block_table || !kv->ctx_len) return SE_ERR_INVALID_ARG;
+    if (need_meta && !kv->meta) return SE_ERR_INVALID_ARG;
+    if (kv->page_size != SE_PAGE_SIZE || !head_dim_ok(kv->head_dim)) return SE_ERR_UNSUPPORTED;
+    if (kv->num_kv_heads <= 0 || kv->num_pages <= 0 || kv->max_pages_per_seq <= 0)
+        return SE_ERR_INVALID_ARG;
+    if (!aligned(kv->k, 16) || !aligned(kv->v, 16) || (kv->meta && !aligned(kv->meta, 16)))
+        return SE_ERR_INVALID_ARG;
+    if ((int64_t)kv->num_pages * kv->num_kv_heads * SE_PAGE_SIZE > INT32_MAX)
+        return SE_ERR_UNSUPPORTED;
+    return SE_OK;
+}
+
+int check_varlen(const se_varlen_kv* kv) {
+    if (!kv || !kv->k || !kv->v || !kv->pos || !kv->seg_off || !kv->seg_len || !kv->seq_len)
+        return SE_ERR_INVALID_ARG;
+    if (!head_dim_ok(kv->head_dim)) return SE_ERR_UNSUPPORTED;
+    if (kv->num_kv_heads <= 0 || kv->seg_cap < 0 || kv->total_rows <= 0) return SE_ERR_INVALID_ARG;
+    if (!aligned(kv->k, 16) || !aligned(kv->v, 16)) return SE_ERR_INVALID_ARG;
+    return SE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SE_OK : SE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* se_status_str(int status) {
+    switch (status) {
+        case SE_OK: return "ok";
+        case SE_ERR_INVALID_ARG: return "invalid argument (null pointer, bad size or stride)";
+        case SE_ERR_UNSUPPORTED: return "unsupported shape";
+        case SE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case SE_ERR_CUDA: return "CUDA runtime error";
+        case SE_ERR_CAPACITY: return "output buffer too small";
+        default: return "unknown status";
+    }
+}
+
+int se_version(void) { return 1; }
+
+size_t se_small_workspace(void) { return 256; }
+
+size_t se_quest_select_workspace(int batch, int num_kv_heads, int max_pages_per_seq) {
+    if (batch < 0 || num_kv_heads <= 0 || max_pages_per_seq < 0) return 0;
+    return 256 + align256((size_t)batch * num_kv_heads * max_pages_per_seq * sizeof(float));
+}
+
+size_t se_sparse_decode_workspace(int num_units, int group_size, int head_dim, int max_splits) {
+    if (num_units < 0 || group_size <= 0 || head_dim <= 0 || max_splits <= 0) return 0;
+    return decode_ws_bytes(num_units, group_size, head_dim, max_splits);
+}
+
+int se_page_meta_build(const se_paged_kv* kv, int batch, void* ws, size_t ws_bytes,
+                       se_stream_t stream) {
+    int rc = check_paged(kv, true);
+    if (rc) return rc;
+    if (batch < 0) return SE_ERR_INVALID_ARG;
+    if ((rc = check_ws(ws, ws_bytes, se_small_workspace()))) return rc;
+    return cuda_status(launch_page_meta_build(*kv, batch, static_cast<int*>(ws),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int se_kv_append(const se_paged_kv* kv, const void* k_new, const void* v_new, int batch, void* ws,
+                 size_t ws_bytes, se_stream_t stream) {
+    int rc = check_paged(kv, true);
+    if (rc) return rc;
+    if (batch < 0 || (batch > 0 && (!k_new || !v_new))) return SE_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SE_ERR_INVALID_ARG;
+    if ((rc = check_ws(ws, ws_bytes, se_small_workspace()))) return rc;
+    return cuda_status(launch_kv_append(*kv, k_new, v_new, batch, static_cast<int*>(ws),
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int se_quest_select(const se_paged_kv* kv, const void* q, int batch, int num_q_heads,
+                    const int32_t* budget_tokens, int32_t* sel_pages, int32_t* n_sel,
+                    const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream) {
+    int rc = check_paged(kv, true);
+    if (rc) return rc;
+    if (batch < 0 || num_q_heads <= 0) return SE_ERR_INVALID_ARG;
+    if (num_q_heads % kv->num_kv_heads || !group_ok(num_q_heads / kv->num_kv_heads))
+        return SE_ERR_UNSUPPORTED;
+    if (batch > 0 && (!q || !budget_tokens || !sel_pages || !n_sel || !view || !view->chunk_row ||
+                      !view->n_tokens))
+        return SE_ERR_INVALID_ARG;
+    if (!aligned(q, 16)) return SE_ERR_INVALID_ARG;
+    if (view && view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
+    if (view && view->max_chunks < kv->max_pages_per_seq) return SE_ERR_CAPACITY;
+    if ((rc = check_ws(ws, ws_bytes,
+                       se_quest_select_workspace(batch, kv->num_kv_heads, kv->max_pages_per_seq))))
+        return rc;
+    float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
+    return cuda_status(launch_quest_select(*kv, q, batch, num_q_heads, budget_tokens, sel_pages,
+                                           n_sel, *view, scores, static_cast<int*>(ws),
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int se_view_from_segments(const se_varlen_kv* kv, int batch, const se_view* view, void* ws,
+                          size_t ws_bytes, se_stream_t stream) {
+    int rc = check_varlen(kv);
+    if (rc) return rc;
+    if (batch < 0 || !view || !view->chunk_row || !view->n_tokens) return SE_ERR_INVALID_ARG;
+    if (view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
+    if ((int64_t)view->max_chunks * SE_PAGE_SIZE < kv->seg_cap) return SE_ERR_CAPACITY;
+    if ((rc = check_ws(ws, ws_bytes, se_small_workspace()))) return rc;
+    return cuda_status(launch_view_from_segments(*kv, batch, *view, static_cast<int*>(ws),
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int se_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows, const se_view* view,
+                     const void* q, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                     float scale, const se_decode_opts* opts, void* out, float* lse, void* ws,
+                     size_t ws_bytes, se_stream_t stream) {
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0) return SE_ERR_INVALID_ARG;
+    if (!head_dim_ok(head_dim)) return SE_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads || !group_ok(num_q_heads / num_kv_heads))
+        return SE_ERR_UNSUPPORTED;
+    if (batch == 0) return SE_OK;
+    if (!k_rows || !v_rows || !view || !view->chunk_row || !view->n_tokens || !q || !out)
+        return SE_ERR_INVALID_ARG;
+    if (total_rows <= 0 || total_rows > INT32_MAX) return SE_ERR_INVALID_ARG;
+    if (!aligned(k_rows, 16) || !aligned(v_rows, 16) || !aligned(q, 16) || !aligned(out, 4))
+        return SE_ERR_INVALID_ARG;
+    if (view->num_units != batch * num_kv_heads || view->max_chunks <= 0) return SE_ERR_INVALID_ARG;
+    const int G = num_q_heads / num_kv_heads;
+    se_decode_opts o = {0, SE_MAX_SPLITS, nullptr, 0, nullptr, nullptr};
+    if (opts) {
+        o = *opts;
+        if (o.max_splits == 0) o.max_splits = SE_MAX_SPLITS;
+    }
+    if (o.out_dtype != 0 && o.out_dtype != 1) return SE_ERR_INVALID_ARG;
+    if (o.max_splits < 1 || o.max_splits > SE_MAX_SPLITS) return SE_ERR_INVALID_ARG;
+    if (o.logits_out && o.logits_stride < (int64_t)view->max_chunks * SE_PAGE_SIZE)
+        return SE_ERR_CAPACITY;
+    const int units = batch * num_kv_heads;
+    int rc = check_ws(ws, ws_bytes, decode_ws_bytes(units, G, head_dim, o.max_splits));
+    if (rc) return rc;
+    const DecodeWs w = decode_ws_carve(ws, units, G, head_dim, o.max_splits);
+    return cuda_status(launch_sparse_decode(
+        k_rows, v_rows, total_rows, *view, q, batch, num_q_heads, num_kv_heads, head_dim, scale,
+        o.out_dtype, o.max_splits, o.logits_out, o.logits_stride,
+        static_cast<cudaEvent_t>(o.ev_kernel_begin), static_cast<cudaEvent_t>(o.ev_kernel_end), out,
+        lse, w, static_cast<cudaStream_t>(stream)));
+}
+
+int se_varlen_append(const se_varlen_kv* kv, const void* k_new, const void* v_new, int batch,
+                     void* ws, size_t ws_bytes, se_stream_t stream) {
+    int rc = check_varlen(kv);
+    if (rc) return rc;
+    if (batch < 0 || (batch > 0 && (!k_new || !v_new))) return SE_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SE_ERR_INVALID_ARG;
+    if ((rc = check_ws(ws, ws_bytes, se_small_workspace()))) return rc;
+    return cuda_status(launch_varlen_append(*kv, k_new, v_new, batch, static_cast<int*>(ws),
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+// Not yet implemented: SnapKV compaction and the H2O step.
+size_t se_snapkv_workspace(int, int, int, int, int) { return 256; }
+size_t se_h2o_workspace(int, int, int, int, int) { return 256; }
+int se_snapkv_compact(const se_paged_kv*, const void*, int, int, int, int, int, int, float,
+                      const se_varlen_kv*, void*, size_t, se_stream_t) {
+    return SE_ERR_UNSUPPORTED;
+}
+int se_h2o_step(const se_h2o_state*, const void*, const void*, const void*, int, int, float, int,
+                void*, float*, int32_t*, void*, size_t, se_stream_t) {
+    return SE_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,582 @@
+// Split-K GQA decode attention over an AttentionView, and its log-sum-exp merge.
+//
+// The attention reads only the rows the view exposes ("SparseEngine：稀疏优先推理
+// 引擎", section "方法 / 关键模块": AttentionView exposes the selected
+// positions in one format, so methods need no kernel changes; tokendh.com
+// article on SparseEngine, section "把边界划在'生命周期'上").
+//
+// Design (sm_103a):
+//  * plan_kernel (1 CTA) cuts every unit's chunk list into pieces of about equal
+//    size (at most max_splits per unit) and writes a work list.
+//  * decode_kernel is persistent: one producer warp streams each 16-row K and V
+//    chunk into a ring of shared-memory stages with 2-D TMA loads (128B swizzle,
+//    mbarrier completion); consumer warp w owns the stages s with s % 4 == w.  Per
+//    16-token chunk a warp computes S^T = K Q^T (tokens as M=16, the GQA group
+//    as N=8) with ldmatrix + mma.sync.m16n8k16 (bf16 -> fp32), an online
+//    softmax in the exp2 domain, transposes P in registers (movmatrix) and
+//    accumulates O^T = V^T P^T (head_dim as M) with ldmatrix.trans + mma.
+//    At the end of a piece the four warps merge through shared memory; a unit
+//    cut into one piece is written directly, others go to fp32 partials.
+//  * combine_kernel merges the partials of multi-piece units by their LSE.
+#include "common.cuh"
+#include "internal.h"
+
+namespace se {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D, int NT>
+struct DecShape {
+    static constexpr int kBoxes = D / 64;                  // 64-column TMA boxes per chunk
+    static constexpr int kChunkBytes = kBoxes * 2048;      // 16 rows x D bf16
+    static constexpr int kStageBytes = 2 * kChunkBytes;    // K chunk then V chunk
+    // Stage s is always consumed by warp s % 4 (kStages is a multiple of 4), so a
+    // warp never waits on a stage more than one phase ahead of its own use.
+    static constexpr int kStages = D == 64 ? 16 : 8;
+    static_assert(kStages % kConsumerWarps == 0, "stage ownership needs kStages % 4 == 0");
+    static constexpr int kHeads = NT * 8;                  // padded group
+    static constexpr int kMergeFloats = kConsumerWarps * kHeads * (D + 2);
+    static constexpr size_t kSmem = 1024 /* alignment slack */ + (size_t)kStages * kStageBytes +
+                                    (size_t)kStages * 16 /* full, empty */ +
+                                    (size_t)kStages * 4 /* ntok */ + 16 /* abort */ +
+                                    (size_t)kMergeFloats * 4;
+};
+
+struct DecodeParams {
+    const int32_t* chunk_row;
+    const int32_t* n_tokens;
+    int max_chunks;
+    const uint16_t* q;
+    int Hq, Hkv, G;
+    float scale, scale_log2;
+    const int4* items;
+    const int* n_items;
+    float* o_part;
+    float* lse_part;
+    void* out;
+    int out_f32;
+    float* lse_out;
+    float* logits_out;
+    int logits_stride;
+    int64_t total_rows;
+    int* status;
+};
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ int unit_tokens(const DecodeParams& p, int u) {
+    int n = p.n_tokens[u];
+    const int lim = p.max_chunks * kPage;
+    if (n < 0 || n > lim) {
+        flag(p.status, SE_DEV_BAD_LENGTH);
+        n = n < 0 ? 0 : lim;
+    }
+    return n;
+}
+
+// TWO_TERM: P is fed to the PV product as bf16 hi + bf16 lo (about 16
+// mantissa bits) for the fp32-output mode; otherwise P is rounded once to bf16.
+template <int D, int NT, bool TWO_TERM>
+__global__ void __launch_bounds__(kDecodeThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                  const DecodeParams p) {
+    using S = DecShape<D, NT>;
+    constexpr int NS = S::kStages;
+    constexpr int KSTEPS = D / 16;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(stages + NS * S::kStageBytes);
+    uint64_t* empty = full + NS;
+    int* stage_ntok = reinterpret_cast<int*>(empty + NS);
+    volatile int* abort_flag = stage_ntok + NS;
+    float* merge = reinterpret_cast<float*>(stage_ntok + NS + 4);   // 16-byte aligned
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int n_items = *p.n_items;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------ producer ------------------------------
+        if (lane != 0) return;
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        uint32_t seq = 0;
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+            const int4 item = p.items[it];
+            const int u = item.x;
+            const int ntok = unit_tokens(p, u);
+            const int32_t* crow = p.chunk_row + (int64_t)u * p.max_chunks;
+            for (int c = item.y; c < item.z; ++c, ++seq) {
+                const int s = seq % NS;
+                const uint32_t ph = (seq / NS) & 1;
+                if (!*abort_flag && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+                    *abort_flag = 1;
+                    flag(p.status, SE_DEV_TIMEOUT);
+                }
+                const int row = crow[c];
+                int cnt = min(kPage, ntok - c * kPage);
+                if (row < 0 || (int64_t)row >= p.total_rows) {
+                    flag(p.status, SE_DEV_BAD_INDEX);
+                    cnt = 0;
+                }
+                stage_ntok[s] = cnt;
+                if (cnt > 0 && !*abort_flag) {
+                    uint8_t* kdst = stages + s * S::kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+#pragma unroll
+                    for (int bx = 0; bx < S::kBoxes; ++bx) {
+                        tma_load_2d(kdst + bx * 2048, &tk, &full[s], 64 * bx, row);
+                        tma_load_2d(kdst + S::kChunkBytes + bx * 2048, &tv, &full[s], 64 * bx, row);
+                    }
+                } else {
+                    mbar_arrive(&full[s]);
+                }
+            }
+        }
+        // Drain: every copy issued by this CTA lands before the CTA may exit.
+        const uint32_t first = seq > (uint32_t)NS ? seq - NS : 0;
+        volatile int never = 0;
+        for (uint32_t q2 = first; q2 < seq; ++q2) mbar_wait(&full[q2 % NS], (q2 / NS) & 1, &never);
+        return;
+    }
+
+    // -------------------------------- consumers --------------------------------
+    const int r = lane >> 2, cq = lane & 3;
+    const int ctid = threadIdx.x;                          // 0..127
+    const int G = p.G;
+    float* mw = merge;                                      // [4][kHeads]
+    float* lw = merge + kConsumerWarps * S::kHeads;         // [4][kHeads]
+    float* ow = merge + 2 * kConsumerWarps * S::kHeads;     // [4][kHeads][D]
+    // ldmatrix lane roles
+    const int lj = lane >> 3, lr = lane & 7;
+    const int k_tok = (lj & 1) * 8 + lr, k_dof = (lj >> 1) * 8;   // K as A (token x d)
+    const int v_tok = (lj >> 1) * 8 + lr, v_dof = (lj & 1) * 8;   // V^T as A (d x token)
+
+    uint32_t seq = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int4 item = p.items[it];
+        const int u = item.x;
+        const int b = u / p.Hkv, h = u % p.Hkv;
+        const int ntok = unit_tokens(p, u);
+
+        uint32_t qf[KSTEPS][NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int g = nt * 8 + r;
+            const uint16_t* qrow = p.q + ((int64_t)b * p.Hq + h * G + min(g, G - 1)) * D;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const uint32_t x0 = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * cq);
+                const uint32_t x1 = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * cq);
+                qf[kk][nt][0] = g < G ? x0 : 0u;
+                qf[kk][nt][1] = g < G ? x1 : 0u;
+            }
+        }
+        float m[NT][2], l[NT][2], o[KSTEPS][NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+        }
+
+        for (int c = item.y; c < item.z; ++c, ++seq) {
+            if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
+            const int s = seq % NS;
+            const uint32_t ph = (seq / NS) & 1;
+            if (!*abort_flag && !mbar_wait(&full[s], ph, abort_flag)) {
+                *abort_flag = 1;
+                flag(p.status, SE_DEV_TIMEOUT);
+            }
+            const int cnt = *abort_flag ? 0 : stage_ntok[s];
+            if (cnt > 0) {
+                uint8_t* kb = stages + s * S::kStageBytes;
+                uint8_t* vb = kb + S::kChunkBytes;
+                if (cnt < kPage) {
+                    // rows past the valid count may hold anything: zero them in V
+                    // (P is 0 there, but 0 * NaN would not be)
+                    const int per_row = S::kBoxes * 8;
+                    for (int idx = lane; idx < (kPage - cnt) * per_row; idx += 32) {
+                        const int row = cnt + idx / per_row, rem = idx % per_row;
+                        *reinterpret_cast<uint4*>(vb + (rem >> 3) * 2048 + row * 128 + (rem & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                // ---- S^T = K Q^T ----
+                float sacc[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+                const uint32_t kbase = smem_u32(kb);
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int d = kk * 16 + k_dof;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kbase + (d >> 6) * 2048 + swz128(k_tok, (d & 63) >> 3), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_16816(sacc[nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                }
+                // ---- mask, optional logits, online softmax (exp2 domain) ----
+                const int tok_base = c * kPage;
+                float pr[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float sv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tok = r + ((e >> 1) << 3);
+                        sv[e] = tok < cnt ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+                        if (p.logits_out != nullptr && tok < cnt) {
+                            const int g = nt * 8 + 2 * cq + (e & 1);
+                            if (g < G)
+                                p.logits_out[((int64_t)u * p.logits_stride + tok_base + tok) * G + g] =
+                                    sacc[nt][e] * p.scale;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float mx = fmaxf(sv[j], sv[j + 2]);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float m_new = fmaxf(m[nt][j], mx);
+                        const float base = m_new == -INFINITY ? 0.f : m_new;
+                        const float alpha = exp2f(m[nt][j] - base);
+                        const float p0 = exp2f(sv[j] - base), p1 = exp2f(sv[j + 2] - base);
+                        l[nt][j] = l[nt][j] * alpha + p0 + p1;
+                        m[nt][j] = m_new;
+                        pr[nt][j] = p0;
+                        pr[nt][j + 2] = p1;
+#pragma unroll
+                        for (int mt = 0; mt < KSTEPS; ++mt) {
+                            o[mt][nt][j] *= alpha;
+                            o[mt][nt][j + 2] *= alpha;
+                        }
+                    }
+                }
+                // ---- O^T += V^T P^T ----
+                uint32_t pb[NT][2], pbl[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint32_t x0 = pack_bf16(pr[nt][0], pr[nt][1]);
+                    const uint32_t x1 = pack_bf16(pr[nt][2], pr[nt][3]);
+                    pb[nt][0] = movmatrix_t(x0);
+                    pb[nt][1] = movmatrix_t(x1);
+                    if (TWO_TERM) {
+                        const uint32_t y0 = pack_bf16(pr[nt][0] - bf_lo(x0), pr[nt][1] - bf_hi(x0));
+                        const uint32_t y1 = pack_bf16(pr[nt][2] - bf_lo(x1), pr[nt][3] - bf_hi(x1));
+                        pbl[nt][0] = movmatrix_t(y0);
+                        pbl[nt][1] = movmatrix_t(y1);
+                    }
+                }
+                const uint32_t vbase = smem_u32(vb);
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const int d = mt * 16 + v_dof;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(vbase + (d >> 6) * 2048 + swz128(v_tok, (d & 63) >> 3), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_16816(o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                        if (TWO_TERM) mma_16816(o[mt][nt], a0, a1, a2, a3, pbl[nt][0], pbl[nt][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        // ---- merge the four warps' partial softmax states ----
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float x = l[nt][j];
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                x += __shfl_xor_sync(0xffffffffu, x, 8);
+                x += __shfl_xor_sync(0xffffffffu, x, 16);
+                l[nt][j] = x;
+            }
+        if (r == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    mw[warp * S::kHeads + nt * 8 + 2 * cq + j] = m[nt][j];
+                    lw[warp * S::kHeads + nt * 8 + 2 * cq + j] = l[nt][j];
+                }
+        }
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int head = nt * 8 + 2 * cq + (e & 1);
+                    const int d = mt * 16 + r + ((e >> 1) << 3);
+                    ow[(warp * S::kHeads + head) * D + d] = o[mt][nt][e];
+                }
+        consumer_bar();
+        const int slot = item.w;
+        for (int idx = ctid; idx < G * D; idx += kConsumerWarps * 32) {
+            const int g = idx / D, d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w * S::kHeads + g]);
+            float L = 0.f, O = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float f = exp2f(mw[w * S::kHeads + g] - M);
+                    L += lw[w * S::kHeads + g] * f;
+                    O += ow[(w * S::kHeads + g) * D + d] * f;
+                }
+            }
+            const float val = L > 0.f ? O / L : 0.f;
+            const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
+            const int64_t hq = (int64_t)b * p.Hq + h * G + g;
+            if (slot < 0) {
+                if (p.out_f32)
+                    static_cast<float*>(p.out)[hq * D + d] = val;
+                else
+                    static_cast<uint16_t*>(p.out)[hq * D + d] = to_bf16_bits(val);
+                if (d == 0 && p.lse_out) p.lse_out[hq] = lse2 * kLn2;
+            } else {
+                p.o_part[((int64_t)slot * G + g) * D + d] = val;
+                if (d == 0) p.lse_part[(int64_t)slot * G + g] = lse2;
+            }
+        }
+        consumer_bar();
+    }
+}
+
+// One CTA: per unit, nc = ceil(n_tokens/16) chunks are cut into pieces of
+// cps chunks, where the piece size aims at `target_items` pieces overall (at
+// least `min_chunks` chunks each) and each unit has at most max_splits pieces.
+__global__ void __launch_bounds__(1024)
+    plan_kernel(const int32_t* __restrict__ n_tokens, int units, int max_chunks, int max_splits,
+                int target_items, int min_chunks, int4* __restrict__ items,
+                int2* __restrict__ unit_items, int* __restrict__ n_items, int* status) {
+    __shared__ int tmp[33];
+    const int lim = max_chunks * kPage;
+    auto chunks_of = [&](int u) {
+        int n = n_tokens[u];
+        n = n < 0 ? 0 : (n > lim ? lim : n);
+        return (n + kPage - 1) / kPage;
+    };
+    int total = 0;
+    for (int base = 0; base < units; base += blockDim.x) {
+        const int u = base + threadIdx.x;
+        int t;
+        block_exclusive_scan(u < units ? chunks_of(u) : 0, tmp, &t);
+        total += t;
+    }
+    const int C = max(min_chunks, (total + target_items - 1) / max(1, target_items));
+    int run = 0;
+    for (int base = 0; base < units; base += blockDim.x) {
+        const int u = base + threadIdx.x;
+        int nc = 0, splits = 0, cps = 1;
+        if (u < units) {
+            nc = chunks_of(u);
+            splits = nc == 0 ? 1 : min(max_splits, (nc + C - 1) / C);
+            cps = nc == 0 ? 1 : (nc + splits - 1) / splits;
+            splits = nc == 0 ? 1 : (nc + cps - 1) / cps;
+        }
+        int t;
+        const int off = run + block_exclusive_scan(splits, tmp, &t);
+        if (u < units) {
+            unit_items[u] = make_int2(off, splits);
+            for (int k = 0; k < splits; ++k)
+                items[off + k] = make_int4(u, k * cps, min(nc, (k + 1) * cps), splits == 1 ? -1 : off + k);
+        }
+        run += t;
+    }
+    if (threadIdx.x == 0) *n_items = run;
+}
+
+// grid units*G, block 128: out = sum_s w_s o_s / sum_s w_s with w_s = 2^(lse_s - max).
+__global__ void __launch_bounds__(128)
+    combine_kernel(const int2* __restrict__ unit_items, const float* __restrict__ o_part,
+                   const float* __restrict__ lse_part, int Hq, int Hkv, int G, int D, int out_f32,
+                   void* out, float* lse_out) {
+    __shared__ float w[SE_MAX_SPLITS];
+    __shared__ float s_M, s_L;
+    const int u = blockIdx.x / G, g = blockIdx.x % G;
+    const int2 ui = unit_items[u];
+    if (ui.y <= 1) return;
+    const int n = min(ui.y, SE_MAX_SPLITS);
+    if (threadIdx.x < 32) {
+        float M = -INFINITY;
+        for (int s = threadIdx.x; s < n; s += 32) M = fmaxf(M, lse_part[(int64_t)(ui.x + s) * G + g]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f;
+        for (int s = threadIdx.x; s < n; s += 32) {
+            const float x = lse_part[(int64_t)(ui.x + s) * G + g];
+            const float f = M == -INFINITY ? 0.f : exp2f(x - M);
+            w[s] = f;
+            L += f;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (threadIdx.x == 0) {
+            s_M = M;
+            s_L = L;
+        }
+    }
+    __syncthreads();
+    const float L = s_L;
+    const int b = u / Hkv, h = u % Hkv;
+    const int64_t hq = (int64_t)b * Hq + h * G + g;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < n; ++s) acc += w[s] * o_part[((int64_t)(ui.x + s) * G + g) * D + d];
+        const float val = L > 0.f ? acc / L : 0.f;
+        if (out_f32)
+            static_cast<float*>(out)[hq * D + d] = val;
+        else
+            static_cast<uint16_t*>(out)[hq * D + d] = to_bf16_bits(val);
+    }
+    if (threadIdx.x == 0 && lse_out) lse_out[hq] = L > 0.f ? (s_M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+template <int D, int NT, bool TWO>
+cudaError_t run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                       int grid, cudaStream_t s) {
+    using S = DecShape<D, NT>;
+    auto kern = decode_kernel<D, NT, TWO>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(S::kSmem));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kDecodeThreads, S::kSmem, s>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+template <int D, int NT>
+int ctas_per_sm() {
+    using S = DecShape<D, NT>;
+    return S::kSmem * 2 + 2048 <= 228 * 1024 ? 2 : 1;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+size_t decode_ws_bytes(int num_units, int G, int D, int max_splits) {
+    const size_t items = (size_t)num_units * max_splits;
+    return 256 + align256(items * sizeof(int4)) + align256((size_t)num_units * sizeof(int2)) +
+           align256(items * G * sizeof(float)) + align256(items * G * D * sizeof(float));
+}
+
+DecodeWs decode_ws_carve(void* ws, int num_units, int G, int D, int max_splits) {
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const size_t items = (size_t)num_units * max_splits;
+    DecodeWs w;
+    w.status = reinterpret_cast<int*>(base);
+    w.n_items = reinterpret_cast<int*>(base + 16);
+    size_t off = 256;
+    w.items = reinterpret_cast<int4*>(base + off);
+    off += align256(items * sizeof(int4));
+    w.unit_items = reinterpret_cast<int2*>(base + off);
+    off += align256((size_t)num_units * sizeof(int2));
+    w.lse_part = reinterpret_cast<float*>(base + off);
+    off += align256(items * G * sizeof(float));
+    w.o_part = reinterpret_cast<float*>(base + off);
+    return w;
+}
+
+cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
+                                 const se_view& view, const void* q, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, float scale, int out_dtype,
+                                 int max_splits, float* logits_out, int logits_stride,
+                                 cudaEvent_t ev_begin, cudaEvent_t ev_end, void* out, float* lse,
+                                 const DecodeWs& w, cudaStream_t s) {
+    const int units = batch * num_kv_heads;
+    if (units == 0) return cudaSuccess;
+    const int G = num_q_heads / num_kv_heads;
+    const int NT = G > 8 ? 2 : 1;
+    CUtensorMap tk, tv;
+    if (!encode_rows_map(&tk, k_rows, total_rows, head_dim) ||
+        !encode_rows_map(&tv, v_rows, total_rows, head_dim))
+        return cudaErrorInvalidValue;
+
+    const int cps = head_dim == 64 ? ctas_per_sm<64, 1>()
+                                   : (NT == 1 ? ctas_per_sm<128, 1>() : ctas_per_sm<128, 2>());
+    const int max_items = units * max_splits;
+    const int grid = max(1, min(max_items, num_sms() * cps));
+
+    plan_kernel<<<1, 1024, 0, s>>>(view.n_tokens, units, view.max_chunks, max_splits, grid, 4,
+                                   w.items, w.unit_items, w.n_items, w.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    DecodeParams p;
+    p.chunk_row = view.chunk_row;
+    p.n_tokens = view.n_tokens;
+    p.max_chunks = view.max_chunks;
+    p.q = static_cast<const uint16_t*>(q);
+    p.Hq = num_q_heads;
+    p.Hkv = num_kv_heads;
+    p.G = G;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.items = w.items;
+    p.n_items = w.n_items;
+    p.o_part = w.o_part;
+    p.lse_part = w.lse_part;
+    p.out = out;
+    p.out_f32 = out_dtype == 1;
+    p.lse_out = lse;
+    p.logits_out = logits_out;
+    p.logits_stride = logits_stride;
+    p.total_rows = total_rows;
+    p.status = w.status;
+
+    if (ev_begin) {
+        e = cudaEventRecord(ev_begin, s);
+        if (e != cudaSuccess) return e;
+    }
+    const bool two = out_dtype == 1;
+    if (head_dim == 64) {
+        e = NT == 1 ? (two ? run_decode<64, 1, true>(tk, tv, p, grid, s)
+                           : run_decode<64, 1, false>(tk, tv, p, grid, s))
+                    : (two ? run_decode<64, 2, true>(tk, tv, p, grid, s)
+                           : run_decode<64, 2, false>(tk, tv, p, grid, s));
+    } else {
+        e = NT == 1 ? (two ? run_decode<128, 1, true>(tk, tv, p, grid, s)
+                           : run_decode<128, 1, false>(tk, tv, p, grid, s))
+                    : (two ? run_decode<128, 2, true>(tk, tv, p, grid, s)
+                           : run_decode<128, 2, false>(tk, tv, p, grid, s));
+    }
+    if (e != cudaSuccess) return e;
+    if (ev_end) {
+        e = cudaEventRecord(ev_end, s);
+        if (e != cudaSuccess) return e;
+    }
+    combine_kernel<<<units * G, 128, 0, s>>>(w.unit_items, w.o_part, w.lse_part, num_q_heads,
+                                             num_kv_heads, G, head_dim, out_dtype == 1, out, lse);
+    return cudaGetLastError();
+}
+
+}  // namespace se

@@ -1,0 +1,52 @@
+// Host-side launch interface between the C ABI layer (api.cu) and the kernel
+// translation units.  Every launcher enqueues on `stream` and returns the
+// launch's cudaError_t; arguments were validated by the caller.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sparse_engine.h"
+
+namespace se {
+
+int num_sms();                       // SMs of the current device (cached)
+
+// ---- meta.cu ----
+cudaError_t launch_page_meta_build(const se_paged_kv& kv, int batch, int* status, cudaStream_t s);
+cudaError_t launch_kv_append(const se_paged_kv& kv, const void* k_new, const void* v_new,
+                             int batch, int* status, cudaStream_t s);
+cudaError_t launch_varlen_append(const se_varlen_kv& kv, const void* k_new, const void* v_new,
+                                 int batch, int* status, cudaStream_t s);
+cudaError_t launch_view_from_segments(const se_varlen_kv& kv, int batch, const se_view& view,
+                                      int* status, cudaStream_t s);
+
+// ---- quest.cu ----
+cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch, int num_q_heads,
+                                const int32_t* budget, int32_t* sel_pages, int32_t* n_sel,
+                                const se_view& view, float* scores, int* status, cudaStream_t s);
+
+// ---- decode.cu ----
+struct DecodeWs {
+    int* status;
+    int* n_items;
+    int4* items;          // [num_units * max_splits]
+    int2* unit_items;     // [num_units]: (first item, item count)
+    float* lse_part;      // [num_units * max_splits][G]   (log2 domain)
+    float* o_part;        // [num_units * max_splits][G][D] (normalised)
+};
+size_t decode_ws_bytes(int num_units, int G, int D, int max_splits);
+DecodeWs decode_ws_carve(void* ws, int num_units, int G, int D, int max_splits);
+cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
+                                 const se_view& view, const void* q, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, float scale, int out_dtype,
+                                 int max_splits, float* logits_out, int logits_stride,
+                                 cudaEvent_t ev_begin, cudaEvent_t ev_end, void* out, float* lse,
+                                 const DecodeWs& w, cudaStream_t s);
+
+// ---- tensor maps (api.cu) ----
+// 2-D bf16 map over [rows][head_dim] with 16-row x 64-column boxes, 128B swizzle.
+bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int head_dim);
+
+}  // namespace se

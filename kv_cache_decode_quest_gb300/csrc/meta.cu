@@ -1,0 +1,215 @@
+// Cache maintenance kernels: Quest page summaries (channel-wise key min/max per
+// (page, KV head)), the decode-step appends for the paged and the
+// variable-length caches, and the AttentionView of whole varlen segments.
+//
+// The page summary is Quest's "summary index" kept beside the full history
+// (tokendh.com article on SparseEngine, section "历史太长,会撑爆什么");
+// pages of 16 tokens with a token->page table follow the paged KV layout of
+// "长程 agent 把显存撑爆以后", section "四、为什么进不了 vLLM 一类的引擎".
+#include "common.cuh"
+#include "internal.h"
+
+namespace se {
+namespace {
+
+// Each task covers 8 channels (one 16-byte vector) of one KV head.
+struct Bf8 {
+    float x[8];
+};
+__device__ __forceinline__ Bf8 unpack8(uint4 w) {
+    Bf8 r;
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r.x[2 * i] = bf_lo(a[i]);
+        r.x[2 * i + 1] = bf_hi(a[i]);
+    }
+    return r;
+}
+__device__ __forceinline__ uint4 pack8(const Bf8& v) {
+    // Values are bf16-representable (min/max of bf16 inputs): rounding is exact.
+    return make_uint4(pack_bf16(v.x[0], v.x[1]), pack_bf16(v.x[2], v.x[3]),
+                      pack_bf16(v.x[4], v.x[5]), pack_bf16(v.x[6], v.x[7]));
+}
+
+__global__ void page_meta_build_kernel(se_paged_kv kv, int* status) {
+    const int b = blockIdx.y, p = blockIdx.x;
+    const int H = kv.num_kv_heads, D = kv.head_dim, segs = D / 8;
+    int ctx = kv.ctx_len[b];
+    const int cap = kv.max_pages_per_seq * kPage;
+    if (ctx < 0 || ctx > cap) {
+        if (p == 0 && threadIdx.x == 0) flag(status, SE_DEV_BAD_LENGTH);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    const int n = (ctx + kPage - 1) / kPage;
+    if (p >= n) return;
+    const int phys = kv.block_table[(int64_t)b * kv.max_pages_per_seq + p];
+    if (phys < 0 || phys >= kv.num_pages) {
+        if (threadIdx.x == 0) flag(status, SE_DEV_BAD_INDEX);
+        return;
+    }
+    const int valid = min(kPage, ctx - p * kPage);
+    const uint4* K = static_cast<const uint4*>(kv.k);
+    uint4* M = static_cast<uint4*>(kv.meta);
+    for (int t = threadIdx.x; t < H * segs; t += blockDim.x) {
+        const int h = t / segs, sg = t % segs;
+        const int64_t row0 = ((int64_t)phys * H + h) * kPage;
+        Bf8 mn = unpack8(K[row0 * segs + sg]), mx = mn;
+        for (int r = 1; r < valid; ++r) {
+            const Bf8 x = unpack8(K[(row0 + r) * segs + sg]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mn.x[i] = fminf(mn.x[i], x.x[i]);
+                mx.x[i] = fmaxf(mx.x[i], x.x[i]);
+            }
+        }
+        const int64_t m0 = ((int64_t)phys * H + h) * 2;
+        M[m0 * segs + sg] = pack8(mn);
+        M[(m0 + 1) * segs + sg] = pack8(mx);
+    }
+}
+
+__global__ void kv_append_kernel(se_paged_kv kv, const uint4* k_new, const uint4* v_new,
+                                 int* status) {
+    const int b = blockIdx.x;
+    const int H = kv.num_kv_heads, D = kv.head_dim, segs = D / 8;
+    __shared__ int s_pos;
+    if (threadIdx.x == 0) s_pos = kv.ctx_len[b];
+    __syncthreads();
+    const int pos = s_pos;
+    const int p = pos / kPage, slot = pos % kPage;
+    bool ok = pos >= 0 && p < kv.max_pages_per_seq;
+    int phys = -1;
+    if (ok) {
+        phys = kv.block_table[(int64_t)b * kv.max_pages_per_seq + p];
+        if (phys < 0 || phys >= kv.num_pages) {
+            if (threadIdx.x == 0) flag(status, SE_DEV_BAD_INDEX);
+            ok = false;
+        }
+    } else if (threadIdx.x == 0) {
+        flag(status, pos < 0 ? SE_DEV_BAD_LENGTH : SE_DEV_CAPACITY);
+    }
+    if (ok) {
+        uint4* K = static_cast<uint4*>(kv.k);
+        uint4* V = static_cast<uint4*>(kv.v);
+        uint4* M = static_cast<uint4*>(kv.meta);
+        for (int t = threadIdx.x; t < H * segs; t += blockDim.x) {
+            const int h = t / segs, sg = t % segs;
+            const uint4 kw = k_new[((int64_t)b * H + h) * segs + sg];
+            const uint4 vw = v_new[((int64_t)b * H + h) * segs + sg];
+            const int64_t row = ((int64_t)phys * H + h) * kPage + slot;
+            K[row * segs + sg] = kw;
+            V[row * segs + sg] = vw;
+            const int64_t m0 = ((int64_t)phys * H + h) * 2;
+            if (slot == 0) {
+                M[m0 * segs + sg] = kw;
+                M[(m0 + 1) * segs + sg] = kw;
+            } else {
+                Bf8 mn = unpack8(M[m0 * segs + sg]), mx = unpack8(M[(m0 + 1) * segs + sg]);
+                const Bf8 x = unpack8(kw);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    mn.x[i] = fminf(mn.x[i], x.x[i]);
+                    mx.x[i] = fmaxf(mx.x[i], x.x[i]);
+                }
+                M[m0 * segs + sg] = pack8(mn);
+                M[(m0 + 1) * segs + sg] = pack8(mx);
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && ok) kv.ctx_len[b] = pos + 1;
+}
+
+__global__ void varlen_append_kernel(se_varlen_kv kv, const uint4* k_new, const uint4* v_new,
+                                     int* status) {
+    const int b = blockIdx.x;
+    const int H = kv.num_kv_heads, D = kv.head_dim, segs = D / 8;
+    __shared__ int s_pos;
+    if (threadIdx.x == 0) s_pos = kv.seq_len[b];
+    __syncthreads();
+    const int pos = s_pos;
+    uint4* K = static_cast<uint4*>(kv.k);
+    uint4* V = static_cast<uint4*>(kv.v);
+    for (int t = threadIdx.x; t < H * segs; t += blockDim.x) {
+        const int h = t / segs, sg = t % segs;
+        const int u = b * H + h;
+        const int len = kv.seg_len[u];
+        const int off = kv.seg_off[u];
+        if (len < 0 || len >= kv.seg_cap) {
+            if (sg == 0) flag(status, len < 0 ? SE_DEV_BAD_LENGTH : SE_DEV_CAPACITY);
+            continue;
+        }
+        const int64_t row = (int64_t)off + len;
+        if (off < 0 || row >= kv.total_rows) {
+            if (sg == 0) flag(status, SE_DEV_BAD_INDEX);
+            continue;
+        }
+        K[row * segs + sg] = k_new[((int64_t)b * H + h) * segs + sg];
+        V[row * segs + sg] = v_new[((int64_t)b * H + h) * segs + sg];
+        if (sg == 0) {
+            kv.pos[row] = pos;
+            if (kv.score) kv.score[row] = 0.0f;
+        }
+    }
+    __syncthreads();
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        const int u = b * H + h;
+        const int len = kv.seg_len[u];
+        const int64_t row = (int64_t)kv.seg_off[u] + len;
+        if (len >= 0 && len < kv.seg_cap && kv.seg_off[u] >= 0 && row < kv.total_rows)
+            kv.seg_len[u] = len + 1;
+    }
+    if (threadIdx.x == 0) kv.seq_len[b] = pos + 1;
+}
+
+__global__ void view_segments_kernel(se_varlen_kv kv, se_view view, int* status) {
+    const int u = blockIdx.x;
+    int len = kv.seg_len[u];
+    const int lim = min(kv.seg_cap, view.max_chunks * kPage);
+    if (len < 0 || len > lim) {
+        if (threadIdx.x == 0) flag(status, SE_DEV_BAD_LENGTH);
+        len = len < 0 ? 0 : lim;
+    }
+    const int off = kv.seg_off[u];
+    const int nc = (len + kPage - 1) / kPage;
+    for (int c = threadIdx.x; c < nc; c += blockDim.x)
+        view.chunk_row[(int64_t)u * view.max_chunks + c] = off + c * kPage;
+    if (threadIdx.x == 0) view.n_tokens[u] = len;
+}
+
+}  // namespace
+
+cudaError_t launch_page_meta_build(const se_paged_kv& kv, int batch, int* status,
+                                   cudaStream_t s) {
+    if (batch == 0 || kv.max_pages_per_seq == 0) return cudaSuccess;
+    dim3 grid(kv.max_pages_per_seq, batch);
+    page_meta_build_kernel<<<grid, 128, 0, s>>>(kv, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(const se_paged_kv& kv, const void* k_new, const void* v_new,
+                             int batch, int* status, cudaStream_t s) {
+    if (batch == 0) return cudaSuccess;
+    kv_append_kernel<<<batch, 128, 0, s>>>(kv, static_cast<const uint4*>(k_new),
+                                           static_cast<const uint4*>(v_new), status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_append(const se_varlen_kv& kv, const void* k_new, const void* v_new,
+                                 int batch, int* status, cudaStream_t s) {
+    if (batch == 0) return cudaSuccess;
+    varlen_append_kernel<<<batch, 128, 0, s>>>(kv, static_cast<const uint4*>(k_new),
+                                               static_cast<const uint4*>(v_new), status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_view_from_segments(const se_varlen_kv& kv, int batch, const se_view& view,
+                                      int* status, cudaStream_t s) {
+    const int units = batch * kv.num_kv_heads;
+    if (units == 0) return cudaSuccess;
+    view_segments_kernel<<<units, 128, 0, s>>>(kv, view, status);
+    return cudaGetLastError();
+}
+
+}  // namespace se

@@ -1,0 +1,131 @@
+"""Device-side set-up and decode-step drivers for the synthetic workloads.
+
+A driver owns the caller-side buffers of one workload (caches, views,
+workspaces, per-step inputs) and issues the library's entry points for one
+decode step.  Set-up (placing the prefill cache into pages, building page
+summaries) happens once, outside any timed region.  All arithmetic of the
+path runs in the library's kernels; this module only moves bytes.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import binding as se
+from . import synth
+
+PAGE = synth.PAGE_SIZE
+
+
+def to_dev_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """Upload bf16 bit patterns (uint16) as a bfloat16 tensor."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device, non_blocking=False).view(torch.bfloat16)
+
+
+def paged_layout(seqs_k, seqs_v, lengths, block_table, num_pages, num_kv_heads, head_dim):
+    """Scatter per-sequence logical K/V ([Hkv][T][D] bf16 bits, first `lengths[b]`
+    tokens) into physical pages [num_pages][Hkv][16][D] by the block table."""
+    K = np.zeros((num_pages, num_kv_heads, PAGE, head_dim), dtype=np.uint16)
+    V = np.zeros_like(K)
+    for b, L in enumerate(lengths):
+        n = -(-int(L) // PAGE)
+        if n == 0:
+            continue
+        for src, dst in ((seqs_k[b], K), (seqs_v[b], V)):
+            blk = np.zeros((num_kv_heads, n * PAGE, head_dim), dtype=np.uint16)
+            blk[:, :L] = src[:, :L]
+            dst[block_table[b, :n]] = blk.reshape(num_kv_heads, n, PAGE, head_dim).transpose(1, 0, 2, 3)
+    return K, V
+
+
+class QuestRun:
+    """Paged KV + Quest selection + split-K decode, one appended token per step."""
+
+    def __init__(self, w: synth.QuestWorkload, inputs: dict, out_dtype: int = 0,
+                 max_splits: int | None = None, device="cuda"):
+        self.w = w
+        B, Hq, Hkv, D, S = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.steps
+        self.B, self.Hq, self.Hkv, self.D, self.S = B, Hq, Hkv, D, S
+        self.G = Hq // Hkv
+        self.scale = 1.0 / math.sqrt(D)
+        self.out_dtype = out_dtype
+        self.max_splits = max_splits or w.max_splits
+        ctx = np.asarray(w.ctx, dtype=np.int64)
+        pages = -(-(ctx + S) // PAGE)
+        bt, num_pages = synth.block_table(w.seed, w.name + "/block_table", pages)
+        self.block_table_np = bt
+        K, V = paged_layout(inputs["k"], inputs["v"], ctx, bt, num_pages, Hkv, D)
+        self.kv = se.PagedKV(
+            k=to_dev_bf16(K, device), v=to_dev_bf16(V, device),
+            meta=torch.zeros(num_pages, Hkv, 2, D, dtype=torch.bfloat16, device=device),
+            block_table=torch.from_numpy(bt).to(device),
+            ctx_len=torch.from_numpy(ctx.astype(np.int32)).to(device))
+        del K, V
+        # per-step inputs
+        self.q = to_dev_bf16(inputs["q"], device)                               # [S][B][Hq][D]
+        kn = np.stack([np.stack([inputs["k"][b][:, ctx[b] + s] for b in range(B)]) for s in range(S)])
+        vn = np.stack([np.stack([inputs["v"][b][:, ctx[b] + s] for b in range(B)]) for s in range(S)])
+        self.k_new = to_dev_bf16(kn, device)                                     # [S][B][Hkv][D]
+        self.v_new = to_dev_bf16(vn, device)
+        self.budget = torch.tensor([min(b, 2 ** 31 - 1) for b in w.budget], dtype=torch.int32,
+                                   device=device)
+        units = B * Hkv
+        maxp = bt.shape[1]
+        self.sel = torch.zeros(units, maxp, dtype=torch.int32, device=device)
+        self.n_sel = torch.zeros(units, dtype=torch.int32, device=device)
+        self.view = se.View.empty(units, maxp, device)
+        self.ws_small = se.workspace(se.se_small_workspace(), device)
+        self.ws_sel = se.workspace(se.se_quest_select_workspace(B, Hkv, maxp), device)
+        self.ws_dec = se.workspace(se.se_sparse_decode_workspace(units, self.G, D, self.max_splits),
+                                   device)
+        odt = torch.float32 if out_dtype == 1 else torch.bfloat16
+        self.out = torch.zeros(B, Hq, D, dtype=odt, device=device)
+        self.lse = torch.zeros(B, Hq, dtype=torch.float32, device=device)
+        se.se_page_meta_build(self.kv, B, self.ws_small)
+
+    def append(self, s: int):
+        se.se_kv_append(self.kv, self.k_new[s], self.v_new[s], self.B, self.ws_small)
+
+    def select(self, s: int):
+        se.se_quest_select(self.kv, self.q[s], self.B, self.Hq, self.budget, self.sel, self.n_sel,
+                           self.view, self.ws_sel)
+
+    def decode(self, s: int, out=None, lse=None, ev_begin=None, ev_end=None):
+        se.se_sparse_decode(self.kv.k, self.kv.v, self.view, self.q[s], self.B, self.Hq, self.Hkv,
+                            self.D, self.scale, self.out if out is None else out,
+                            self.lse if lse is None else lse, self.ws_dec,
+                            out_dtype=self.out_dtype, max_splits=self.max_splits,
+                            ev_begin=ev_begin, ev_end=ev_end)
+
+    def step(self, s: int, out=None, lse=None, ev_begin=None, ev_end=None):
+        """One decode step: append the step's token, select pages, attend."""
+        self.append(s)
+        self.select(s)
+        self.decode(s, out, lse, ev_begin, ev_end)
+
+    def status(self) -> int:
+        return se.status_word(self.ws_small) | se.status_word(self.ws_sel) | \
+            se.status_word(self.ws_dec)
+
+    def algorithmic_bytes(self, ctx_now: np.ndarray) -> dict:
+        """Bytes one step must move at least, given each sequence's length after
+        the append: page summaries of every candidate page (2*D*2 bytes per page
+        and KV head), K and V of every selected token (2*D*2 bytes per token and
+        KV head), q, the appended k/v, and the output."""
+        D, Hkv, Hq = self.D, self.Hkv, self.Hq
+        meta = sel = 0
+        for b, L in enumerate(ctx_now):
+            n = -(-int(L) // PAGE)
+            k = max(1, min(self.w.budget[b], 2 ** 31 - 1) // PAGE)
+            meta += max(0, n - 1) * Hkv * 2 * D * 2
+            if n <= k:
+                toks = int(L)
+            else:
+                toks = (k - 1) * PAGE + (int(L) - PAGE * (n - 1))
+            sel += toks * Hkv * 2 * D * 2
+        outb = 4 if self.out_dtype == 1 else 2
+        small = self.B * (Hq * D * 2 + 2 * Hkv * D * 2 + Hq * D * outb)
+        return {"meta": meta, "kv": sel, "small": small, "total": meta + sel + small}

@@ -1,0 +1,104 @@
+"""The C-ABI library builds, loads, exports every entry point that
+include/sparse_engine.h declares, and rejects bad arguments on the host
+(these calls return before any CUDA call, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kv_cache_decode_quest_gb300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "sparse_engine.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(se_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if not n.endswith("_t")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = declared_functions()
+    for n in ("se_quest_select", "se_sparse_decode", "se_snapkv_compact", "se_h2o_step"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_functions()) == set(binding.SIGNATURES)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.se_version() == 1
+    for rc in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(lib.se_status_str(rc), bytes)
+
+
+def test_workspace_sizes(lib):
+    assert lib.se_small_workspace() == 256
+    assert lib.se_quest_select_workspace(16, 4, 2052) >= 16 * 4 * 2052 * 4
+    assert lib.se_quest_select_workspace(16, 4, 2052) % 256 == 0
+    d = lib.se_sparse_decode_workspace(64, 8, 128, 64)
+    assert d >= 64 * 64 * 8 * 128 * 4 and d % 256 == 0
+
+
+def _paged(head_dim=128, page_size=16, nulls=False):
+    fake = None if nulls else 1 << 20       # never dereferenced: validation fails first
+    return binding.PagedKVC(fake, fake, fake, fake, fake, 10, 4, 4, head_dim, page_size)
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    ws = ctypes.c_void_p(1 << 20)
+    # null cache pointers
+    assert lib.se_page_meta_build(ctypes.byref(_paged(nulls=True)), 1, ws, 256, None) == -1
+    # unsupported head_dim / page size
+    assert lib.se_page_meta_build(ctypes.byref(_paged(head_dim=96)), 1, ws, 256, None) == -2
+    assert lib.se_page_meta_build(ctypes.byref(_paged(page_size=32)), 1, ws, 256, None) == -2
+    # workspace too small / misaligned
+    assert lib.se_page_meta_build(ctypes.byref(_paged()), 1, ws, 16, None) == -3
+    assert lib.se_page_meta_build(ctypes.byref(_paged()), 1, ctypes.c_void_p((1 << 20) + 8),
+                                  256, None) == -3
+    # decode: unsupported group size (Hq/Hkv = 3) and head_dim
+    view = binding.ViewC(1 << 20, 1 << 20, 4, 8)
+    args = [ctypes.c_void_p(1 << 20)] * 2
+    assert lib.se_sparse_decode(*args, 100, ctypes.byref(view), ctypes.c_void_p(1 << 20), 1, 12,
+                                4, 128, 0.1, None, ctypes.c_void_p(1 << 20), None, ws,
+                                1 << 30, None) == -2
+    assert lib.se_sparse_decode(*args, 100, ctypes.byref(view), ctypes.c_void_p(1 << 20), 1, 32,
+                                4, 80, 0.1, None, ctypes.c_void_p(1 << 20), None, ws,
+                                1 << 30, None) == -2
+    # decode: view unit count mismatch
+    assert lib.se_sparse_decode(*args, 100, ctypes.byref(view), ctypes.c_void_p(1 << 20), 2, 32,
+                                4, 128, 0.1, None, ctypes.c_void_p(1 << 20), None, ws,
+                                1 << 30, None) == -1
+    # decode: max_splits out of range
+    opts = binding.DecodeOptsC(0, 65, None, 0, None, None)
+    assert lib.se_sparse_decode(*args, 100, ctypes.byref(view), ctypes.c_void_p(1 << 20), 1, 32,
+                                4, 128, 0.1, ctypes.byref(opts), ctypes.c_void_p(1 << 20), None,
+                                ws, 1 << 30, None) == -1
+    # decode: workspace too small for the split count
+    assert lib.se_sparse_decode(*args, 100, ctypes.byref(view), ctypes.c_void_p(1 << 20), 1, 32,
+                                4, 128, 0.1, None, ctypes.c_void_p(1 << 20), None, ws,
+                                1024, None) == -3
+    # quest select: view too small for the block table width
+    small_view = binding.ViewC(1 << 20, 1 << 20, 4, 2)
+    assert lib.se_quest_select(ctypes.byref(_paged()), ctypes.c_void_p(1 << 20), 1, 32,
+                               ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 20),
+                               ctypes.c_void_p(1 << 20), ctypes.byref(small_view), ws,
+                               1 << 30, None) == -5
+
+
+def test_zero_batch_is_a_no_op(lib):
+    view = binding.ViewC(None, None, 0, 0)
+    assert lib.se_sparse_decode(None, None, 0, ctypes.byref(view), None, 0, 32, 4, 128, 0.1,
+                                None, None, None, None, 0, None) == 0

@@ -1,0 +1,148 @@
+"""GPU parity: Quest selection + split-K decode (through the C ABI) against the
+oracle, step by step, on seeded inputs: the tiny single-query case, ragged
+multi-step cases across group sizes and head dims, the edge cases (k = 1,
+budget >= context, empty prefill, one split vs many), and the full-size
+32K-context and ragged 64K-128K workloads on sampled (step, unit) pairs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_decode_quest_gb300 import synth
+from kv_cache_decode_quest_gb300.workloads import QuestRun
+from tests.parity import TOL_BF16, TOL_F32, bf16_tensor_to_f64, check_topk, max_abs
+
+pytestmark = pytest.mark.gpu
+U32 = synth.UNBOUNDED_BUDGET
+
+
+def oracle_unit(w, inputs, b, h, s, gpu_pages=None):
+    """Oracle for unit (b, h) at step s (after that step's append).  Returns
+    (U, oracle pages, k, out [G][D], lse [G]) where the attention uses the
+    GPU's page set when given (after it passed the selection check)."""
+    G = w.num_q_heads // w.num_kv_heads
+    L = w.ctx[b] + s + 1
+    K = oracle.widen(inputs["k"][b][h, :L])
+    V = oracle.widen(inputs["v"][b][h, :L])
+    q = oracle.widen(inputs["q"][s, b, h * G:(h + 1) * G])
+    kmin, kmax = oracle.page_minmax(K)
+    U = oracle.quest_bound(q, kmin, kmax)
+    k = oracle.quest_k_pages(min(w.budget[b], U32))
+    pages = oracle.quest_select(U, k)
+    use = pages if gpu_pages is None else np.asarray(gpu_pages)
+    tok = oracle.quest.selected_tokens(use, L)
+    out, lse = oracle.attend(q, K[tok], V[tok], 1.0 / math.sqrt(w.head_dim))
+    return U, pages, k, out, lse
+
+
+def check_step(run, inputs, s, units=None):
+    w = run.w
+    G, Hkv = run.G, run.Hkv
+    sel = run.sel.cpu().numpy()
+    n_sel = run.n_sel.cpu().numpy()
+    out = bf16_tensor_to_f64(run.out)
+    lse = run.lse.cpu().numpy().astype(np.float64)
+    tol = TOL_F32 if run.out_dtype == 1 else TOL_BF16
+    worst = 0.0
+    allowed = 0
+    for u in (range(run.B * Hkv) if units is None else units):
+        b, h = divmod(u, Hkv)
+        gpu_pages = sel[u, :n_sel[u]]
+        assert np.all(np.diff(gpu_pages) > 0), "pages not ascending"
+        U, pages, k, _, _ = oracle_unit(w, inputs, b, h, s)
+        n = len(U)
+        if n > k:
+            cand = U[:n - 1]
+            boundary = cand[oracle.rank_order(cand)[k - 2]] if k >= 2 else np.inf
+            assert gpu_pages[-1] == n - 1, "last page not forced"
+            if k >= 2:
+                allowed += check_topk(gpu_pages[:-1], pages[:-1], cand, boundary,
+                                      what=f"step {s} unit {u}")
+            else:
+                assert len(gpu_pages) == 1
+        else:
+            assert np.array_equal(gpu_pages, pages)
+        _, _, _, o_ref, l_ref = oracle_unit(w, inputs, b, h, s, gpu_pages)
+        err = max_abs(out[b, h * G:(h + 1) * G], o_ref)
+        worst = max(worst, err)
+        assert err <= tol, f"step {s} unit {u}: max-abs {err} > {tol}"
+        assert max_abs(lse[b, h * G:(h + 1) * G], l_ref) <= 1e-3
+    return worst, allowed
+
+
+def run_and_check(w, out_dtype=0, max_splits=None, steps=None, units=None):
+    inputs = synth.quest_inputs(w)
+    run = QuestRun(w, inputs, out_dtype=out_dtype, max_splits=max_splits)
+    worst = 0.0
+    for s in range(w.steps):
+        run.step(s)
+        if steps is None or s in steps:
+            torch.cuda.synchronize()
+            e, _ = check_step(run, inputs, s, units)
+            worst = max(worst, e)
+    torch.cuda.synchronize()
+    assert run.status() == 0, f"device status word {run.status()}"
+    return worst
+
+
+def test_tiny_quest_single_query():
+    w = synth.workloads()["tiny_quest"]
+    run_and_check(w)
+    run_and_check(w, out_dtype=1)
+
+
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_ragged_multi_step_outliers(out_dtype):
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name="quest_ragged_small", batch=4, ctx=(1000, 2053, 300, 0),
+                     budget=(256, 512, 4096, 64), steps=5)
+    run_and_check(w, out_dtype=out_dtype)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 128), (8, 4, 64), (32, 4, 128), (32, 2, 64),
+                                       (64, 4, 128), (16, 4, 64)])
+def test_group_sizes_and_head_dims(hq, hkv, d):
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name=f"quest_g{hq // hkv}_d{d}", batch=2, num_q_heads=hq,
+                     num_kv_heads=hkv, head_dim=d, ctx=(777, 1600), budget=(128, 256), steps=2)
+    run_and_check(w)
+
+
+def test_budget_of_one_page_and_full_budget():
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name="quest_edges", batch=3, ctx=(500, 129, 2000),
+                     budget=(16, U32, U32), steps=2)
+    run_and_check(w, out_dtype=1)
+
+
+@pytest.mark.parametrize("max_splits", [1, 3, 64])
+def test_split_count_does_not_change_results(max_splits):
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name="quest_splits", batch=2, ctx=(3000, 1234), budget=(U32, 1024),
+                     steps=1)
+    run_and_check(w, out_dtype=1, max_splits=max_splits)
+
+
+def test_ragged_long_scaled():
+    base = synth.workloads()["ragged_quest_128k"]
+    w = synth.scaled(base, name="ragged_small", batch=4, ctx=(2300, 4100, 3333, 2900),
+                     budget=(U32, 512, U32, 512), steps=3)
+    run_and_check(w)
+
+
+@pytest.mark.slow
+def test_full_size_quest_32k_sampled():
+    """The 16 x 32K-context workload, all 64 steps on the GPU with the bench's
+    launch configuration; the oracle checks steps 0, 31, 63 on every unit."""
+    w = synth.workloads()["quest_32k"]
+    run_and_check(w, steps={0, 31, 63})
+
+
+@pytest.mark.slow
+def test_full_size_ragged_128k_sampled():
+    """The ragged 64K-128K workload (half dense-equivalent), all 32 steps on
+    the GPU; the oracle checks steps 0 and 31 on units of every sequence."""
+    w = synth.workloads()["ragged_quest_128k"]
+    run_and_check(w, steps={0, 31}, units=list(range(0, 32, 3)))
