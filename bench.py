@@ -1,0 +1,470 @@
+"""Benchmark of the sparse-decode hot path on GB300.
+
+Headline: the Quest decode workload with 16 sequences of 32K context (32 query
+/ 4 KV heads, head_dim 128, bf16 paged KV, 2048-token budget per KV head).
+One step = one decode step of the whole batch: append the new token
+(page-summary update), Quest selection (scores + top-k + AttentionView),
+split-K decode + LSE merge.  Metric: decode queries/s (one query = one
+sequence's step over all query heads), with the decode kernel's achieved HBM
+bandwidth against the measured peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+L2 is flushed (a 512 MiB write) before every timed step; steps are timed
+with CUDA events on the launching stream.  Under torchrun each rank runs an
+independent replica (no collective on the data path); rank 0 prints one JSON
+line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode-attn queries/s at 1 GB300; achieved HBM GB/s vs peak"
+HEADLINE = "quest_32k"
+FLUSH_BYTES = 512 << 20
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+DECODE_SRC = os.path.join(ROOT, "kv_cache_decode_quest_gb300", "csrc", "decode.cu")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(name, src):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary, or None
+    when the summary is missing or the kernel source changed since."""
+    path = os.path.join(PROFILE_DIR, name)
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_sha") != file_sha(src):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (spawned workers; the oracle as it stands)
+# ---------------------------------------------------------------------------
+
+def _oracle_worker(args):
+    """Run oracle Quest queries of one sequence for about `seconds`."""
+    name, b, seconds = args
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    sys.path.insert(0, ROOT)
+    import oracle
+    from kv_cache_decode_quest_gb300 import synth
+    w = synth.workloads()[name]
+    k, v = synth.quest_sequence(w, b)
+    q = synth.quest_queries(w)
+    G = w.num_q_heads // w.num_kv_heads
+    scale = 1.0 / math.sqrt(w.head_dim)
+    done, t0 = 0, time.perf_counter()
+    s = 0
+    while True:
+        L = w.ctx[b] + s + 1
+        for h in range(w.num_kv_heads):
+            K = oracle.widen(k[h, :L])
+            V = oracle.widen(v[h, :L])
+            qg = oracle.widen(q[s, b, h * G:(h + 1) * G])
+            U = oracle.quest_bound(qg, *oracle.page_minmax(K))
+            pages = oracle.quest_select(U, oracle.quest_k_pages(min(w.budget[b], 2 ** 31 - 1)))
+            tok = oracle.quest.selected_tokens(pages, L)
+            oracle.attend(qg, K[tok], V[tok], scale)
+        done += 1
+        s = (s + 1) % w.steps
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(name, seconds=12.0, cores=None):
+    import multiprocessing as mp
+    cores = cores or max(1, os.cpu_count() or 1)
+    from kv_cache_decode_quest_gb300 import synth
+    B = synth.workloads()[name].batch
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_worker, [(name, i % B, seconds) for i in range(cores)])
+    wall = time.perf_counter() - t0
+    q = sum(r[0] for r in res)
+    per_worker = [r[0] / r[1] for r in res]
+    return {"value": sum(per_worker), "unit": "queries/s", "cores": cores, "kind": "oracle",
+            "sample": f"{q} oracle queries ({name}: page summaries, bound, top-k, fp64 "
+                      f"attention per KV head), ~{seconds:.0f} s per core on {cores} "
+                      f"single-threaded spawned workers, wall {wall:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# GPU timing
+# ---------------------------------------------------------------------------
+
+class QuestBench:
+    """Drives a QuestRun through timed steps, wrapping around its step inputs
+    (restoring the page summaries and lengths, outside the timed region)."""
+
+    def __init__(self, name, device):
+        import torch
+        from kv_cache_decode_quest_gb300 import synth, workloads
+        self.torch = torch
+        self.w = synth.workloads()[name]
+        inputs = synth.quest_inputs(self.w)
+        self.run = workloads.QuestRun(self.w, inputs, device=device)
+        del inputs
+        self.meta0 = self.run.kv.meta.clone()
+        self.ctx0 = self.run.kv.ctx_len.clone()
+        self.s = 0
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def next_index(self):
+        if self.s == self.w.steps:
+            self.run.kv.meta.copy_(self.meta0)
+            self.run.kv.ctx_len.copy_(self.ctx0)
+            self.s = 0
+        s = self.s
+        self.s += 1
+        return s
+
+    def bytes_for(self, s):
+        import numpy as np
+        ctx_now = np.asarray(self.w.ctx) + s + 1
+        return self.run.algorithmic_bytes(ctx_now)
+
+    def timed(self, K, W):
+        torch = self.torch
+        for _ in range(W):
+            s = self.next_index()
+            self.flush.zero_()
+            self.run.step(s)
+        torch.cuda.synchronize()
+        E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        evs, idx = [], []
+        for _ in range(K):
+            s = self.next_index()
+            self.flush.zero_()
+            e = (E(), E(), E(), E())
+            # torch creates an event on its first record(); the library then
+            # re-records the kernel events around the decode kernel itself
+            e[2].record()
+            e[3].record()
+            e[0].record()
+            self.run.step(s, ev_begin=e[2], ev_end=e[3])
+            e[1].record()
+            evs.append(e)
+            idx.append(s)
+        torch.cuda.synchronize()
+        step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        kern_ms = [e[2].elapsed_time(e[3]) for e in evs]
+        return step_ms, kern_ms, idx
+
+    def timed_e2e(self, K, W):
+        """Same steps through host buffers: H2D of the step's q/k/v from pinned
+        memory and D2H of its output inside the timed region."""
+        torch = self.torch
+        r = self.run
+        qh = r.q.cpu().pin_memory()
+        kh = r.k_new.cpu().pin_memory()
+        vh = r.v_new.cpu().pin_memory()
+        oh = torch.empty((r.S,) + tuple(r.out.shape), dtype=r.out.dtype).pin_memory()
+
+        def one(s):
+            r.q[s].copy_(qh[s], non_blocking=True)
+            r.k_new[s].copy_(kh[s], non_blocking=True)
+            r.v_new[s].copy_(vh[s], non_blocking=True)
+            r.step(s)
+            oh[s].copy_(r.out, non_blocking=True)
+
+        for _ in range(W):
+            s = self.next_index()
+            self.flush.zero_()
+            one(s)
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(K):
+            s = self.next_index()
+            self.flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            one(s)
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in evs]
+        h2d = qh[0].numel() * 2 + kh[0].numel() * 2 + vh[0].numel() * 2
+        d2h = oh[0].numel() * oh.element_size()
+        return ms, h2d, d2h
+
+
+def reduce_max(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    import torch
+    torch.cuda.synchronize()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    import __graft_entry__
+    __graft_entry__.build()
+
+    # oracle baseline first (spawned workers), rank 0 only
+    cpu = cpu_baseline(HEADLINE, seconds=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None
+
+    peak, peak_kind = peaks()
+    qb = QuestBench(HEADLINE, device)
+    B = qb.w.batch
+    barrier(ws)
+    with ClockSampler(local) as clk:
+        step_ms, kern_ms, idx = qb.timed(args.steps, args.warmup)
+    barrier(ws)
+    total_ms = reduce_max(sum(step_ms), ws)
+    ms_per_step = total_ms / args.steps
+    value = ws * B * args.steps / (total_ms / 1e3)
+
+    bytes_steps = [qb.bytes_for(s) for s in idx]
+    dec_bytes = [b["kv"] + b["small"] for b in bytes_steps]
+    achieved = sum(dec_bytes) / (sum(kern_ms) / 1e3) / 1e9
+    step_gbs = sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9
+
+    e2e_ms, h2d, d2h = qb.timed_e2e(args.steps, args.warmup)
+    e2e_total = reduce_max(sum(e2e_ms), ws)
+    e2e_value = ws * B * args.steps / (e2e_total / 1e3)
+
+    extra = {}
+    if args.extras:
+        extra = run_extras(args, device, peak)
+
+    if rank != 0:
+        return
+    traffic = profiled_traffic("decode_kernel_quest_32k.json", DECODE_SRC)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "quest_32k: Qwen3-30B-A3B-shaped layer (32 q / 4 kv heads, "
+                               "head_dim 128), batch 16, context 32768 + 1 token/step, page 16, "
+                               "Quest budget 2048 tokens per KV head, K with 4 outlier channels x8",
+                   "global_batch": B * ws, "seq_len": 32768, "parallelism": f"replicas x{ws}",
+                   "l2": "flushed (512 MiB write) before every timed step",
+                   "step": "append + Quest select (score, top-k, view) + split-K decode + merge"},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": int(sum(dec_bytes) / len(dec_bytes)),
+                     "kernel_ms_per_launch": round(sum(kern_ms) / len(kern_ms), 5),
+                     "step_algorithmic_gbs": round(step_gbs, 1),
+                     "step_frac": round(step_gbs / peak, 4)},
+        "e2e": {"value": round(e2e_value, 1), "unit": "queries/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    if extra:
+        line["extra"] = extra
+    print(json.dumps(line), flush=True)
+
+
+def run_extras(args, device, peak):
+    """The other workloads of the path, timed the same way (reported beside the headline)."""
+    out = {}
+    qb = QuestBench("ragged_quest_128k", device)
+    K = min(16, qb.w.steps)
+    step_ms, kern_ms, idx = qb.timed(K, 3)
+    bytes_steps = [qb.bytes_for(s) for s in idx]
+    dec = sum(b["kv"] + b["small"] for b in bytes_steps)
+    out["ragged_quest_128k"] = {
+        "queries_per_s": round(qb.w.batch * K / (sum(step_ms) / 1e3), 1),
+        "ms_per_step": round(sum(step_ms) / K, 5),
+        "decode_gbs": round(dec / (sum(kern_ms) / 1e3) / 1e9, 1),
+        "decode_frac": round(dec / (sum(kern_ms) / 1e3) / 1e9 / peak, 4),
+        "step_gbs": round(sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9, 1),
+        "steps": K, "warmup": 3}
+    del qb
+    import torch
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step is one query of
+    the headline workload (rank 0 only)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    import oracle
+    from kv_cache_decode_quest_gb300 import synth
+    w = synth.workloads()[HEADLINE]
+    G = w.num_q_heads // w.num_kv_heads
+    scale = 1.0 / math.sqrt(w.head_dim)
+    seqs = {}
+
+    def query(i):
+        b, s = i % w.batch, (i // w.batch) % w.steps
+        if b not in seqs:
+            seqs.clear()
+            seqs[b] = synth.quest_sequence(w, b)
+        k, v = seqs[b]
+        L = w.ctx[b] + s + 1
+        for h in range(w.num_kv_heads):
+            K = oracle.widen(k[h, :L])
+            V = oracle.widen(v[h, :L])
+            qg = oracle.widen(q[s, b, h * G:(h + 1) * G])
+            U = oracle.quest_bound(qg, *oracle.page_minmax(K))
+            pages = oracle.quest_select(U, oracle.quest_k_pages(w.budget[b]))
+            tok = oracle.quest.selected_tokens(pages, L)
+            oracle.attend(qg, K[tok], V[tok], scale)
+
+    q = synth.quest_queries(w)
+    # order queries so a sequence's inputs are generated once per run of steps
+    order = [b + w.batch * s for b in range(w.batch) for s in range(w.steps)]
+    for i in range(args.warmup):
+        query(order[i % len(order)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        query(order[(args.warmup + i) % len(order)])
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "queries/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEADLINE, "global_batch": w.batch, "seq_len": 32768,
+                   "parallelism": "none (host CPU)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "queries/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{args.steps} oracle queries of {HEADLINE} (one sequence's "
+                                   f"decode step over 4 KV heads each), single thread"},
+        "e2e": {"value": round(value, 3), "unit": "queries/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="seconds of oracle work per host core for cpu_baseline (0 = skip)")
+    ap.add_argument("--no-extras", dest="extras", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -220,6 +220,26 @@ def workloads(seed: int = 0) -> dict:
 # tensor sets
 # ---------------------------------------------------------------------------
 
+def quest_sequence(w: QuestWorkload, b: int, tag: str = "") -> tuple:
+    """Logical k, v of sequence b: [Hkv][ctx_b + steps][D] bf16 bits (prefill,
+    then the appended tokens of each step)."""
+    Hkv, D, S = w.num_kv_heads, w.head_dim, w.steps
+    label = w.name + tag
+    T = w.ctx[b] + S
+    cs = None
+    if w.outliers:
+        cs = outlier_scale(w.seed, label + "/outliers", (w.batch, Hkv), D)[b][:, None, :]
+    k = normal_bf16(w.seed, f"{label}/k/{b}", (Hkv, T, D), lead=1, channel_scale=cs)
+    v = normal_bf16(w.seed, f"{label}/v/{b}", (Hkv, T, D), lead=1)
+    return k, v
+
+
+def quest_queries(w: QuestWorkload, tag: str = "") -> np.ndarray:
+    """q [steps][B][Hq][D] bf16 bits."""
+    return normal_bf16(w.seed, w.name + tag + "/q", (w.steps, w.batch, w.num_q_heads, w.head_dim),
+                       lead=2)
+
+
 def quest_inputs(w: QuestWorkload, tag: str = "") -> dict:
     """Logical tensors of a Quest decode run (bf16 bits, uint16).
 
@@ -227,17 +247,12 @@ def quest_inputs(w: QuestWorkload, tag: str = "") -> dict:
     q:      [steps][B][Hq][D]
     The appended token of step s for sequence b is row ctx_b + s.
     """
-    B, Hq, Hkv, D, S = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.steps
-    label = w.name + tag
-    scale = outlier_scale(w.seed, label + "/outliers", (B, Hkv), D) if w.outliers else None
     ks, vs = [], []
-    for b in range(B):
-        T = w.ctx[b] + S
-        cs = scale[b][:, None, :] if scale is not None else None
-        ks.append(normal_bf16(w.seed, f"{label}/k/{b}", (Hkv, T, D), lead=1, channel_scale=cs))
-        vs.append(normal_bf16(w.seed, f"{label}/v/{b}", (Hkv, T, D), lead=1))
-    q = normal_bf16(w.seed, label + "/q", (S, B, Hq, D), lead=2)
-    return {"k": ks, "v": vs, "q": q}
+    for b in range(w.batch):
+        k, v = quest_sequence(w, b, tag)
+        ks.append(k)
+        vs.append(v)
+    return {"k": ks, "v": vs, "q": quest_queries(w, tag)}
 
 
 def snapkv_inputs(w: SnapKVWorkload, group: int) -> dict:
