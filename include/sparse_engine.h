@@ -220,6 +220,27 @@ int se_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
                      int num_kv_heads, int head_dim, float scale, const se_decode_opts* opts,
                      void* out, float* lse, void* ws, size_t ws_bytes, se_stream_t stream);
 
+/* se_sparse_decode for callers that cannot allocate device memory (no
+ * counterpart in the pages: this is a library-usage addition).  Callers that run
+ * inside another framework's memory pool, that must not pay cudaMalloc's device
+ * synchronisation, or whose host application owns every allocation cannot pass
+ * a workspace; this variant takes its scratch from a fixed 8 MiB device array
+ * inside the library (held by every GPU that loads it until the process exits)
+ * and allocates nothing.  Same arguments and results as se_sparse_decode with
+ * default options, except:
+ *   - no workspace; out_dtype as in se_decode_opts; the split-K piece count is
+ *     the largest (<= 64) whose partials fit the array, and a batch whose single
+ *     piece per unit does not fit returns SE_ERR_CAPACITY;
+ *   - status_out: NULL or a device int32 that receives the SE_DEV_* bits;
+ *   - all calls share the array: calls that overlap on the GPU race (order them
+ *     on one stream); each call clears the part that must start at zero;
+ *   - the first call on a device looks up the array's device address; make it
+ *     before any stream capture. */
+int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t total_rows,
+                             const se_view* view, const void* q, int batch, int num_q_heads,
+                             int num_kv_heads, int head_dim, float scale, int out_dtype, void* out,
+                             float* lse, int32_t* status_out, se_stream_t stream);
+
 /* Varlen append for decode over compacted caches: writes k_new/v_new (bf16
  * [batch][num_kv_heads][head_dim]) at row seg_off[u] + seg_len[u] with
  * pos = seq_len[b], then increments seg_len[u] and seq_len[b].  A full segment

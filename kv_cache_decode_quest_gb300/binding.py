@@ -71,6 +71,8 @@ SIGNATURES = {
     "se_view_from_segments": (_I, [_VP, _I, _VP, _VP, _SZ, _VP]),
     "se_sparse_decode": (_I, [_VP, _VP, _I64, _VP, _VP, _I, _I, _I, _I, _F, _VP, _VP, _VP,
                               _VP, _SZ, _VP]),
+    "se_sparse_decode_noalloc": (_I, [_VP, _VP, _I64, _VP, _VP, _I, _I, _I, _I, _F, _I, _VP,
+                                      _VP, _VP, _VP]),
     "se_varlen_append": (_I, [_VP, _VP, _VP, _I, _VP, _SZ, _VP]),
     "se_snapkv_compact": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _SZ, _VP]),
     "se_h2o_step": (_I, [_VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
@@ -279,6 +281,18 @@ def se_sparse_decode(k_rows, v_rows, view: View, q, batch: int, num_q_heads: int
                                    batch, num_q_heads, num_kv_heads, head_dim, scale,
                                    ctypes.byref(opts), _p(out), _p(lse), _p(ws), ws.numel(),
                                    _stream(stream)), "se_sparse_decode")
+
+
+def se_sparse_decode_noalloc(k_rows, v_rows, view: View, q, batch: int, num_q_heads: int,
+                             num_kv_heads: int, head_dim: int, scale: float, out, lse,
+                             out_dtype: int = 0, status_out=None, stream=None):
+    """se_sparse_decode without a workspace (scratch inside the library)."""
+    vc = view.c
+    total_rows = k_rows.numel() // head_dim
+    _check(load().se_sparse_decode_noalloc(_p(k_rows), _p(v_rows), total_rows, ctypes.byref(vc),
+                                           _p(q), batch, num_q_heads, num_kv_heads, head_dim,
+                                           scale, out_dtype, _p(out), _p(lse), _p(status_out),
+                                           _stream(stream)), "se_sparse_decode_noalloc")
 
 
 def se_varlen_append(kv: VarlenKV, k_new, v_new, batch: int, ws, stream=None):
