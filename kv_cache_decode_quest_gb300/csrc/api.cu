@@ -191,7 +191,7 @@ int se_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
     if (!k_rows || !v_rows || !view || !view->chunk_row || !view->n_tokens || !q || !out)
         return SE_ERR_INVALID_ARG;
     if (total_rows <= 0 || total_rows > INT32_MAX) return SE_ERR_INVALID_ARG;
-    if (!aligned(k_rows, 16) || !aligned(v_rows, 16) || !aligned(q, 16) || !aligned(out, 4))
+    if (!aligned(k_rows, 16) || !aligned(v_rows, 16) || !aligned(q, 16) || !aligned(out, 16))
         return SE_ERR_INVALID_ARG;
     if (view->num_units != batch * num_kv_heads || view->max_chunks <= 0) return SE_ERR_INVALID_ARG;
     const int G = num_q_heads / num_kv_heads;

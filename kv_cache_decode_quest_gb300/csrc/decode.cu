@@ -17,7 +17,8 @@
 //    accumulates O^T = V^T P^T (head_dim as M) with ldmatrix.trans + mma.
 //    At the end of a piece the four warps merge through shared memory; a unit
 //    cut into one piece is written directly, others go to fp32 partials.
-//  * combine_kernel merges the partials of multi-piece units by their LSE.
+//  * A unit cut into several pieces is merged by the last of its pieces to
+//    finish (an arrival counter per unit; nobody waits on another CTA).
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,6 +26,7 @@ namespace se {
 namespace {
 
 constexpr int kConsumerWarps = 4;
+constexpr int kMaxGrid = 2048;              // persistent decode CTAs at most
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -54,7 +56,9 @@ struct DecodeParams {
     int Hq, Hkv, G;
     float scale, scale_log2;
     const int4* items;
-    const int* n_items;
+    const int* cta_first;     // [grid+1]: CTA c runs items cta_first[c] .. cta_first[c+1]-1
+    const int2* unit_items;
+    int* counters;
     float* o_part;
     float* lse_part;
     void* out;
@@ -107,50 +111,68 @@ __global__ void __launch_bounds__(kDecodeThreads)
         fence_barrier_init();
     }
     __syncthreads();
-    const int n_items = *p.n_items;
+    const int it_begin = p.cta_first[blockIdx.x], it_end = p.cta_first[blockIdx.x + 1];
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
-        if (lane != 0) return;
-        prefetch_tmap(&tk);
-        prefetch_tmap(&tv);
+        // The whole warp walks the chunk sequence; each lane loads one chunk row
+        // of a 32-chunk block (one coalesced load, the next block prefetched),
+        // lane 0 waits for the stage to be free and issues the TMA copies.
+        if (lane == 0) {
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+        }
         uint32_t seq = 0;
-        for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        for (int it = it_begin; it < it_end; ++it) {
             const int4 item = p.items[it];
             const int u = item.x;
             const int ntok = unit_tokens(p, u);
             const int32_t* crow = p.chunk_row + (int64_t)u * p.max_chunks;
-            for (int c = item.y; c < item.z; ++c, ++seq) {
-                const int s = seq % NS;
-                const uint32_t ph = (seq / NS) & 1;
-                if (!*abort_flag && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
-                    *abort_flag = 1;
-                    flag(p.status, SE_DEV_TIMEOUT);
-                }
-                const int row = crow[c];
-                int cnt = min(kPage, ntok - c * kPage);
-                if (row < 0 || (int64_t)row >= p.total_rows) {
-                    flag(p.status, SE_DEV_BAD_INDEX);
-                    cnt = 0;
-                }
-                stage_ntok[s] = cnt;
-                if (cnt > 0 && !*abort_flag) {
-                    uint8_t* kdst = stages + s * S::kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+            int row_next = item.y + lane < item.z ? crow[item.y + lane] : -1;
+            for (int cb = item.y; cb < item.z; cb += 32) {
+                const int row_l = row_next;
+                row_next = cb + 32 + lane < item.z ? crow[cb + 32 + lane] : -1;
+                const int nb = min(32, item.z - cb);
+                for (int j = 0; j < nb; ++j, ++seq) {
+                    const int row = __shfl_sync(0xffffffffu, row_l, j);
+                    if (lane == 0) {
+                        const int c = cb + j;
+                        const int s = seq % NS;
+                        const uint32_t ph = (seq / NS) & 1;
+                        if (!*abort_flag && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+                            *abort_flag = 1;
+                            flag(p.status, SE_DEV_TIMEOUT);
+                        }
+                        int cnt = min(kPage, ntok - c * kPage);
+                        if (row < 0 || (int64_t)row >= p.total_rows) {
+                            flag(p.status, SE_DEV_BAD_INDEX);
+                            cnt = 0;
+                        }
+                        stage_ntok[s] = cnt;
+                        if (cnt > 0 && !*abort_flag) {
+                            uint8_t* kdst = stages + s * S::kStageBytes;
+                            mbar_arrive_expect_tx(&full[s], S::kStageBytes);
 #pragma unroll
-                    for (int bx = 0; bx < S::kBoxes; ++bx) {
-                        tma_load_2d(kdst + bx * 2048, &tk, &full[s], 64 * bx, row);
-                        tma_load_2d(kdst + S::kChunkBytes + bx * 2048, &tv, &full[s], 64 * bx, row);
+                            for (int bx = 0; bx < S::kBoxes; ++bx) {
+                                tma_load_2d(kdst + bx * 2048, &tk, &full[s], 64 * bx, row);
+                                tma_load_2d(kdst + S::kChunkBytes + bx * 2048, &tv, &full[s],
+                                            64 * bx, row);
+                            }
+                        } else {
+                            mbar_arrive(&full[s]);
+                        }
                     }
-                } else {
-                    mbar_arrive(&full[s]);
+                    __syncwarp();
                 }
             }
         }
         // Drain: every copy issued by this CTA lands before the CTA may exit.
-        const uint32_t first = seq > (uint32_t)NS ? seq - NS : 0;
-        volatile int never = 0;
-        for (uint32_t q2 = first; q2 < seq; ++q2) mbar_wait(&full[q2 % NS], (q2 / NS) & 1, &never);
+        if (lane == 0) {
+            const uint32_t first = seq > (uint32_t)NS ? seq - NS : 0;
+            volatile int never = 0;
+            for (uint32_t q2 = first; q2 < seq; ++q2)
+                mbar_wait(&full[q2 % NS], (q2 / NS) & 1, &never);
+        }
         return;
     }
 
@@ -167,7 +189,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int v_tok = (lj >> 1) * 8 + lr, v_dof = (lj & 1) * 8;   // V^T as A (d x token)
 
     uint32_t seq = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    for (int it = it_begin; it < it_end; ++it) {
         const int4 item = p.items[it];
         const int u = item.x;
         const int b = u / p.Hkv, h = u % p.Hkv;
@@ -368,97 +390,176 @@ __global__ void __launch_bounds__(kDecodeThreads)
             }
         }
         consumer_bar();
+        if (slot >= 0) {
+            // The last piece of unit u to finish merges all of u's pieces by
+            // their LSE (an arrival counter, no waiting on other CTAs).
+            volatile int* last = stage_ntok + NS + 1;
+            const int2 ui = p.unit_items[u];
+            if (ctid == 0) {
+                // the CTA barrier above orders the other threads' partial writes
+                // before this thread's release (fences are cumulative)
+                __threadfence();
+                const int old = atomicAdd(&p.counters[u], 1);
+                *last = old == ui.y - 1;
+                if (old == ui.y - 1) atomicExch(&p.counters[u], 0);
+            }
+            consumer_bar();
+            if (*last) {
+                __threadfence();
+                const int n = min(ui.y, SE_MAX_SPLITS);
+                float* wv = ow;                         // [n][G] weights, then [G] M and L
+                for (int i = ctid; i < n * G; i += kConsumerWarps * 32)
+                    wv[i] = __ldcg(p.lse_part + (int64_t)ui.x * G + i);
+                consumer_bar();
+                if (ctid < G) {
+                    float M = -INFINITY, L = 0.f;
+                    for (int i = 0; i < n; ++i) M = fmaxf(M, wv[i * G + ctid]);
+                    for (int i = 0; i < n; ++i) {
+                        const float f = M == -INFINITY ? 0.f : exp2f(wv[i * G + ctid] - M);
+                        wv[i * G + ctid] = f;
+                        L += f;
+                    }
+                    wv[n * G + ctid] = M;
+                    wv[n * G + G + ctid] = L;
+                }
+                consumer_bar();
+                for (int idx = ctid; idx < G * D / 4; idx += kConsumerWarps * 32) {
+                    const int g = idx / (D / 4), d = (idx % (D / 4)) * 4;
+                    const float L = wv[n * G + G + g];
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4* src =
+                        reinterpret_cast<const float4*>(p.o_part + ((int64_t)ui.x * G + g) * D + d);
+                    const int64_t step = (int64_t)G * D / 4;
+#pragma unroll 8
+                    for (int i = 0; i < n; ++i) {
+                        const float4 x = __ldcg(src + i * step);
+                        const float f = wv[i * G + g];
+                        acc.x += f * x.x;
+                        acc.y += f * x.y;
+                        acc.z += f * x.z;
+                        acc.w += f * x.w;
+                    }
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    const int64_t hq = (int64_t)b * p.Hq + h * G + g;
+                    if (p.out_f32) {
+                        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + hq * D + d) =
+                            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    } else {
+                        uint2 o;
+                        o.x = pack_bf16(acc.x * inv, acc.y * inv);
+                        o.y = pack_bf16(acc.z * inv, acc.w * inv);
+                        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + hq * D + d) = o;
+                    }
+                    if (d == 0 && p.lse_out)
+                        p.lse_out[hq] = L > 0.f ? (wv[n * G + g] + log2f(L)) * kLn2 : -INFINITY;
+                }
+            }
+            consumer_bar();
+        }
     }
 }
 
-// One CTA: per unit, nc = ceil(n_tokens/16) chunks are cut into pieces of
-// cps chunks, where the piece size aims at `target_items` pieces overall (at
-// least `min_chunks` chunks each) and each unit has at most max_splits pieces.
+// One CTA.  Stream-K plan: the units' chunks are laid end to end (unit u owns
+// global chunks [P_u, P_u + nc_u)); CTA c owns the global range
+// [c*per, (c+1)*per) with per = ceil(total / grid), so every CTA streams the
+// same number of chunks.  A unit is cut at range boundaries into pieces
+// (items); per is raised when needed so that no unit has more than max_splits
+// pieces.  With max_splits < 3 a unit is cut into at most max_splits equal
+// pieces instead.  Outputs: items (unit, first chunk, end chunk, partial slot
+// or -1 when the piece is the whole unit), per-unit (first item, count), and
+// cta_first[c] = first item of CTA c (items whose global start lies in its range).
 __global__ void __launch_bounds__(1024)
     plan_kernel(const int32_t* __restrict__ n_tokens, int units, int max_chunks, int max_splits,
-                int target_items, int min_chunks, int4* __restrict__ items,
-                int2* __restrict__ unit_items, int* __restrict__ n_items, int* status) {
+                int grid, int4* __restrict__ items, int* __restrict__ gstart,
+                int2* __restrict__ unit_items, int* __restrict__ cta_first,
+                int* __restrict__ n_items, int* __restrict__ counters, int* status) {
     __shared__ int tmp[33];
+    __shared__ int s_max;
     const int lim = max_chunks * kPage;
     auto chunks_of = [&](int u) {
         int n = n_tokens[u];
-        n = n < 0 ? 0 : (n > lim ? lim : n);
+        if (n < 0 || n > lim) {
+            flag(status, SE_DEV_BAD_LENGTH);
+            n = n < 0 ? 0 : lim;
+        }
         return (n + kPage - 1) / kPage;
     };
+    if (threadIdx.x == 0) s_max = 0;
+    for (int u = threadIdx.x; u < units; u += blockDim.x) counters[u] = 0;
+    __syncthreads();
     int total = 0;
     for (int base = 0; base < units; base += blockDim.x) {
         const int u = base + threadIdx.x;
+        const int nc = u < units ? chunks_of(u) : 0;
+        if (nc > 0) atomicMax(&s_max, nc);
         int t;
-        block_exclusive_scan(u < units ? chunks_of(u) : 0, tmp, &t);
+        block_exclusive_scan(nc, tmp, &t);
         total += t;
     }
-    const int C = max(min_chunks, (total + target_items - 1) / max(1, target_items));
-    int run = 0;
+    __syncthreads();
+    const bool streamk = max_splits >= 3;
+    int per = max(1, (total + grid - 1) / max(1, grid));
+    if (streamk) per = max(per, (s_max + max_splits - 3) / (max_splits - 2));
+
+    int run_items = 0, run_chunks = 0;
     for (int base = 0; base < units; base += blockDim.x) {
         const int u = base + threadIdx.x;
-        int nc = 0, splits = 0, cps = 1;
+        int nc = 0, pieces = 0;
         if (u < units) {
             nc = chunks_of(u);
-            splits = nc == 0 ? 1 : min(max_splits, (nc + C - 1) / C);
-            cps = nc == 0 ? 1 : (nc + splits - 1) / splits;
-            splits = nc == 0 ? 1 : (nc + cps - 1) / cps;
         }
-        int t;
-        const int off = run + block_exclusive_scan(splits, tmp, &t);
+        int t_chunks;
+        const int P = run_chunks + block_exclusive_scan(nc, tmp, &t_chunks);
         if (u < units) {
-            unit_items[u] = make_int2(off, splits);
-            for (int k = 0; k < splits; ++k)
-                items[off + k] = make_int4(u, k * cps, min(nc, (k + 1) * cps), splits == 1 ? -1 : off + k);
+            if (nc == 0)
+                pieces = 1;
+            else if (streamk)
+                pieces = (P + nc - 1) / per - P / per + 1;
+            else
+                pieces = min(max_splits, nc);
         }
-        run += t;
-    }
-    if (threadIdx.x == 0) *n_items = run;
-}
-
-// grid units*G, block 128: out = sum_s w_s o_s / sum_s w_s with w_s = 2^(lse_s - max).
-__global__ void __launch_bounds__(128)
-    combine_kernel(const int2* __restrict__ unit_items, const float* __restrict__ o_part,
-                   const float* __restrict__ lse_part, int Hq, int Hkv, int G, int D, int out_f32,
-                   void* out, float* lse_out) {
-    __shared__ float w[SE_MAX_SPLITS];
-    __shared__ float s_M, s_L;
-    const int u = blockIdx.x / G, g = blockIdx.x % G;
-    const int2 ui = unit_items[u];
-    if (ui.y <= 1) return;
-    const int n = min(ui.y, SE_MAX_SPLITS);
-    if (threadIdx.x < 32) {
-        float M = -INFINITY;
-        for (int s = threadIdx.x; s < n; s += 32) M = fmaxf(M, lse_part[(int64_t)(ui.x + s) * G + g]);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float L = 0.f;
-        for (int s = threadIdx.x; s < n; s += 32) {
-            const float x = lse_part[(int64_t)(ui.x + s) * G + g];
-            const float f = M == -INFINITY ? 0.f : exp2f(x - M);
-            w[s] = f;
-            L += f;
+        int t_items;
+        const int off = run_items + block_exclusive_scan(pieces, tmp, &t_items);
+        if (u < units) {
+            unit_items[u] = make_int2(off, pieces);
+            for (int k = 0; k < pieces; ++k) {
+                int c0, c1;
+                if (nc == 0) {
+                    c0 = c1 = 0;
+                } else if (streamk) {
+                    const int g0 = k == 0 ? P : (P / per + k) * per;
+                    const int g1 = min(P + nc, (P / per + k + 1) * per);
+                    c0 = g0 - P;
+                    c1 = g1 - P;
+                } else {
+                    c0 = (int)((int64_t)nc * k / pieces);
+                    c1 = (int)((int64_t)nc * (k + 1) / pieces);
+                }
+                items[off + k] = make_int4(u, c0, c1, pieces == 1 ? -1 : off + k);
+                gstart[off + k] = P + c0;
+            }
         }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (threadIdx.x == 0) {
-            s_M = M;
-            s_L = L;
-        }
+        run_items += t_items;
+        run_chunks += t_chunks;
     }
     __syncthreads();
-    const float L = s_L;
-    const int b = u / Hkv, h = u % Hkv;
-    const int64_t hq = (int64_t)b * Hq + h * G + g;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < n; ++s) acc += w[s] * o_part[((int64_t)(ui.x + s) * G + g) * D + d];
-        const float val = L > 0.f ? acc / L : 0.f;
-        if (out_f32)
-            static_cast<float*>(out)[hq * D + d] = val;
-        else
-            static_cast<uint16_t*>(out)[hq * D + d] = to_bf16_bits(val);
+    const int n = run_items;
+    // CTA c takes the items whose global start lies in [c*per, (c+1)*per);
+    // the last CTA also takes anything past the end.
+    for (int c = threadIdx.x; c <= grid; c += blockDim.x) {
+        int lo = 0, hi = n;
+        if (c == grid) {
+            lo = n;
+        } else {
+            const int64_t key = (int64_t)c * per;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (gstart[mid] < key) lo = mid + 1; else hi = mid;
+            }
+        }
+        cta_first[c] = (c == 0) ? 0 : lo;
     }
-    if (threadIdx.x == 0 && lse_out) lse_out[hq] = L > 0.f ? (s_M + log2f(L)) * kLn2 : -INFINITY;
+    if (threadIdx.x == 0) *n_items = n;
 }
 
 template <int D, int NT, bool TWO>
@@ -485,8 +586,10 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 size_t decode_ws_bytes(int num_units, int G, int D, int max_splits) {
     const size_t items = (size_t)num_units * max_splits;
-    return 256 + align256(items * sizeof(int4)) + align256((size_t)num_units * sizeof(int2)) +
-           align256(items * G * sizeof(float)) + align256(items * G * D * sizeof(float));
+    return 256 + align256(items * sizeof(int4)) + align256(items * sizeof(int)) +
+           align256((size_t)num_units * sizeof(int2)) + align256((size_t)num_units * sizeof(int)) +
+           align256((kMaxGrid + 1) * sizeof(int)) + align256(items * G * sizeof(float)) +
+           align256(items * G * D * sizeof(float));
 }
 
 DecodeWs decode_ws_carve(void* ws, int num_units, int G, int D, int max_splits) {
@@ -498,8 +601,14 @@ DecodeWs decode_ws_carve(void* ws, int num_units, int G, int D, int max_splits) 
     size_t off = 256;
     w.items = reinterpret_cast<int4*>(base + off);
     off += align256(items * sizeof(int4));
+    w.gstart = reinterpret_cast<int*>(base + off);
+    off += align256(items * sizeof(int));
     w.unit_items = reinterpret_cast<int2*>(base + off);
     off += align256((size_t)num_units * sizeof(int2));
+    w.counters = reinterpret_cast<int*>(base + off);
+    off += align256((size_t)num_units * sizeof(int));
+    w.cta_first = reinterpret_cast<int*>(base + off);
+    off += align256((kMaxGrid + 1) * sizeof(int));
     w.lse_part = reinterpret_cast<float*>(base + off);
     off += align256(items * G * sizeof(float));
     w.o_part = reinterpret_cast<float*>(base + off);
@@ -524,10 +633,11 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
     const int cps = head_dim == 64 ? ctas_per_sm<64, 1>()
                                    : (NT == 1 ? ctas_per_sm<128, 1>() : ctas_per_sm<128, 2>());
     const int max_items = units * max_splits;
-    const int grid = max(1, min(max_items, num_sms() * cps));
+    const int grid = max(1, min(kMaxGrid, min(max_items, num_sms() * cps)));
 
-    plan_kernel<<<1, 1024, 0, s>>>(view.n_tokens, units, view.max_chunks, max_splits, grid, 4,
-                                   w.items, w.unit_items, w.n_items, w.status);
+    plan_kernel<<<1, 1024, 0, s>>>(view.n_tokens, units, view.max_chunks, max_splits, grid, w.items,
+                                   w.gstart, w.unit_items, w.cta_first, w.n_items, w.counters,
+                                   w.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -542,7 +652,9 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.items = w.items;
-    p.n_items = w.n_items;
+    p.cta_first = w.cta_first;
+    p.unit_items = w.unit_items;
+    p.counters = w.counters;
     p.o_part = w.o_part;
     p.lse_part = w.lse_part;
     p.out = out;
@@ -574,9 +686,7 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
         e = cudaEventRecord(ev_end, s);
         if (e != cudaSuccess) return e;
     }
-    combine_kernel<<<units * G, 128, 0, s>>>(w.unit_items, w.o_part, w.lse_part, num_q_heads,
-                                             num_kv_heads, G, head_dim, out_dtype == 1, out, lse);
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace se

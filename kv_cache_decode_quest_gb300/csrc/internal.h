@@ -32,7 +32,10 @@ struct DecodeWs {
     int* status;
     int* n_items;
     int4* items;          // [num_units * max_splits]
+    int* gstart;          // [num_units * max_splits]: global first chunk of each item
+    int* cta_first;       // [grid + 1]: first item of each decode CTA
     int2* unit_items;     // [num_units]: (first item, item count)
+    int* counters;        // [num_units]: pieces finished (zeroed by the plan kernel)
     float* lse_part;      // [num_units * max_splits][G]   (log2 domain)
     float* o_part;        // [num_units * max_splits][G][D] (normalised)
 };

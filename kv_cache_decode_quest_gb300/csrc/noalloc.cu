@@ -64,7 +64,7 @@ int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t tot
     if (total_rows <= 0 || total_rows > INT32_MAX) return SE_ERR_INVALID_ARG;
     const uintptr_t a = reinterpret_cast<uintptr_t>(k_rows) | reinterpret_cast<uintptr_t>(v_rows) |
                         reinterpret_cast<uintptr_t>(q);
-    if ((a & 15) || (reinterpret_cast<uintptr_t>(out) & 3)) return SE_ERR_INVALID_ARG;
+    if ((a & 15) || (reinterpret_cast<uintptr_t>(out) & 15)) return SE_ERR_INVALID_ARG;
     const int units = batch * num_kv_heads;
     if (view->num_units != units || view->max_chunks <= 0) return SE_ERR_INVALID_ARG;
 
