@@ -261,7 +261,7 @@ int se_varlen_append(const se_varlen_kv* kv, const void* k_new, const void* v_ne
  * (the unpooled A of each kept token) when non-NULL; seg_len[u] = n_kept;
  * seq_len[b] = L.  n_kept = min(keep, L-recent) + recent must fit seg_cap.
  * prefill: paged K/V (meta unused); q_win bf16 [batch][window][num_q_heads][head_dim].
- * Limits: 1 <= window <= 64, window*G <= 512, 1 <= recent <= L, L <= max_ctx of the
+ * Limits: 1 <= window <= 64, window*G <= 256, 1 <= recent <= L, L <= max_ctx of the
  * workspace query, pool_kernel odd and <= 63.
  * Workspace: se_snapkv_workspace(batch, num_kv_heads, num_q_heads, window, max_ctx). */
 int se_snapkv_compact(const se_paged_kv* prefill, const void* q_win, int batch, int num_q_heads,

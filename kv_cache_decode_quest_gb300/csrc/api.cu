@@ -3,6 +3,7 @@
 // negative status without launching when they are wrong, and otherwise
 // enqueues its kernels on the caller's stream.
 #include <atomic>
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -226,12 +227,47 @@ int se_varlen_append(const se_varlen_kv* kv, const void* k_new, const void* v_ne
                                             static_cast<cudaStream_t>(stream)));
 }
 
-// Not yet implemented: SnapKV compaction and the H2O step.
-size_t se_snapkv_workspace(int, int, int, int, int) { return 256; }
+// Not yet implemented: the H2O step.
 size_t se_h2o_workspace(int, int, int, int, int) { return 256; }
-int se_snapkv_compact(const se_paged_kv*, const void*, int, int, int, int, int, int, float,
-                      const se_varlen_kv*, void*, size_t, se_stream_t) {
-    return SE_ERR_UNSUPPORTED;
+size_t se_snapkv_workspace(int batch, int num_kv_heads, int num_q_heads, int window,
+                           int max_ctx) {
+    (void)num_q_heads;
+    (void)window;
+    if (batch < 0 || num_kv_heads <= 0 || max_ctx < 0) return 0;
+    return snapkv_ws_bytes(batch * num_kv_heads, max_ctx);
+}
+
+int se_snapkv_compact(const se_paged_kv* prefill, const void* q_win, int batch, int num_q_heads,
+                      int window, int pool_kernel, int keep, int recent, float scale,
+                      const se_varlen_kv* out, void* ws, size_t ws_bytes, se_stream_t stream) {
+    int rc = check_paged(prefill, false);
+    if (rc) return rc;
+    if ((rc = check_varlen(out))) return rc;
+    if (batch < 0 || num_q_heads <= 0) return SE_ERR_INVALID_ARG;
+    if (num_q_heads % prefill->num_kv_heads) return SE_ERR_UNSUPPORTED;
+    const int G = num_q_heads / prefill->num_kv_heads;
+    if (!group_ok(G)) return SE_ERR_UNSUPPORTED;
+    if (out->num_kv_heads != prefill->num_kv_heads || out->head_dim != prefill->head_dim)
+        return SE_ERR_INVALID_ARG;
+    if (window < 1 || window > 64 || window * G > 256) return SE_ERR_UNSUPPORTED;
+    if (pool_kernel < 1 || pool_kernel > 63 || pool_kernel % 2 == 0) return SE_ERR_UNSUPPORTED;
+    if (keep < 0 || recent < 1) return SE_ERR_INVALID_ARG;
+    if (batch == 0) return SE_OK;
+    if (!q_win || !aligned(q_win, 16)) return SE_ERR_INVALID_ARG;
+    // the workspace fixes the longest context it can score
+    const size_t base = se_snapkv_workspace(batch, prefill->num_kv_heads, num_q_heads, window, 0);
+    const size_t per_ctx = (size_t)batch * prefill->num_kv_heads * 8;
+    if (!ws || !aligned(ws, 256) || ws_bytes < base) return SE_ERR_WORKSPACE;
+    int64_t max_ctx = (int64_t)((ws_bytes - base) / per_ctx);
+    max_ctx = std::min<int64_t>(max_ctx, (int64_t)prefill->max_pages_per_seq * SE_PAGE_SIZE);
+    while (max_ctx > 0 &&
+           se_snapkv_workspace(batch, prefill->num_kv_heads, num_q_heads, window, (int)max_ctx) >
+               ws_bytes)
+        --max_ctx;
+    if (max_ctx <= 0) return SE_ERR_WORKSPACE;
+    return cuda_status(launch_snapkv_compact(*prefill, q_win, batch, num_q_heads, window,
+                                             pool_kernel, keep, recent, scale, *out, ws,
+                                             (int)max_ctx, static_cast<cudaStream_t>(stream)));
 }
 int se_h2o_step(const se_h2o_state*, const void*, const void*, const void*, int, int, float, int,
                 void*, float*, int32_t*, void*, size_t, se_stream_t) {

@@ -172,4 +172,60 @@ __device__ __forceinline__ uint32_t swz128(int r, int u) {
     return static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4));
 }
 
+// Inclusive scan over the first 256 threads of the block (all threads call it);
+// `tmp` holds 8 ints of shared memory.
+__device__ __forceinline__ int scan256(int v, int* tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (threadIdx.x < 256 && lane == 31) tmp[warp] = x;
+    __syncthreads();
+    int before = 0;
+    if (threadIdx.x < 256)
+        for (int i = 0; i < warp; ++i) before += tmp[i];
+    __syncthreads();
+    return x + before;
+}
+
+// Exact selection threshold for the K largest of m unsigned keys (1 <= K <= m),
+// block-wide (blockDim.x >= 256): four 8-bit MSB-first radix passes.  Returns
+// the K-th largest key T; *need_eq receives how many keys equal to T belong to
+// the top K (every key > T does).  key_at(i) must be callable by any thread.
+// Shared memory: hist[256], tmp[33], sel[2].
+template <typename KeyAt>
+__device__ uint32_t block_radix_select(KeyAt key_at, int m, int K, int* hist, int* tmp, int* sel,
+                                       int* need_eq) {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = K;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        if (threadIdx.x < 256) hist[threadIdx.x] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < m; i += blockDim.x) {
+            const uint32_t key = key_at(i);
+            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+        }
+        __syncthreads();
+        const int v = threadIdx.x < 256 ? hist[255 - threadIdx.x] : 0;
+        const int incl = scan256(v, tmp);
+        if (threadIdx.x < 256) {
+            const int excl = incl - v;
+            if (excl < remaining && incl >= remaining) {
+                sel[0] = 255 - threadIdx.x;
+                sel[1] = excl;
+            }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(sel[0]) << shift;
+        mask |= 255u << shift;
+        remaining -= sel[1];
+        __syncthreads();
+    }
+    *need_eq = remaining;
+    return prefix;
+}
+
 }  // namespace se

@@ -48,6 +48,12 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
                                  cudaEvent_t ev_begin, cudaEvent_t ev_end, void* out, float* lse,
                                  const DecodeWs& w, cudaStream_t s);
 
+// ---- snapkv.cu ----
+size_t snapkv_ws_bytes(int units, int max_ctx);
+cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int batch, int Hq,
+                                  int W, int pool_kernel, int keep, int recent, float scale,
+                                  const se_varlen_kv& out, void* ws, int max_ctx, cudaStream_t s);
+
 // ---- tensor maps (api.cu) ----
 // 2-D bf16 map over [rows][head_dim] with 16-row x 64-column boxes, 128B swizzle.
 bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int head_dim);

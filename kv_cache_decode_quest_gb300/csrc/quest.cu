@@ -111,24 +111,6 @@ __global__ void __launch_bounds__(kScoreWarps * 32)
     }
 }
 
-// Inclusive scan over the first 256 threads (8 warps); `tmp` holds 8 ints.
-__device__ __forceinline__ int scan256(int v, int* tmp) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (threadIdx.x < 256 && lane == 31) tmp[warp] = x;
-    __syncthreads();
-    int before = 0;
-    if (threadIdx.x < 256)
-        for (int i = 0; i < warp; ++i) before += tmp[i];
-    __syncthreads();
-    return x + before;
-}
-
 // One CTA (1024 threads) per unit: exact top-(k-1) of pages 0..n-2 by
 // (score desc, page asc) via a 4-pass 8-bit radix select on order-preserving
 // keys, then an index-ordered emit, plus the forced last page.

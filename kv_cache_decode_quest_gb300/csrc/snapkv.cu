@@ -1,0 +1,513 @@
+// SnapKV compaction at the end of prefill: observation-window attention
+// scores, 1-D max-pool, per-KV-head top-k, and compaction of the survivors
+// into a per-(sequence, KV head) variable-length cache.
+//
+// SnapKV inspects how the last few query rows attend over the history, keeps
+// the important part and physically deletes the rest (tokendh.com article on
+// SparseEngine, section "把边界划在'生命周期'上"); kept tokens keep their
+// logical positions (same article, section "聊天记录也能'续命':Chain Cache").
+//
+// Definitions (unit u = (b, h), L = ctx_len[b], window rows i = 0..W-1 at
+// positions L-W+i, G query heads per KV head, M = W*G rows r = i*G + g):
+//   s[r,j] = scale * q_win[b,i,hG+g] . k[j]          for j <= L-W+i (causal)
+//   A[j]   = sum_r exp(s[r,j] - lse_r),  lse_r = log sum_j exp(s[r,j])
+//   candidates [0, L-recent): pooled A (odd window, clipped), best `keep` kept
+//   under (pooled desc, position asc), plus [L-recent, L).
+//
+// Kernels:
+//   snapkv_score_kernel<PASS 1>: per (unit, key range) the per-row running
+//     (max, sum) of exp2 over the range -> partials;
+//   snapkv_score_kernel<PASS 2>: merges the partials into lse_r, recomputes S
+//     and writes the column sums A[j] of its key range;
+//   snapkv_select_kernel: per unit, pool -> keys, exact radix top-k, emit the
+//     kept positions ascending, gather their K/V rows into the varlen cache.
+// S = Q K^T is the one dense contraction of the path (M = W*G rows): Q rows
+// sit in registers as mma.sync A fragments, 64-key blocks of K are staged by
+// TMA from the paged cache (producer warp + mbarriers), B fragments come from
+// ldmatrix on the 128B-swizzled boxes.
+#include "common.cuh"
+#include "internal.h"
+
+namespace se {
+namespace {
+
+constexpr int kSkWarps = 8;                 // consumer warps (16*MT rows each)
+constexpr int kSkThreads = (kSkWarps + 1) * 32;
+constexpr int kSkBlockKeys = 64;            // keys per stage (4 pages)
+constexpr int kSkStages = 4;
+constexpr int kSnapMaxSplits = 64;      // key ranges per unit at most
+constexpr float kLog2eF = 1.4426950408889634f;
+
+template <int D, int MT>
+struct SkShape {
+    static constexpr int kRows = kSkWarps * 16 * MT;          // padded M
+    static constexpr int kQStride = D + 8;                     // bf16 elems per smem row
+    static constexpr int kPageBytes = (D / 64) * 2048;
+    static constexpr int kStageBytes = 4 * kPageBytes;         // 64 keys of K
+    static constexpr size_t kSmem = 1024 + (size_t)kSkStages * kStageBytes +
+                                    (size_t)kRows * kQStride * 2 + kSkStages * 8 * 2 + 64 +
+                                    (size_t)kRows * 4 + kSkBlockKeys * 4 * kSkWarps;
+};
+
+struct SkParams {
+    se_paged_kv kv;
+    const uint16_t* q_win;   // [B][W][Hq][D]
+    int W, Hq, G, M;          // M = W*G real rows
+    int splits;               // key ranges per unit
+    float scale_log2;
+    float2* part;             // [units][splits][kRows] (max, sum) in the exp2 domain
+    float* colsum;            // [units][max_ctx]
+    int max_ctx;
+    int* status;
+};
+
+template <int D, int MT, int PASS>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    snapkv_score_kernel(const __grid_constant__ CUtensorMap tk, const SkParams p) {
+    using S = SkShape<D, MT>;
+    constexpr int KSTEPS = D / 16;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = smem;
+    uint16_t* qs = reinterpret_cast<uint16_t*>(stages + kSkStages * S::kStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(qs + S::kRows * S::kQStride);
+    uint64_t* empty = full + kSkStages;
+    volatile int* abort_flag = reinterpret_cast<int*>(empty + kSkStages);
+    float* lse2 = reinterpret_cast<float*>(empty + kSkStages) + 16;   // [kRows]
+    float* wsum = lse2 + S::kRows;                                    // [warps][64]
+
+    const int H = p.kv.num_kv_heads;
+    const int u = blockIdx.y, split = blockIdx.x;
+    const int b = u / H, h = u % H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int L = p.kv.ctx_len[b];
+    if (L < 0 || L > min(p.max_ctx, p.kv.max_pages_per_seq * kPage)) {
+        if (threadIdx.x == 0 && split == 0) flag(p.status, SE_DEV_BAD_LENGTH);
+        L = L < 0 ? 0 : min(p.max_ctx, p.kv.max_pages_per_seq * kPage);
+    }
+    const int nblk = (L + kSkBlockKeys - 1) / kSkBlockKeys;
+    const int per = (nblk + p.splits - 1) / p.splits;
+    const int blk0 = min(nblk, split * per), blk1 = min(nblk, blk0 + per);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSkStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kSkWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    // window queries -> shared memory (rows past M are zero)
+    for (int i = threadIdx.x; i < S::kRows * (D / 8); i += blockDim.x) {
+        const int r = i / (D / 8), sg = i % (D / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < p.M) {
+            const int wi = r / p.G, g = r % p.G;
+            v = reinterpret_cast<const uint4*>(
+                p.q_win + (((int64_t)b * p.W + wi) * p.Hq + h * p.G + g) * D)[sg];
+        }
+        *reinterpret_cast<uint4*>(qs + r * S::kQStride + sg * 8) = v;
+    }
+    if (PASS == 2) {
+        // merge the pass-1 partials of every row into lse (exp2 domain)
+        for (int r = threadIdx.x; r < S::kRows; r += blockDim.x) {
+            float m = -INFINITY, l = 0.f;
+            for (int s2 = 0; s2 < p.splits; ++s2) {
+                const float2 x = p.part[((int64_t)u * p.splits + s2) * S::kRows + r];
+                if (x.y <= 0.f) continue;
+                const float mn = fmaxf(m, x.x);
+                l = l * exp2f(m - mn) + x.y * exp2f(x.x - mn);
+                m = mn;
+            }
+            lse2[r] = (r < p.M && l > 0.f) ? m + log2f(l) : INFINITY;
+        }
+    }
+    __syncthreads();
+
+    if (warp == kSkWarps) {
+        // ---------------- producer: one 64-key block (4 pages) per stage ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tk);
+            const int32_t* bt = p.kv.block_table + (int64_t)b * p.kv.max_pages_per_seq;
+            uint32_t seq = 0;
+            for (int blk = blk0; blk < blk1; ++blk, ++seq) {
+                const int s = seq % kSkStages;
+                const uint32_t ph = (seq / kSkStages) & 1;
+                if (!*abort_flag && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+                    *abort_flag = 1;
+                    flag(p.status, SE_DEV_TIMEOUT);
+                }
+                int rows[4];
+                int n = 0;
+                for (int pg = 0; pg < 4; ++pg) {
+                    const int page = blk * 4 + pg;
+                    rows[pg] = -1;
+                    if (page * kPage < L) {
+                        const int phys = bt[page];
+                        if (phys >= 0 && phys < p.kv.num_pages) {
+                            rows[pg] = (phys * H + h) * kPage;
+                            ++n;
+                        } else {
+                            flag(p.status, SE_DEV_BAD_INDEX);
+                        }
+                    }
+                }
+                if (n > 0 && !*abort_flag) {
+                    mbar_arrive_expect_tx(&full[s], n * S::kPageBytes);
+                    for (int pg = 0; pg < 4; ++pg) {
+                        if (rows[pg] < 0) continue;
+#pragma unroll
+                        for (int bx = 0; bx < D / 64; ++bx)
+                            tma_load_2d(stages + s * S::kStageBytes + pg * S::kPageBytes + bx * 2048,
+                                        &tk, &full[s], 64 * bx, rows[pg]);
+                    }
+                } else {
+                    mbar_arrive(&full[s]);
+                }
+            }
+            const uint32_t first = seq > (uint32_t)kSkStages ? seq - kSkStages : 0;
+            volatile int never = 0;
+            for (uint32_t q2 = first; q2 < seq; ++q2)
+                mbar_wait(&full[q2 % kSkStages], (q2 / kSkStages) & 1, &never);
+        }
+        return;
+    }
+
+    // ------------------------------ consumers ------------------------------
+    constexpr int NG = 4;                         // n-tiles (8 keys) per group
+    const int r4 = lane >> 2, cq = lane & 3;
+    uint32_t qa[MT][KSTEPS][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+            const int row = warp * 16 * MT + mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int col = kk * 16 + (lane >> 4) * 8;
+            ldsm_x4(smem_u32(qs + row * S::kQStride + col), qa[mt][kk][0], qa[mt][kk][1],
+                    qa[mt][kk][2], qa[mt][kk][3]);
+        }
+    // rows of this thread: [mt][half] -> row index, last visible key, lse
+    int last_key[MT][2];
+    float lrow[MT][2];
+    float m[MT][2], l[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int row = warp * 16 * MT + mt * 16 + r4 + hf * 8;
+            last_key[mt][hf] = row < p.M ? L - p.W + row / p.G : -1;
+            lrow[mt][hf] = PASS == 2 ? lse2[row] : 0.f;
+            m[mt][hf] = -INFINITY;
+            l[mt][hf] = 0.f;
+        }
+    const int lj = lane >> 3, lr = lane & 7;
+
+    uint32_t seq = 0;
+    for (int blk = blk0; blk < blk1; ++blk, ++seq) {
+        const int s = seq % kSkStages;
+        const uint32_t ph = (seq / kSkStages) & 1;
+        if (!*abort_flag && !mbar_wait(&full[s], ph, abort_flag)) {
+            *abort_flag = 1;
+            flag(p.status, SE_DEV_TIMEOUT);
+        }
+        const uint8_t* kb = stages + s * S::kStageBytes;
+        const uint32_t kbase = smem_u32(kb);
+        float colp[kSkBlockKeys / 8][2];
+#pragma unroll
+        for (int grp = 0; grp < kSkBlockKeys / 8 / NG; ++grp) {
+            float sacc[NG][MT][4];
+#pragma unroll
+            for (int n = 0; n < NG; ++n)
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[n][mt][e] = 0.f;
+#pragma unroll
+            for (int n = 0; n < NG; ++n) {
+                const int nt = grp * NG + n;
+                const int keyrow = (nt & 1) * 8 + lr;
+#pragma unroll
+                for (int k2 = 0; k2 < KSTEPS / 2; ++k2) {
+                    const int d = k2 * 32 + lj * 8;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kbase + (nt >> 1) * S::kPageBytes + (d >> 6) * 2048 +
+                                swz128(keyrow, (d & 63) >> 3),
+                            b0, b1, b2, b3);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        mma_16816(sacc[n][mt], qa[mt][2 * k2][0], qa[mt][2 * k2][1],
+                                  qa[mt][2 * k2][2], qa[mt][2 * k2][3], b0, b1);
+                        mma_16816(sacc[n][mt], qa[mt][2 * k2 + 1][0], qa[mt][2 * k2 + 1][1],
+                                  qa[mt][2 * k2 + 1][2], qa[mt][2 * k2 + 1][3], b2, b3);
+                    }
+                }
+            }
+            // mask (causal, past-the-end, padding rows) and scale to the exp2 domain
+#pragma unroll
+            for (int n = 0; n < NG; ++n)
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = blk * kSkBlockKeys + (grp * NG + n) * 8 + 2 * cq + (e & 1);
+                        const bool ok = key <= last_key[mt][e >> 1];
+                        sacc[n][mt][e] = ok ? sacc[n][mt][e] * p.scale_log2 : -INFINITY;
+                    }
+            if (PASS == 1) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float mx = m[mt][hf];
+#pragma unroll
+                        for (int n = 0; n < NG; ++n)
+                            mx = fmaxf(mx, fmaxf(sacc[n][mt][2 * hf], sacc[n][mt][2 * hf + 1]));
+                        if (mx == -INFINITY) continue;
+                        float acc = l[mt][hf] * exp2f(m[mt][hf] - mx);
+#pragma unroll
+                        for (int n = 0; n < NG; ++n)
+                            acc += exp2f(sacc[n][mt][2 * hf] - mx) + exp2f(sacc[n][mt][2 * hf + 1] - mx);
+                        l[mt][hf] = acc;
+                        m[mt][hf] = mx;
+                    }
+            } else {
+#pragma unroll
+                for (int n = 0; n < NG; ++n) {
+                    float c0 = 0.f, c1 = 0.f;
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        c0 += exp2f(sacc[n][mt][0] - lrow[mt][0]) + exp2f(sacc[n][mt][2] - lrow[mt][1]);
+                        c1 += exp2f(sacc[n][mt][1] - lrow[mt][0]) + exp2f(sacc[n][mt][3] - lrow[mt][1]);
+                    }
+                    colp[grp * NG + n][0] = c0;
+                    colp[grp * NG + n][1] = c1;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        if (PASS == 2) {
+            // column sums: over this warp's rows (lanes sharing cq), then over warps
+#pragma unroll
+            for (int nt = 0; nt < kSkBlockKeys / 8; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float x = colp[nt][j];
+                    x += __shfl_xor_sync(0xffffffffu, x, 4);
+                    x += __shfl_xor_sync(0xffffffffu, x, 8);
+                    x += __shfl_xor_sync(0xffffffffu, x, 16);
+                    if (r4 == 0) wsum[warp * kSkBlockKeys + nt * 8 + 2 * cq + j] = x;
+                }
+            asm volatile("bar.sync 1, %0;" ::"r"(kSkWarps * 32) : "memory");
+            if (threadIdx.x < kSkBlockKeys) {
+                const int key = blk * kSkBlockKeys + threadIdx.x;
+                float a = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kSkWarps; ++w2) a += wsum[w2 * kSkBlockKeys + threadIdx.x];
+                if (key < L) p.colsum[(int64_t)u * p.max_ctx + key] = a;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kSkWarps * 32) : "memory");
+        }
+    }
+    if (PASS == 1) {
+        // merge the four lanes that share each row, then store (max, sum)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float mm = m[mt][hf], ll = l[mt][hf];
+#pragma unroll
+                for (int o = 1; o <= 2; o <<= 1) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, mm, o);
+                    const float l2 = __shfl_xor_sync(0xffffffffu, ll, o);
+                    const float mn = fmaxf(mm, m2);
+                    if (mn != -INFINITY) {
+                        ll = ll * exp2f(mm - mn) + l2 * exp2f(m2 - mn);
+                        mm = mn;
+                    }
+                }
+                if (cq == 0) {
+                    const int row = warp * 16 * MT + mt * 16 + r4 + hf * 8;
+                    p.part[((int64_t)u * p.splits + split) * S::kRows + row] = make_float2(mm, ll);
+                }
+            }
+    }
+}
+
+struct SkSelParams {
+    se_paged_kv kv;
+    se_varlen_kv out;
+    const float* colsum;     // [units][max_ctx]
+    uint32_t* keys;          // [units][max_ctx]
+    int max_ctx, recent, keep, pool_kernel;
+    int* status;
+};
+
+// One CTA per unit: pooled keys, exact top-`keep` of the candidates by
+// (pooled desc, position asc), kept positions ascending + the recent window,
+// then the gather of the kept K/V rows (and their unpooled scores).
+__global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p) {
+    __shared__ int hist[256];
+    __shared__ int tmp[33];
+    __shared__ int sel[2];
+    const int H = p.kv.num_kv_heads, D = p.kv.head_dim, segs = D / 8;
+    const int u = blockIdx.x, b = u / H, h = u % H;
+    int L = p.kv.ctx_len[b];
+    const int lim = min(p.max_ctx, p.kv.max_pages_per_seq * kPage);
+    if (L < 0 || L > lim) {
+        if (threadIdx.x == 0 && h == 0) flag(p.status, SE_DEV_BAD_LENGTH);
+        L = L < 0 ? 0 : lim;
+    }
+    const int R = min(p.recent, L);
+    const int ncand = L - R;
+    const int rad = p.pool_kernel / 2;
+    const float* A = p.colsum + (int64_t)u * p.max_ctx;
+    uint32_t* ky = p.keys + (int64_t)u * p.max_ctx;
+    for (int j = threadIdx.x; j < ncand; j += blockDim.x) {
+        float mx = A[j];
+        for (int t = 1; t <= rad; ++t) {
+            if (j - t >= 0) mx = fmaxf(mx, A[j - t]);
+            if (j + t < ncand) mx = fmaxf(mx, A[j + t]);
+        }
+        ky[j] = float_key(mx);
+    }
+    __syncthreads();
+
+    const int K = min(p.keep, ncand);
+    const int off = p.out.seg_off[u];
+    const int cap = p.out.seg_cap;
+    const int n_kept = K + R;
+    if (threadIdx.x == 0 && n_kept > cap) flag(p.status, SE_DEV_CAPACITY);
+    if (threadIdx.x == 0 && (off < 0 || (int64_t)off + min(n_kept, cap) > p.out.total_rows))
+        flag(p.status, SE_DEV_BAD_INDEX);
+    const bool off_ok = off >= 0 && (int64_t)off + min(n_kept, cap) <= p.out.total_rows;
+    int32_t* pos = p.out.pos + off;
+    if (off_ok) {
+        if (K == ncand) {
+            for (int j = threadIdx.x; j < ncand && j < cap; j += blockDim.x) pos[j] = j;
+        } else if (K > 0) {
+            int need_eq;
+            const uint32_t T = block_radix_select([&](int i) { return ky[i]; }, ncand, K, hist, tmp,
+                                                  sel, &need_eq);
+            int run_eq = 0, run_out = 0;
+            for (int base = 0; base < ncand; base += blockDim.x) {
+                const int i = base + threadIdx.x;
+                const uint32_t key = i < ncand ? ky[i] : 0u;
+                const int gt = (i < ncand && key > T) ? 1 : 0;
+                const int eq = (i < ncand && key == T) ? 1 : 0;
+                int eq_tot, take_tot;
+                const int eq_before = block_exclusive_scan(eq, tmp, &eq_tot);
+                const int take = gt || (eq && run_eq + eq_before < need_eq);
+                const int o = block_exclusive_scan(take, tmp, &take_tot);
+                if (take && run_out + o < cap) pos[run_out + o] = i;
+                run_eq += eq_tot;
+                run_out += take_tot;
+            }
+        }
+        for (int t = threadIdx.x; t < R; t += blockDim.x)
+            if (K + t < cap) pos[K + t] = ncand + t;
+    }
+    __syncthreads();
+    const int n = off_ok ? min(n_kept, cap) : 0;
+    const int32_t* bt = p.kv.block_table + (int64_t)b * p.kv.max_pages_per_seq;
+    const uint4* Ks = static_cast<const uint4*>(p.kv.k);
+    const uint4* Vs = static_cast<const uint4*>(p.kv.v);
+    uint4* Kd = static_cast<uint4*>(p.out.k);
+    uint4* Vd = static_cast<uint4*>(p.out.v);
+    for (int i = threadIdx.x; i < n * segs; i += blockDim.x) {
+        const int r = i / segs, sg = i % segs;
+        const int ps = pos[r];
+        const int phys = bt[ps / kPage];
+        const int64_t dst = (int64_t)off + r;
+        if (phys < 0 || phys >= p.kv.num_pages) {
+            if (sg == 0) flag(p.status, SE_DEV_BAD_INDEX);
+            continue;
+        }
+        const int64_t src = ((int64_t)phys * H + h) * kPage + ps % kPage;
+        Kd[dst * segs + sg] = Ks[src * segs + sg];
+        Vd[dst * segs + sg] = Vs[src * segs + sg];
+        if (sg == 0 && p.out.score) p.out.score[dst] = A[ps];
+    }
+    if (threadIdx.x == 0) {
+        p.out.seg_len[u] = n;
+        if (h == 0) p.out.seq_len[b] = L;
+    }
+}
+
+template <int D, int MT, int PASS>
+cudaError_t run_score(const CUtensorMap& tk, const SkParams& p, int units, cudaStream_t s) {
+    using S = SkShape<D, MT>;
+    auto kern = snapkv_score_kernel<D, MT, PASS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(S::kSmem));
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(p.splits, units), kSkThreads, S::kSmem, s>>>(tk, p);
+    return cudaGetLastError();
+}
+
+template <int D, int MT>
+cudaError_t run_both(const CUtensorMap& tk, const SkParams& p, int units, cudaStream_t s) {
+    cudaError_t e = run_score<D, MT, 1>(tk, p, units, s);
+    if (e != cudaSuccess) return e;
+    return run_score<D, MT, 2>(tk, p, units, s);
+}
+
+size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+size_t snapkv_ws_bytes(int units, int max_ctx) {
+    return 256 + al256((size_t)units * kSnapMaxSplits * 256 * sizeof(float2)) +
+           2 * al256((size_t)units * max_ctx * sizeof(float));
+}
+
+cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int batch, int Hq,
+                                  int W, int pool_kernel, int keep, int recent, float scale,
+                                  const se_varlen_kv& out, void* ws, int max_ctx, cudaStream_t s) {
+    const int H = kv.num_kv_heads, units = batch * H, G = Hq / H, D = kv.head_dim;
+    if (units == 0) return cudaSuccess;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    SkParams p;
+    p.kv = kv;
+    p.q_win = static_cast<const uint16_t*>(q_win);
+    p.W = W;
+    p.Hq = Hq;
+    p.G = G;
+    p.M = W * G;
+    const int nblk = (max_ctx + kSkBlockKeys - 1) / kSkBlockKeys;
+    p.splits = max(1, min(kSnapMaxSplits, min(nblk, (num_sms() * 4 + units / 2) / units)));
+    p.scale_log2 = scale * kLog2eF;
+    p.status = reinterpret_cast<int*>(base);
+    size_t off = 256;
+    p.part = reinterpret_cast<float2*>(base + off);
+    off += al256((size_t)units * kSnapMaxSplits * 256 * sizeof(float2));
+    p.colsum = reinterpret_cast<float*>(base + off);
+    off += al256((size_t)units * max_ctx * sizeof(float));
+    uint32_t* keys = reinterpret_cast<uint32_t*>(base + off);
+    p.max_ctx = max_ctx;
+    CUtensorMap tk;
+    if (!encode_rows_map(&tk, kv.k, (int64_t)kv.num_pages * H * kPage, D)) return cudaErrorInvalidValue;
+    cudaError_t e;
+    const bool small = p.M <= 128;
+    if (D == 128)
+        e = small ? run_both<128, 1>(tk, p, units, s) : run_both<128, 2>(tk, p, units, s);
+    else
+        e = small ? run_both<64, 1>(tk, p, units, s) : run_both<64, 2>(tk, p, units, s);
+    if (e != cudaSuccess) return e;
+    SkSelParams q;
+    q.kv = kv;
+    q.out = out;
+    q.colsum = p.colsum;
+    q.keys = keys;
+    q.max_ctx = max_ctx;
+    q.recent = recent;
+    q.keep = keep;
+    q.pool_kernel = pool_kernel;
+    q.status = p.status;
+    snapkv_select_kernel<<<units, 1024, 0, s>>>(q);
+    return cudaGetLastError();
+}
+
+}  // namespace se

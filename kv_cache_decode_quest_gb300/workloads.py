@@ -129,3 +129,82 @@ class QuestRun:
         outb = 4 if self.out_dtype == 1 else 2
         small = self.B * (Hq * D * 2 + 2 * Hkv * D * 2 + Hq * D * outb)
         return {"meta": meta, "kv": sel, "small": small, "total": meta + sel + small}
+
+
+class SnapKVRun:
+    """SnapKV compaction of `groups` prefill batches into one per-(sequence, KV
+    head) varlen cache, then decode over it with one appended token per step."""
+
+    def __init__(self, w: synth.SnapKVWorkload, groups=None, device="cuda", max_splits=None,
+                 keep_inputs=False, with_score=False):
+        self.w = w
+        self.groups = w.groups if groups is None else groups
+        B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+        self.B, self.Hq, self.Hkv, self.D = B, Hq, Hkv, D
+        self.Bt = B * self.groups
+        self.G = Hq // Hkv
+        self.scale = 1.0 / math.sqrt(D)
+        self.max_splits = max_splits or w.max_splits
+        self.device = device
+        L = w.ctx
+        kept = min(w.keep, max(0, L - w.window)) + min(w.window, L)
+        self.seg_cap = kept + w.steps
+        self.cache = se.VarlenKV.empty(self.Bt, Hkv, self.seg_cap, D, with_score=with_score,
+                                       device=device)
+        self.inputs = [] if keep_inputs else None
+        self.prefill = None
+        pages = -(-L // PAGE)
+        self.ws_snap = se.workspace(se.se_snapkv_workspace(B, Hkv, Hq, w.window, L), device)
+        for g in range(self.groups):
+            inp = synth.snapkv_inputs(w, g)
+            if keep_inputs:
+                self.inputs.append(inp)
+            bt, num_pages = synth.block_table(w.seed, f"{w.name}/g{g}/block_table",
+                                              np.full(B, pages))
+            K, V = paged_layout(list(inp["k"]), list(inp["v"]), np.full(B, L), bt, num_pages,
+                                Hkv, D)
+            pre = se.PagedKV(k=to_dev_bf16(K, device), v=to_dev_bf16(V, device),
+                             meta=torch.zeros(1, dtype=torch.bfloat16, device=device),
+                             block_table=torch.from_numpy(bt).to(device),
+                             ctx_len=torch.full((B,), L, dtype=torch.int32, device=device))
+            del K, V
+            q_win = to_dev_bf16(inp["q_win"], device)
+            self.compact_group(g, pre, q_win)
+            if g == self.groups - 1:
+                self.prefill, self.q_win = pre, q_win      # last group kept for timing
+            torch.cuda.synchronize()
+        dec = synth.snapkv_decode_inputs(w)
+        self.q = to_dev_bf16(dec["q"], device)
+        self.k_new = to_dev_bf16(dec["k_new"], device)
+        self.v_new = to_dev_bf16(dec["v_new"], device)
+        self.dec_inputs = dec if keep_inputs else None
+        units = self.Bt * Hkv
+        self.view = se.View.empty(units, -(-self.seg_cap // PAGE), device)
+        self.ws_small = se.workspace(se.se_small_workspace(), device)
+        self.ws_dec = se.workspace(se.se_sparse_decode_workspace(units, self.G, D, self.max_splits),
+                                   device)
+        self.out = torch.zeros(self.Bt, Hq, D, dtype=torch.bfloat16, device=device)
+        self.lse = torch.zeros(self.Bt, Hq, dtype=torch.float32, device=device)
+
+    def group_slice(self, g) -> se.VarlenKV:
+        """The varlen cache restricted to compaction group g's units."""
+        c, B, H = self.cache, self.B, self.Hkv
+        return se.VarlenKV(c.k, c.v, c.pos, c.score, c.seg_off[g * B * H:(g + 1) * B * H],
+                           c.seg_len[g * B * H:(g + 1) * B * H], c.seq_len[g * B:(g + 1) * B],
+                           c.seg_cap, H)
+
+    def compact_group(self, g, prefill, q_win):
+        w = self.w
+        se.se_snapkv_compact(prefill, q_win, self.B, self.Hq, w.window, w.pool_kernel, w.keep,
+                             w.window, self.scale, self.group_slice(g), self.ws_snap)
+
+    def step(self, s, ev_begin=None, ev_end=None):
+        se.se_varlen_append(self.cache, self.k_new[s], self.v_new[s], self.Bt, self.ws_small)
+        se.se_view_from_segments(self.cache, self.Bt, self.view, self.ws_small)
+        se.se_sparse_decode(self.cache.k, self.cache.v, self.view, self.q[s], self.Bt, self.Hq,
+                            self.Hkv, self.D, self.scale, self.out, self.lse, self.ws_dec,
+                            max_splits=self.max_splits, ev_begin=ev_begin, ev_end=ev_end)
+
+    def status(self) -> int:
+        return se.status_word(self.ws_small) | se.status_word(self.ws_snap) | \
+            se.status_word(self.ws_dec)
