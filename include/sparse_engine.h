@@ -131,11 +131,11 @@ typedef struct se_varlen_kv {
     int32_t head_dim;
 } se_varlen_kv;
 
-/* H2O state: a varlen cache whose segments hold at most budget+1 slots, with
- * scores, plus the slot freed by the last eviction. */
+/* H2O state: a varlen cache with scores.  Unit u holds its tokens in slots
+ * [0, seg_len[u]) of its segment, in no particular order (an eviction moves the
+ * segment's last token into the freed slot); seg_cap must be >= budget + 1. */
 typedef struct se_h2o_state {
-    se_varlen_kv kv;          /* seg_cap >= budget + 1, score != NULL */
-    int32_t* free_slot;       /* int32 [num_units]: slot of the next token when full */
+    se_varlen_kv kv;          /* score != NULL */
     int32_t budget;           /* tokens kept after each step */
     int32_t recent;           /* newest positions never evicted (1 <= recent <= budget) */
 } se_h2o_state;
@@ -272,16 +272,16 @@ int se_snapkv_compact(const se_paged_kv* prefill, const void* q_win, int batch, 
  * every decode step, then a physical deletion) -----------------------------------
  * For each unit u = (b, h):
  *   1. the new token (k_new/v_new bf16 [batch][num_kv_heads][head_dim]) goes to slot
- *      seg_len[u] while seg_len[u] < seg_cap, else to free_slot[u], with
- *      pos = seq_len[b] and score 0;
+ *      seg_len[u] with pos = seq_len[b] and score 0;
  *   2. decode attention of q (bf16 [batch][num_q_heads][head_dim]) over all held
  *      tokens -> out (bf16 or fp32 per out_dtype), lse (fp32, NULL allowed);
  *   3. score[t] += sum_g exp(s[g,t] - lse[g]) for every held token t;
  *   4. if more than `budget` tokens are held: among tokens whose position is not
  *      one of the `recent` largest, the last under (score desc, position asc) --
- *      the lowest score, the higher position on equal scores -- is evicted; its
- *      slot becomes free_slot[u] and its position goes to evicted_pos[u] (else -1).
- * seq_len[b] is incremented.  Positions stay unique per unit.
+ *      the lowest score, the higher position on equal scores -- is evicted: its
+ *      position goes to evicted_pos[u] (else -1) and the segment's last token
+ *      moves into its slot.
+ * seq_len[b] is incremented.  Positions must be unique per unit.
  * Workspace: se_h2o_workspace(batch, num_kv_heads, num_q_heads, head_dim, seg_cap). */
 int se_h2o_step(const se_h2o_state* st, const void* q, const void* k_new, const void* v_new,
                 int batch, int num_q_heads, float scale, int out_dtype, void* out, float* lse,

@@ -45,8 +45,7 @@ class VarlenKVC(ctypes.Structure):
 
 
 class H2OStateC(ctypes.Structure):
-    _fields_ = [("kv", VarlenKVC), ("free_slot", ctypes.c_void_p),
-                ("budget", ctypes.c_int32), ("recent", ctypes.c_int32)]
+    _fields_ = [("kv", VarlenKVC), ("budget", ctypes.c_int32), ("recent", ctypes.c_int32)]
 
 
 class DecodeOptsC(ctypes.Structure):
@@ -194,14 +193,13 @@ class VarlenKV:
 
 @dataclasses.dataclass
 class H2OState:
-    kv: VarlenKV
-    free_slot: torch.Tensor    # int32 [units]
+    kv: VarlenKV               # with score
     budget: int
     recent: int
 
     @property
     def c(self) -> H2OStateC:
-        return H2OStateC(self.kv.c, _p(self.free_slot), self.budget, self.recent)
+        return H2OStateC(self.kv.c, self.budget, self.recent)
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:

@@ -227,8 +227,6 @@ int se_varlen_append(const se_varlen_kv* kv, const void* k_new, const void* v_ne
                                             static_cast<cudaStream_t>(stream)));
 }
 
-// Not yet implemented: the H2O step.
-size_t se_h2o_workspace(int, int, int, int, int) { return 256; }
 size_t se_snapkv_workspace(int batch, int num_kv_heads, int num_q_heads, int window,
                            int max_ctx) {
     (void)num_q_heads;
@@ -269,9 +267,37 @@ int se_snapkv_compact(const se_paged_kv* prefill, const void* q_win, int batch, 
                                              pool_kernel, keep, recent, scale, *out, ws,
                                              (int)max_ctx, static_cast<cudaStream_t>(stream)));
 }
-int se_h2o_step(const se_h2o_state*, const void*, const void*, const void*, int, int, float, int,
-                void*, float*, int32_t*, void*, size_t, se_stream_t) {
-    return SE_ERR_UNSUPPORTED;
+
+size_t se_h2o_workspace(int batch, int num_kv_heads, int num_q_heads, int head_dim, int seg_cap) {
+    if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads ||
+        seg_cap < 0 || !head_dim_ok(head_dim))
+        return 0;
+    return h2o_ws_bytes(batch, num_kv_heads, num_q_heads, head_dim, seg_cap);
+}
+
+int se_h2o_step(const se_h2o_state* st, const void* q, const void* k_new, const void* v_new,
+                int batch, int num_q_heads, float scale, int out_dtype, void* out, float* lse,
+                int32_t* evicted_pos, void* ws, size_t ws_bytes, se_stream_t stream) {
+    if (!st) return SE_ERR_INVALID_ARG;
+    int rc = check_varlen(&st->kv);
+    if (rc) return rc;
+    const se_varlen_kv& kv = st->kv;
+    if (!kv.score) return SE_ERR_INVALID_ARG;
+    if (batch < 0 || num_q_heads <= 0 || num_q_heads % kv.num_kv_heads) return SE_ERR_INVALID_ARG;
+    if (!group_ok(num_q_heads / kv.num_kv_heads)) return SE_ERR_UNSUPPORTED;
+    if (st->budget < 1 || st->recent < 1 || st->recent > st->budget) return SE_ERR_INVALID_ARG;
+    if (kv.seg_cap < st->budget + 1) return SE_ERR_CAPACITY;
+    if (out_dtype != 0 && out_dtype != 1) return SE_ERR_INVALID_ARG;
+    if (batch == 0) return SE_OK;
+    if (!q || !k_new || !v_new || !out || !evicted_pos) return SE_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16))
+        return SE_ERR_INVALID_ARG;
+    if ((rc = check_ws(ws, ws_bytes, se_h2o_workspace(batch, kv.num_kv_heads, num_q_heads,
+                                                      kv.head_dim, kv.seg_cap))))
+        return rc;
+    return cuda_status(launch_h2o_step(*st, q, k_new, v_new, batch, num_q_heads, scale, out_dtype,
+                                       out, lse, evicted_pos, ws,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

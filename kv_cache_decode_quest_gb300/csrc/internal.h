@@ -54,6 +54,13 @@ cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int 
                                   int W, int pool_kernel, int keep, int recent, float scale,
                                   const se_varlen_kv& out, void* ws, int max_ctx, cudaStream_t s);
 
+// ---- h2o.cu ----
+size_t h2o_ws_bytes(int batch, int Hkv, int Hq, int D, int seg_cap);
+cudaError_t launch_h2o_step(const se_h2o_state& st, const void* q, const void* k_new,
+                            const void* v_new, int batch, int Hq, float scale, int out_dtype,
+                            void* out, float* lse, int32_t* evicted_pos, void* ws,
+                            cudaStream_t s);
+
 // ---- tensor maps (api.cu) ----
 // 2-D bf16 map over [rows][head_dim] with 16-row x 64-column boxes, 128B swizzle.
 bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int head_dim);

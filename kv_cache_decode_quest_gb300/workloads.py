@@ -208,3 +208,53 @@ class SnapKVRun:
     def status(self) -> int:
         return se.status_word(self.ws_small) | se.status_word(self.ws_snap) | \
             se.status_word(self.ws_dec)
+
+
+class H2ORun:
+    """H2O decode: the prefill's window column scores (pool 1) seed the scores
+    and the initial retained set (recent + best budget-recent), then one
+    se_h2o_step per decode step."""
+
+    def __init__(self, w: synth.H2OWorkload, device="cuda", keep_inputs=False, out_dtype=0):
+        self.w = w
+        B, Hq, Hkv, D, L = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.ctx
+        self.B, self.Hq, self.Hkv, self.D = B, Hq, Hkv, D
+        self.G = Hq // Hkv
+        self.scale = 1.0 / math.sqrt(D)
+        self.out_dtype = out_dtype
+        inp = synth.h2o_inputs(w)
+        self.inputs = inp if keep_inputs else None
+        pages = -(-L // PAGE)
+        bt, num_pages = synth.block_table(w.seed, w.name + "/block_table", np.full(B, pages))
+        K, V = paged_layout(list(inp["k"]), list(inp["v"]), np.full(B, L), bt, num_pages, Hkv, D)
+        pre = se.PagedKV(k=to_dev_bf16(K, device), v=to_dev_bf16(V, device),
+                         meta=torch.zeros(1, dtype=torch.bfloat16, device=device),
+                         block_table=torch.from_numpy(bt).to(device),
+                         ctx_len=torch.full((B,), L, dtype=torch.int32, device=device))
+        del K, V
+        self.cap = w.budget + 1
+        cache = se.VarlenKV.empty(B, Hkv, self.cap, D, with_score=True, device=device)
+        ws = se.workspace(se.se_snapkv_workspace(B, Hkv, Hq, w.window, L), device)
+        se.se_snapkv_compact(pre, to_dev_bf16(inp["q_win"], device), B, Hq, w.window, 1,
+                             max(0, w.budget - w.recent), w.recent, self.scale, cache, ws)
+        torch.cuda.synchronize()
+        self.init_status = se.status_word(ws)
+        del pre, ws
+        self.state = se.H2OState(cache, w.budget, w.recent)
+        self.q = to_dev_bf16(inp["q"], device)
+        self.k_new = to_dev_bf16(inp["k_new"], device)
+        self.v_new = to_dev_bf16(inp["v_new"], device)
+        units = B * Hkv
+        self.ws = se.workspace(se.se_h2o_workspace(B, Hkv, Hq, D, self.cap), device)
+        odt = torch.float32 if out_dtype == 1 else torch.bfloat16
+        self.out = torch.zeros(B, Hq, D, dtype=odt, device=device)
+        self.lse = torch.zeros(B, Hq, dtype=torch.float32, device=device)
+        self.evicted = torch.zeros(units, dtype=torch.int32, device=device)
+
+    def step(self, s, ev_begin=None, ev_end=None):
+        se.se_h2o_step(self.state, self.q[s], self.k_new[s], self.v_new[s], self.B, self.Hq,
+                       self.scale, self.out, self.lse, self.evicted, self.ws,
+                       out_dtype=self.out_dtype)
+
+    def status(self) -> int:
+        return self.init_status | se.status_word(self.ws)
