@@ -370,9 +370,54 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
-def run_extras(args, device, peak):
+def timed_steps(step, K, W, flush, before=None):
+    """W untimed then K timed calls of step(i, ev_begin, ev_end); the L2 is
+    flushed before each.  Returns (step ms list, kernel ms list or None)."""
+    import torch
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for i in range(W):
+        if before:
+            before(i)
+        flush.zero_()
+        step(i, None, None)
+    torch.cuda.synchronize()
+    evs = []
+    for i in range(W, W + K):
+        if before:
+            before(i)
+        flush.zero_()
+        e = (E(), E(), E(), E())
+        e[2].record()
+        e[3].record()
+        e[0].record()
+        step(i, e[2], e[3])
+        e[1].record()
+        evs.append(e)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b, _, _ in evs], [c.elapsed_time(d) for _, _, c, d in evs]
+
+
+EXTRAS = ("ragged_quest_128k", "snapkv_32k", "h2o_16k")
+
+
+def run_extras(args, device, peak, only=None):
     """The other workloads of the path, timed the same way (reported beside the headline)."""
+    import torch
     out = {}
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    want = set(EXTRAS if only is None else [only])
+    # ragged 64K-128K Quest decode (half dense-equivalent), split-K up to 64
+    if "ragged_quest_128k" in want:
+        ragged(out, device, peak)
+    if "snapkv_32k" in want:
+        snapkv(out, device, peak, flush)
+    if "h2o_16k" in want:
+        h2o(out, device, peak, flush)
+    return out
+
+
+def ragged(out, device, peak):
+    import torch
     qb = QuestBench("ragged_quest_128k", device)
     K = min(16, qb.w.steps)
     step_ms, kern_ms, idx = qb.timed(K, 3)
@@ -386,9 +431,83 @@ def run_extras(args, device, peak):
         "step_gbs": round(sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9, 1),
         "steps": K, "warmup": 3}
     del qb
-    import torch
     torch.cuda.empty_cache()
-    return out
+
+
+def snapkv(out, device, peak, flush):
+    """SnapKV: compaction of a batch of 8 x 32K prefills, then decode of the
+    64 compacted requests (8 seeded compaction batches)."""
+    import torch
+    from kv_cache_decode_quest_gb300 import binding as se
+    from kv_cache_decode_quest_gb300 import synth, workloads
+    w = synth.workloads()["snapkv_32k"]
+    sr = workloads.SnapKVRun(w, device=device)
+    scratch = se.VarlenKV.empty(w.batch, w.num_kv_heads, sr.seg_cap, w.head_dim, device=device)
+
+    def compact(i, e0, e1):
+        if e0 is not None:
+            e0.record()
+        se.se_snapkv_compact(sr.prefill, sr.q_win, w.batch, w.num_q_heads, w.window,
+                             w.pool_kernel, w.keep, w.window, sr.scale, scratch, sr.ws_snap)
+        if e1 is not None:
+            e1.record()
+    c_ms, _ = timed_steps(compact, 5, 3, flush)
+    Bh = w.batch * w.num_kv_heads
+    L, D, G = w.ctx, w.head_dim, w.num_q_heads // w.num_kv_heads
+    kept = min(w.keep, L - w.window) + w.window
+    c_bytes = Bh * (L * D * 2 + 2 * kept * D * 2 * 2)       # K read once, kept K/V read + written
+    c_flops = 2 * 2 * Bh * w.window * G * L * D              # two passes of S = Q K^T
+    out["snapkv_32k_compaction"] = {
+        "ms_per_batch": round(sum(c_ms) / len(c_ms), 4),
+        "prefill_tokens_per_s": round(w.batch * L / (sum(c_ms) / len(c_ms) / 1e3), 1),
+        "algorithmic_gbs": round(c_bytes / (sum(c_ms) / len(c_ms) / 1e3) / 1e9, 1),
+        "tensor_tflops": round(c_flops / (sum(c_ms) / len(c_ms) / 1e3) / 1e12, 1),
+        "batch": w.batch, "ctx": L}
+    K2 = min(32, w.steps - 3)
+    s_ms, s_k = timed_steps(lambda i, a, b: sr.step(i, a, b), K2, 3, flush)
+    units_s = sr.Bt * w.num_kv_heads
+    # timed step j attends kept + 3 (warm-up appends) + j + 1 tokens per unit
+    kv_b = sum(units_s * (kept + 4 + j) * 2 * D * 2 for j in range(K2)) / K2
+    out["snapkv_32k_decode"] = {
+        "queries_per_s": round(sr.Bt * K2 / (sum(s_ms) / 1e3), 1),
+        "ms_per_step": round(sum(s_ms) / K2, 5),
+        "decode_gbs": round(kv_b / (sum(s_k) / len(s_k) / 1e3) / 1e9, 1),
+        "decode_frac": round(kv_b / (sum(s_k) / len(s_k) / 1e3) / 1e9 / peak, 4),
+        "batch": sr.Bt, "steps": K2, "warmup": 3}
+    del sr, scratch
+    torch.cuda.empty_cache()
+
+
+def h2o(out, device, peak, flush):
+    """H2O: 64 requests, 4096 retained of 16K, one eviction per unit per step."""
+    import torch
+    from kv_cache_decode_quest_gb300 import synth, workloads
+    w = synth.workloads()["h2o_16k"]
+    hr = workloads.H2ORun(w, device=device)
+    K3 = min(64, w.steps - 3)
+    h_ms, _ = timed_steps(lambda i, a, b: hr.step(i), K3, 3, flush)
+    units = w.batch * w.num_kv_heads
+    n = w.budget + 1
+    G = w.num_q_heads // w.num_kv_heads
+    h_bytes = units * (n * 2 * w.head_dim * 2 + n * G * 4 * 2 + n * 4 * 2)
+    out["h2o_16k"] = {
+        "queries_per_s": round(w.batch * K3 / (sum(h_ms) / 1e3), 1),
+        "ms_per_step": round(sum(h_ms) / K3, 5),
+        "step_algorithmic_gbs": round(h_bytes / (sum(h_ms) / K3 / 1e3) / 1e9, 1),
+        "step_frac": round(h_bytes / (sum(h_ms) / K3 / 1e3) / 1e9 / peak, 4),
+        "batch": w.batch, "steps": K3, "warmup": 3}
+    del hr
+    torch.cuda.empty_cache()
+
+
+def run_only(args):
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    peak, _ = peaks()
+    res = run_extras(args, "cuda:0", peak, only=args.only)
+    print(json.dumps({"only": args.only, **res}), flush=True)
 
 
 def run_reference(args):
@@ -457,11 +576,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="seconds of oracle work per host core for cpu_baseline (0 = skip)")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
+    ap.add_argument("--only", choices=EXTRAS, default=None,
+                    help="run one of the other workloads alone and print its figures")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_ours(args)
 
