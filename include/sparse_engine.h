@@ -75,8 +75,11 @@ typedef void* se_stream_t;       /* cudaStream_t */
  *   k, v   bf16 [num_pages][num_kv_heads][page_size][head_dim]: one (page, head)
  *          chunk is page_size contiguous rows of head_dim elements.  Viewed as
  *          [rows][head_dim], a token is row (page*num_kv_heads + h)*16 + slot.
- *   meta   bf16 [num_pages][num_kv_heads][2][head_dim]: per (page, head) the
- *          channel-wise min over the page's valid tokens, then the max.
+ *   meta   bf16 [batch][max_pages_per_seq][num_kv_heads][2][head_dim]: per
+ *          (sequence, LOGICAL page, head) the channel-wise min over the page's valid
+ *          tokens, then the max.  Summaries are kept in logical page order per
+ *          sequence (not by physical page) so that Quest scoring, which reads every
+ *          summary of a sequence, is one sequential stream.
  *   block_table int32 [batch][max_pages_per_seq]: physical page of each logical
  *          page (entries past a sequence's pages are never read).
  *   ctx_len int32 [batch]: tokens held per sequence (se_kv_append increments it). */
@@ -194,7 +197,8 @@ int se_kv_append(const se_paged_kv* kv, const void* k_new, const void* v_new, in
  *           view->max_chunks >= max_pages_per_seq.
  * U is evaluated in fp32 as sum_d (Q+[d]*kmax[d] + Q-[d]*kmin[d]) with
  * Q+ = sum_g max(q_g, 0), Q- = sum_g min(q_g, 0): the same value in exact
- * arithmetic.  Workspace: se_quest_select_workspace(). */
+ * arithmetic.  Limits: num_kv_heads <= 16, max_pages_per_seq <= 53248 (851968
+ * tokens), else SE_ERR_UNSUPPORTED.  Workspace: se_quest_select_workspace(). */
 int se_quest_select(const se_paged_kv* kv, const void* q, int batch, int num_q_heads,
                     const int32_t* budget_tokens, int32_t* sel_pages, int32_t* n_sel,
                     const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);

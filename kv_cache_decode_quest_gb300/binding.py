@@ -130,7 +130,7 @@ def _ref(x):
 class PagedKV:
     k: torch.Tensor            # bf16 [num_pages][Hkv][16][D]
     v: torch.Tensor
-    meta: torch.Tensor         # bf16 [num_pages][Hkv][2][D]
+    meta: torch.Tensor         # bf16 [B][max_pages][Hkv][2][D], logical page order
     block_table: torch.Tensor  # int32 [B][max_pages]
     ctx_len: torch.Tensor      # int32 [B]
 

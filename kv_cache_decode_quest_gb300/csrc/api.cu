@@ -116,7 +116,7 @@ size_t se_small_workspace(void) { return 256; }
 
 size_t se_quest_select_workspace(int batch, int num_kv_heads, int max_pages_per_seq) {
     if (batch < 0 || num_kv_heads <= 0 || max_pages_per_seq < 0) return 0;
-    return 256 + align256((size_t)batch * num_kv_heads * max_pages_per_seq * sizeof(float));
+    return quest_ws_bytes(batch * num_kv_heads, max_pages_per_seq);
 }
 
 size_t se_sparse_decode_workspace(int num_units, int group_size, int head_dim, int max_splits) {
@@ -159,12 +159,14 @@ int se_quest_select(const se_paged_kv* kv, const void* q, int batch, int num_q_h
     if (!aligned(q, 16)) return SE_ERR_INVALID_ARG;
     if (view && view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
     if (view && view->max_chunks < kv->max_pages_per_seq) return SE_ERR_CAPACITY;
+    // scoring handles up to 16 KV heads per sequence; the top-k keeps one key
+    // per page of a sequence in shared memory (at most 53248 pages)
+    if (kv->num_kv_heads > 16 || kv->max_pages_per_seq > 53248) return SE_ERR_UNSUPPORTED;
     if ((rc = check_ws(ws, ws_bytes,
                        se_quest_select_workspace(batch, kv->num_kv_heads, kv->max_pages_per_seq))))
         return rc;
-    float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
     return cuda_status(launch_quest_select(*kv, q, batch, num_q_heads, budget_tokens, sel_pages,
-                                           n_sel, *view, scores, static_cast<int*>(ws),
+                                           n_sel, *view, ws, static_cast<int*>(ws),
                                            static_cast<cudaStream_t>(stream)));
 }
 

@@ -11,7 +11,7 @@
 
 namespace se {
 
-int num_sms();                       // SMs of the current device (cached)
+int num_sms();
 
 // ---- meta.cu ----
 cudaError_t launch_page_meta_build(const se_paged_kv& kv, int batch, int* status, cudaStream_t s);
@@ -23,9 +23,10 @@ cudaError_t launch_view_from_segments(const se_varlen_kv& kv, int batch, const s
                                       int* status, cudaStream_t s);
 
 // ---- quest.cu ----
+size_t quest_ws_bytes(int units, int max_pages);
 cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch, int num_q_heads,
                                 const int32_t* budget, int32_t* sel_pages, int32_t* n_sel,
-                                const se_view& view, float* scores, int* status, cudaStream_t s);
+                                const se_view& view, void* ws, int* status, cudaStream_t s);
 
 // ---- decode.cu ----
 struct DecodeWs {

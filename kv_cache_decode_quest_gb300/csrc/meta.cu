@@ -63,7 +63,7 @@ __global__ void page_meta_build_kernel(se_paged_kv kv, int* status) {
                 mx.x[i] = fmaxf(mx.x[i], x.x[i]);
             }
         }
-        const int64_t m0 = ((int64_t)phys * H + h) * 2;
+        const int64_t m0 = (((int64_t)b * kv.max_pages_per_seq + p) * H + h) * 2;
         M[m0 * segs + sg] = pack8(mn);
         M[(m0 + 1) * segs + sg] = pack8(mx);
     }
@@ -100,7 +100,7 @@ __global__ void kv_append_kernel(se_paged_kv kv, const uint4* k_new, const uint4
             const int64_t row = ((int64_t)phys * H + h) * kPage + slot;
             K[row * segs + sg] = kw;
             V[row * segs + sg] = vw;
-            const int64_t m0 = ((int64_t)phys * H + h) * 2;
+            const int64_t m0 = (((int64_t)b * kv.max_pages_per_seq + p) * H + h) * 2;
             if (slot == 0) {
                 M[m0 * segs + sg] = kw;
                 M[(m0 + 1) * segs + sg] = kw;

@@ -60,7 +60,7 @@ class QuestRun:
         K, V = paged_layout(inputs["k"], inputs["v"], ctx, bt, num_pages, Hkv, D)
         self.kv = se.PagedKV(
             k=to_dev_bf16(K, device), v=to_dev_bf16(V, device),
-            meta=torch.zeros(num_pages, Hkv, 2, D, dtype=torch.bfloat16, device=device),
+            meta=torch.zeros(B, bt.shape[1], Hkv, 2, D, dtype=torch.bfloat16, device=device),
             block_table=torch.from_numpy(bt).to(device),
             ctx_len=torch.from_numpy(ctx.astype(np.int32)).to(device))
         del K, V
