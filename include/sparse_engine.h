@@ -197,8 +197,8 @@ int se_kv_append(const se_paged_kv* kv, const void* k_new, const void* v_new, in
  *           view->max_chunks >= max_pages_per_seq.
  * U is evaluated in fp32 as sum_d (Q+[d]*kmax[d] + Q-[d]*kmin[d]) with
  * Q+ = sum_g max(q_g, 0), Q- = sum_g min(q_g, 0): the same value in exact
- * arithmetic.  Limits: num_kv_heads <= 16, max_pages_per_seq <= 53248 (851968
- * tokens), else SE_ERR_UNSUPPORTED.  Workspace: se_quest_select_workspace(). */
+ * arithmetic.  Limit: max_pages_per_seq <= 26624 (425984 tokens), else
+ * SE_ERR_UNSUPPORTED.  Workspace: se_quest_select_workspace(). */
 int se_quest_select(const se_paged_kv* kv, const void* q, int batch, int num_q_heads,
                     const int32_t* budget_tokens, int32_t* sel_pages, int32_t* n_sel,
                     const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);

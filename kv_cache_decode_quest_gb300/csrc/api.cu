@@ -159,9 +159,9 @@ int se_quest_select(const se_paged_kv* kv, const void* q, int batch, int num_q_h
     if (!aligned(q, 16)) return SE_ERR_INVALID_ARG;
     if (view && view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
     if (view && view->max_chunks < kv->max_pages_per_seq) return SE_ERR_CAPACITY;
-    // scoring handles up to 16 KV heads per sequence; the top-k keeps one key
-    // per page of a sequence in shared memory (at most 53248 pages)
-    if (kv->num_kv_heads > 16 || kv->max_pages_per_seq > 53248) return SE_ERR_UNSUPPORTED;
+    // the top-k keeps one key and one block-table entry per page of a sequence
+    // in shared memory (at most 26624 pages)
+    if (kv->max_pages_per_seq > 26624) return SE_ERR_UNSUPPORTED;
     if ((rc = check_ws(ws, ws_bytes,
                        se_quest_select_workspace(batch, kv->num_kv_heads, kv->max_pages_per_seq))))
         return rc;

@@ -123,12 +123,26 @@ __global__ void __launch_bounds__(kDecodeThreads)
             prefetch_tmap(&tv);
         }
         uint32_t seq = 0;
+        // the next item's descriptor, token count and first 32 chunk rows are
+        // fetched while the current item streams, so an item boundary costs no
+        // dependent round trips
+        int4 nitem = make_int4(0, 0, 0, 0);
+        int nntok = 0, nrow = -1;
+        auto fetch = [&](int it) {
+            if (it >= it_end) return;
+            nitem = p.items[it];
+            nntok = unit_tokens(p, nitem.x);
+            const int32_t* c = p.chunk_row + (int64_t)nitem.x * p.max_chunks;
+            nrow = nitem.y + lane < nitem.z ? c[nitem.y + lane] : -1;
+        };
+        fetch(it_begin);
         for (int it = it_begin; it < it_end; ++it) {
-            const int4 item = p.items[it];
+            const int4 item = nitem;
             const int u = item.x;
-            const int ntok = unit_tokens(p, u);
+            const int ntok = nntok;
             const int32_t* crow = p.chunk_row + (int64_t)u * p.max_chunks;
-            int row_next = item.y + lane < item.z ? crow[item.y + lane] : -1;
+            int row_next = nrow;
+            fetch(it + 1);
             for (int cb = item.y; cb < item.z; cb += 32) {
                 const int row_l = row_next;
                 row_next = cb + 32 + lane < item.z ? crow[cb + 32 + lane] : -1;
@@ -397,15 +411,18 @@ __global__ void __launch_bounds__(kDecodeThreads)
             const int2 ui = p.unit_items[u];
             if (ctid == 0) {
                 // the CTA barrier above orders the other threads' partial writes
-                // before this thread's release (fences are cumulative)
-                __threadfence();
-                const int old = atomicAdd(&p.counters[u], 1);
+                // before this thread's release; the acquire half orders the last
+                // piece's reads of the other pieces after it (both cumulative)
+                int old;
+                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                             : "=r"(old)
+                             : "l"(p.counters + u)
+                             : "memory");
                 *last = old == ui.y - 1;
                 if (old == ui.y - 1) atomicExch(&p.counters[u], 0);
             }
             consumer_bar();
             if (*last) {
-                __threadfence();
                 const int n = min(ui.y, SE_MAX_SPLITS);
                 float* wv = ow;                         // [n][G] weights, then [G] M and L
                 for (int i = ctid; i < n * G; i += kConsumerWarps * 32)
@@ -497,7 +514,24 @@ __global__ void __launch_bounds__(1024)
         total += t;
     }
     __syncthreads();
-    const bool streamk = max_splits >= 3;
+    // One piece per CTA when possible: unit u gets max(1, floor(nc_u*grid/total))
+    // pieces (at most max_splits); if that fits the grid, every CTA streams one
+    // piece and no CTA pays a second piece's epilogue in mid-stream.
+    int fit_pieces = 0;
+    for (int base = 0; base < units; base += blockDim.x) {
+        const int u = base + threadIdx.x;
+        int pc = 0;
+        if (u < units) {
+            const int nc = chunks_of(u);
+            pc = nc == 0 ? 1
+                         : max(1, min(max_splits, min(nc, (int)((int64_t)nc * grid / max(1, total)))));
+        }
+        int t;
+        block_exclusive_scan(pc, tmp, &t);
+        fit_pieces += t;
+    }
+    const bool one_each = fit_pieces <= grid;
+    const bool streamk = !one_each && max_splits >= 3;
     int per = max(1, (total + grid - 1) / max(1, grid));
     if (streamk) per = max(per, (s_max + max_splits - 3) / (max_splits - 2));
 
@@ -513,6 +547,8 @@ __global__ void __launch_bounds__(1024)
         if (u < units) {
             if (nc == 0)
                 pieces = 1;
+            else if (one_each)
+                pieces = max(1, min(max_splits, min(nc, (int)((int64_t)nc * grid / max(1, total)))));
             else if (streamk)
                 pieces = (P + nc - 1) / per - P / per + 1;
             else
@@ -526,6 +562,9 @@ __global__ void __launch_bounds__(1024)
                 int c0, c1;
                 if (nc == 0) {
                     c0 = c1 = 0;
+                } else if (one_each) {
+                    c0 = (int)((int64_t)nc * k / pieces);
+                    c1 = (int)((int64_t)nc * (k + 1) / pieces);
                 } else if (streamk) {
                     const int g0 = k == 0 ? P : (P / per + k) * per;
                     const int g1 = min(P + nc, (P / per + k + 1) * per);
@@ -547,6 +586,10 @@ __global__ void __launch_bounds__(1024)
     // CTA c takes the items whose global start lies in [c*per, (c+1)*per);
     // the last CTA also takes anything past the end.
     for (int c = threadIdx.x; c <= grid; c += blockDim.x) {
+        if (one_each) {                                   // CTA c runs piece c (if any)
+            cta_first[c] = min(c, n);
+            continue;
+        }
         int lo = 0, hi = n;
         if (c == grid) {
             lo = n;

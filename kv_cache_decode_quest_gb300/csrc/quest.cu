@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     quest_topk_kernel(se_paged_kv kv, const int32_t* __restrict__ budget,
                       const uint32_t* __restrict__ keys_ws, int32_t* __restrict__ sel_pages,
                       int32_t* __restrict__ n_sel, se_view view, int* status) {
-    extern __shared__ uint32_t skeys[];                   // [max_pages_per_seq]
+    extern __shared__ uint32_t skeys[];                   // [max_pages_per_seq] keys, then block table
     __shared__ int hist[256];
     __shared__ int tmp[33];
     __shared__ int stat[2];
@@ -133,12 +133,13 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int n = (ctx + kPage - 1) / kPage;
     const int bud = budget[b];
     const int k = max(1, (bud < 0 ? 0 : bud) / kPage);
-    const int32_t* bt = kv.block_table + (int64_t)b * stride;
+    int32_t* bts = reinterpret_cast<int32_t*>(skeys + stride);   // block-table row in shared memory
+    for (int i = tid; i < n; i += blockDim.x) bts[i] = kv.block_table[(int64_t)b * stride + i];
     int32_t* sel = sel_pages + (int64_t)u * stride;
     int32_t* crow = view.chunk_row + (int64_t)u * view.max_chunks;
     auto emit = [&](int c, int page) {
         sel[c] = page;
-        const int phys = bt[page];
+        const int phys = bts[page];
         if (phys >= 0 && phys < kv.num_pages) {
             crow[c] = (phys * H + h) * kPage;
         } else {
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__(kTopkThreads)
         }
     };
     if (n <= k) {
+        __syncthreads();
         for (int c = tid; c < n; c += blockDim.x) emit(c, c);
         if (tid == 0) {
             n_sel[u] = n;
@@ -217,7 +219,7 @@ cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch,
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int topk_smem = kv.max_pages_per_seq * 4;
+    const int topk_smem = kv.max_pages_per_seq * 8;
     e = cudaFuncSetAttribute(quest_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              topk_smem);
     if (e != cudaSuccess) return e;
