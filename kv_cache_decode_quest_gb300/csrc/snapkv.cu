@@ -340,19 +340,26 @@ struct SkSelParams {
     se_paged_kv kv;
     se_varlen_kv out;
     const float* colsum;     // [units][max_ctx]
-    uint32_t* keys;          // [units][max_ctx]
+    uint32_t* keys;          // [units][max_ctx], used when the keys do not fit shared memory
     int max_ctx, recent, keep, pool_kernel;
+    int keys_in_smem;
     int* status;
 };
+constexpr int kGatherRows = 128;                // kept rows per gather CTA
+constexpr int kSelSmemMax = 200 * 1024;         // shared-memory key budget of the select
 
-// One CTA per unit: pooled keys, exact top-`keep` of the candidates by
-// (pooled desc, position asc), kept positions ascending + the recent window,
-// then the gather of the kept K/V rows (and their unpooled scores).
+// One CTA (1024 threads) per unit: max-pooled candidate scores -> keys (in
+// shared memory when they fit), exact top-`keep` by (pooled desc, position
+// asc) with four 8-bit radix passes, then the kept positions in ascending
+// order (each thread owns a contiguous run of candidates: two block scans
+// place them) followed by the recent window.  The rows are gathered by
+// snapkv_gather_kernel.
 __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p) {
+    extern __shared__ uint32_t skeys[];                   // [max_ctx] when keys_in_smem
     __shared__ int hist[256];
     __shared__ int tmp[33];
     __shared__ int sel[2];
-    const int H = p.kv.num_kv_heads, D = p.kv.head_dim, segs = D / 8;
+    const int H = p.kv.num_kv_heads;
     const int u = blockIdx.x, b = u / H, h = u % H;
     int L = p.kv.ctx_len[b];
     const int lim = min(p.max_ctx, p.kv.max_pages_per_seq * kPage);
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
     const int ncand = L - R;
     const int rad = p.pool_kernel / 2;
     const float* A = p.colsum + (int64_t)u * p.max_ctx;
-    uint32_t* ky = p.keys + (int64_t)u * p.max_ctx;
+    uint32_t* ky = p.keys_in_smem ? skeys : p.keys + (int64_t)u * p.max_ctx;
     for (int j = threadIdx.x; j < ncand; j += blockDim.x) {
         float mx = A[j];
         for (int t = 1; t <= rad; ++t) {
@@ -379,10 +386,10 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
     const int off = p.out.seg_off[u];
     const int cap = p.out.seg_cap;
     const int n_kept = K + R;
+    const int n = min(n_kept, cap);
     if (threadIdx.x == 0 && n_kept > cap) flag(p.status, SE_DEV_CAPACITY);
-    if (threadIdx.x == 0 && (off < 0 || (int64_t)off + min(n_kept, cap) > p.out.total_rows))
-        flag(p.status, SE_DEV_BAD_INDEX);
-    const bool off_ok = off >= 0 && (int64_t)off + min(n_kept, cap) <= p.out.total_rows;
+    const bool off_ok = off >= 0 && (int64_t)off + n <= p.out.total_rows;
+    if (threadIdx.x == 0 && !off_ok) flag(p.status, SE_DEV_BAD_INDEX);
     int32_t* pos = p.out.pos + off;
     if (off_ok) {
         if (K == ncand) {
@@ -391,48 +398,65 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
             int need_eq;
             const uint32_t T = block_radix_select([&](int i) { return ky[i]; }, ncand, K, hist, tmp,
                                                   sel, &need_eq);
-            int run_eq = 0, run_out = 0;
-            for (int base = 0; base < ncand; base += blockDim.x) {
-                const int i = base + threadIdx.x;
-                const uint32_t key = i < ncand ? ky[i] : 0u;
-                const int gt = (i < ncand && key > T) ? 1 : 0;
-                const int eq = (i < ncand && key == T) ? 1 : 0;
-                int eq_tot, take_tot;
-                const int eq_before = block_exclusive_scan(eq, tmp, &eq_tot);
-                const int take = gt || (eq && run_eq + eq_before < need_eq);
-                const int o = block_exclusive_scan(take, tmp, &take_tot);
-                if (take && run_out + o < cap) pos[run_out + o] = i;
-                run_eq += eq_tot;
-                run_out += take_tot;
+            const int per = (ncand + blockDim.x - 1) / blockDim.x;
+            const int i0 = min(ncand, threadIdx.x * per), i1 = min(ncand, i0 + per);
+            int gt = 0, eq = 0;
+            for (int i = i0; i < i1; ++i) {
+                gt += ky[i] > T;
+                eq += ky[i] == T;
+            }
+            int t1, t2;
+            int eq_before = block_exclusive_scan(eq, tmp, &t1);
+            const int take_eq = max(0, min(eq, need_eq - eq_before));
+            int o = block_exclusive_scan(gt + take_eq, tmp, &t2);
+            for (int i = i0; i < i1; ++i) {
+                const uint32_t kk = ky[i];
+                if (kk > T || (kk == T && eq_before++ < need_eq)) {
+                    if (o < cap) pos[o] = i;
+                    ++o;
+                }
             }
         }
         for (int t = threadIdx.x; t < R; t += blockDim.x)
             if (K + t < cap) pos[K + t] = ncand + t;
     }
-    __syncthreads();
-    const int n = off_ok ? min(n_kept, cap) : 0;
+    if (threadIdx.x == 0) {
+        p.out.seg_len[u] = off_ok ? n : 0;
+        if (h == 0) p.out.seq_len[b] = L;
+    }
+}
+
+// grid (row blocks, units): copies the kept rows of K and V (and their
+// unpooled scores) into the unit's varlen segment, in kept order.
+__global__ void __launch_bounds__(256) snapkv_gather_kernel(const SkSelParams p) {
+    const int H = p.kv.num_kv_heads, D = p.kv.head_dim, segs = D / 8;
+    const int u = blockIdx.y, b = u / H, h = u % H;
+    const int n = p.out.seg_len[u];
+    const int off = p.out.seg_off[u];
+    const int r0 = blockIdx.x * kGatherRows;
+    if (r0 >= n) return;
+    const int r1 = min(n, r0 + kGatherRows);
     const int32_t* bt = p.kv.block_table + (int64_t)b * p.kv.max_pages_per_seq;
+    const int32_t* pos = p.out.pos + off;
+    const float* A = p.colsum + (int64_t)u * p.max_ctx;
     const uint4* Ks = static_cast<const uint4*>(p.kv.k);
     const uint4* Vs = static_cast<const uint4*>(p.kv.v);
     uint4* Kd = static_cast<uint4*>(p.out.k);
     uint4* Vd = static_cast<uint4*>(p.out.v);
-    for (int i = threadIdx.x; i < n * segs; i += blockDim.x) {
-        const int r = i / segs, sg = i % segs;
+    for (int i = threadIdx.x; i < (r1 - r0) * segs; i += blockDim.x) {
+        const int r = r0 + i / segs, sg = i % segs;
         const int ps = pos[r];
-        const int phys = bt[ps / kPage];
-        const int64_t dst = (int64_t)off + r;
+        const int page = ps / kPage;
+        const int phys = (ps >= 0 && page < p.kv.max_pages_per_seq) ? bt[page] : -1;
         if (phys < 0 || phys >= p.kv.num_pages) {
             if (sg == 0) flag(p.status, SE_DEV_BAD_INDEX);
             continue;
         }
         const int64_t src = ((int64_t)phys * H + h) * kPage + ps % kPage;
+        const int64_t dst = (int64_t)off + r;
         Kd[dst * segs + sg] = Ks[src * segs + sg];
         Vd[dst * segs + sg] = Vs[src * segs + sg];
         if (sg == 0 && p.out.score) p.out.score[dst] = A[ps];
-    }
-    if (threadIdx.x == 0) {
-        p.out.seg_len[u] = n;
-        if (h == 0) p.out.seq_len[b] = L;
     }
 }
 
@@ -506,7 +530,18 @@ cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int 
     q.keep = keep;
     q.pool_kernel = pool_kernel;
     q.status = p.status;
-    snapkv_select_kernel<<<units, 1024, 0, s>>>(q);
+    const size_t key_bytes = (size_t)max_ctx * sizeof(uint32_t);
+    q.keys_in_smem = key_bytes <= kSelSmemMax;
+    const int smem = q.keys_in_smem ? (int)key_bytes : 0;
+    e = cudaFuncSetAttribute(snapkv_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e != cudaSuccess) return e;
+    snapkv_select_kernel<<<units, 1024, smem, s>>>(q);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int max_rows = min(out.seg_cap, max_ctx);
+    dim3 g((max_rows + kGatherRows - 1) / kGatherRows, units);
+    snapkv_gather_kernel<<<g, 256, 0, s>>>(q);
     return cudaGetLastError();
 }
 
