@@ -311,22 +311,33 @@ class QuestBench:
 
 
 def reduce_max(x, ws):
+    """Max of x over the ranks (the timed region ends when the slowest replica does)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
+def replica_value(per_rank_batch, steps, total_ms, ws):
+    """Whole-job queries/s: every rank ran its own batch for `steps` steps; the
+    job took the slowest rank's time."""
+    return ws * per_rank_batch * steps / (total_ms / 1e3)
+
+
 def barrier(ws):
     import torch
-    torch.cuda.synchronize()
+    cuda = torch.cuda.is_available()
+    if cuda:
+        torch.cuda.synchronize()
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if cuda:
+        torch.cuda.synchronize()
 
 
 def run_ours(args):
@@ -353,7 +364,7 @@ def run_ours(args):
     barrier(ws)
     total_ms = reduce_max(sum(step_ms), ws)
     ms_per_step = total_ms / args.steps
-    value = ws * B * args.steps / (total_ms / 1e3)
+    value = replica_value(B, args.steps, total_ms, ws)
     bytes_steps = [qb.bytes_for(s) for s in idx]
     step_gbs = sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9
 
@@ -364,7 +375,7 @@ def run_ours(args):
 
     e2e_ms, h2d, d2h = qb.timed_e2e(args.steps, args.warmup)
     e2e_total = reduce_max(sum(e2e_ms), ws)
-    e2e_value = ws * B * args.steps / (e2e_total / 1e3)
+    e2e_value = replica_value(B, args.steps, e2e_total, ws)
 
     extra = {}
     if args.extras:
