@@ -49,7 +49,14 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
                                  cudaEvent_t ev_begin, cudaEvent_t ev_end, void* out, float* lse,
                                  const DecodeWs& w, cudaStream_t s);
 
-// ---- snapkv.cu ----
+// ---- snapkv.cu / snapkv_tc.cu ----
+constexpr int kSnapMaxSplits = 64;      // key ranges per unit at most (partials workspace)
+constexpr int kSnapMaxSplitsTc = kSnapMaxSplits;
+// Both scoring passes on tcgen05 (head_dim 128, W*G <= 256): per-row partials
+// into part [units][splits][256] and column scores into colsum [units][max_ctx].
+cudaError_t launch_snapkv_scores_tc(const se_paged_kv& kv, const void* q_win, int batch, int Hq,
+                                    int W, float scale, float2* part, float* colsum, int max_ctx,
+                                    int* status, cudaStream_t s);
 size_t snapkv_ws_bytes(int units, int max_ctx);
 cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int batch, int Hq,
                                   int W, int pool_kernel, int keep, int recent, float scale,

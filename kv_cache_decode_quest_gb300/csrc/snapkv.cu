@@ -35,7 +35,6 @@ constexpr int kSkWarps = 8;                 // consumer warps (16*MT rows each)
 constexpr int kSkThreads = (kSkWarps + 1) * 32;
 constexpr int kSkBlockKeys = 64;            // keys per stage (4 pages)
 constexpr int kSkStages = 4;
-constexpr int kSnapMaxSplits = 64;      // key ranges per unit at most
 constexpr float kLog2eF = 1.4426950408889634f;
 
 template <int D, int MT>
@@ -511,14 +510,17 @@ cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int 
     off += al256((size_t)units * max_ctx * sizeof(float));
     uint32_t* keys = reinterpret_cast<uint32_t*>(base + off);
     p.max_ctx = max_ctx;
-    CUtensorMap tk;
-    if (!encode_rows_map(&tk, kv.k, (int64_t)kv.num_pages * H * kPage, D)) return cudaErrorInvalidValue;
     cudaError_t e;
-    const bool small = p.M <= 128;
-    if (D == 128)
-        e = small ? run_both<128, 1>(tk, p, units, s) : run_both<128, 2>(tk, p, units, s);
-    else
-        e = small ? run_both<64, 1>(tk, p, units, s) : run_both<64, 2>(tk, p, units, s);
+    if (D == 128) {
+        // the window-score contraction on the 5th-generation tensor cores
+        e = launch_snapkv_scores_tc(kv, q_win, batch, Hq, W, scale, p.part, p.colsum, max_ctx,
+                                    p.status, s);
+    } else {
+        CUtensorMap tk;
+        if (!encode_rows_map(&tk, kv.k, (int64_t)kv.num_pages * H * kPage, D))
+            return cudaErrorInvalidValue;
+        e = p.M <= 128 ? run_both<64, 1>(tk, p, units, s) : run_both<64, 2>(tk, p, units, s);
+    }
     if (e != cudaSuccess) return e;
     SkSelParams q;
     q.kv = kv;
