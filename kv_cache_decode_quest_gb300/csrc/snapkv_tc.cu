@@ -25,8 +25,8 @@ namespace {
 
 constexpr int kTcRows = 256;                       // window rows, padded
 constexpr int kTcKeys = 128;                       // keys per tile (8 pages)
-constexpr int kTcStages = 3;
-constexpr int kTcEpiWarps = 8;
+constexpr int kTcStages = 4;
+constexpr int kTcEpiWarps = 16;                    // 4 per TMEM lane quadrant
 constexpr int kTcThreads = (kTcEpiWarps + 2) * 32;  // + TMA producer warp + MMA warp
 constexpr int kQRegion = kTcRows * 128;             // one 64-column region of Q (bytes)
 constexpr int kKRegion = kTcKeys * 128;             // one 64-column region of a K tile
@@ -35,7 +35,7 @@ constexpr int kTileBytes = 2 * kKRegion;            // 32 KB
 constexpr uint32_t kTmemCols = 512;                 // 2 accumulators x 256 columns
 constexpr int kCtrlBytes = 1024;                    // barriers, TMEM slot, flags
 constexpr size_t kTcSmem = 1024 + kQBytes + (size_t)kTcStages * kTileBytes + kCtrlBytes +
-                           kTcRows * 4 /* lse */ + kTcRows * 8 /* half-merge buffer */;
+                           kTcRows * 4 /* lse */ + 4096 /* partial-merge buffer */;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct TcParams {
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     float* nlse2 = reinterpret_cast<float*>(kst + kTcStages * kTileBytes + kCtrlBytes);
-    float* halfbuf = nlse2 + kTcRows;                   // [kTcRows][2]
+    float* halfbuf = nlse2 + kTcRows;                   // 1024 floats
 
     const int H = p.kv.num_kv_heads;
     const int u = blockIdx.y, split = blockIdx.x;
@@ -135,47 +135,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == kTcEpiWarps) {
         // ------------------------------ TMA producer ------------------------------
-        if (lane == 0) {
-            prefetch_tmap(&tk);
-            const int32_t* bt = p.kv.block_table + (int64_t)b * p.kv.max_pages_per_seq;
-            uint32_t seq = 0;
-            for (int kb = t0; kb < t1; ++kb, ++seq) {
-                const int s = seq % kTcStages;
-                if (!*abort_flag && !mbar_wait(&empty[s], ((seq / kTcStages) & 1) ^ 1, abort_flag)) {
-                    *abort_flag = 1;
-                    flag(p.status, SE_DEV_TIMEOUT);
-                }
-                int rows[8], n = 0;
-                for (int pg = 0; pg < 8; ++pg) {
-                    const int page = kb * 8 + pg;
-                    rows[pg] = -1;
-                    if (page * kPage < L) {
-                        const int phys = bt[page];
-                        if (phys >= 0 && phys < p.kv.num_pages) {
-                            rows[pg] = (phys * H + h) * kPage;
-                            ++n;
-                        } else {
-                            flag(p.status, SE_DEV_BAD_INDEX);
-                        }
-                    }
-                }
-                if (n > 0 && !*abort_flag) {
-                    mbar_arrive_expect_tx(&full[s], n * 4096);
-                    uint8_t* dst = kst + s * kTileBytes;
-                    for (int pg = 0; pg < 8; ++pg) {
-                        if (rows[pg] < 0) continue;
-                        tma_load_2d(dst + pg * 2048, &tk, &full[s], 0, rows[pg]);
-                        tma_load_2d(dst + kKRegion + pg * 2048, &tk, &full[s], 64, rows[pg]);
-                    }
-                } else {
-                    mbar_arrive(&full[s]);
+        // Lane pg < 8 owns page pg of a tile: its block-table entry is read two
+        // tiles ahead, and lanes 0..15 issue the tile's 16 boxes (page lane&7,
+        // head_dim half lane>>3) together.
+        if (lane == 0) prefetch_tmap(&tk);
+        const int32_t* bt = p.kv.block_table + (int64_t)b * p.kv.max_pages_per_seq;
+        auto fetch = [&](int kb) -> int {              // -2: no page (past the tile range or L)
+            const int page = kb * 8 + (lane & 7);
+            return (kb < t1 && page * kPage < L) ? bt[page] : -2;
+        };
+        int nxt1 = fetch(t0), nxt2 = fetch(t0 + 1);
+        uint32_t seq = 0;
+        for (int kb = t0; kb < t1; ++kb, ++seq) {
+            const int s = seq % kTcStages;
+            const int cur = nxt1;
+            nxt1 = nxt2;
+            nxt2 = fetch(kb + 2);
+            int row = -1;
+            if (cur != -2) {
+                if (cur >= 0 && cur < p.kv.num_pages) {
+                    row = (cur * H + h) * kPage;
+                } else if (lane < 8) {
+                    flag(p.status, SE_DEV_BAD_INDEX);
                 }
             }
+            const int n = __popc(__ballot_sync(0xffffffffu, lane < 8 && row >= 0));
+            int go = 0;
+            if (lane == 0) {
+                go = !*abort_flag;
+                if (go && !mbar_wait(&empty[s], ((seq / kTcStages) & 1) ^ 1, abort_flag)) {
+                    *abort_flag = 1;
+                    flag(p.status, SE_DEV_TIMEOUT);
+                    go = 0;
+                }
+                if (go && n > 0) mbar_arrive_expect_tx(&full[s], n * 4096);
+                else mbar_arrive(&full[s]);
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            const int rowpg = __shfl_sync(0xffffffffu, row, lane & 7);
+            if (go && lane < 16 && rowpg >= 0) {
+                const int half = lane >> 3;
+                tma_load_2d(kst + s * kTileBytes + half * kKRegion + (lane & 7) * 2048, &tk,
+                            &full[s], half * 64, rowpg);
+            }
+        }
+        if (lane == 0) {
+            // the last stages' copies have landed before the block exits
             const uint32_t first = seq > (uint32_t)kTcStages ? seq - kTcStages : 0;
             volatile int never = 0;
             for (uint32_t q2 = first; q2 < seq; ++q2)
                 mbar_wait(&full[q2 % kTcStages], (q2 / kTcStages) & 1, &never);
         }
+        __syncwarp();
     } else if (warp == kTcEpiWarps + 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
@@ -221,9 +232,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------ epilogue warps ------------------------------
-        const int qd = warp & 3, hf = warp >> 2;
+        // warp w reads TMEM lanes 32*(w%4) .. +31 (its lane quadrant); the four
+        // warps of a quadrant split the accumulator's 256 columns four ways.
+        const int qd = warp & 3, part = warp >> 2;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        // pass 1: row t*128 + 32*qd + lane, keys hf*64 .. hf*64+63 of the tile
+        const int t = part >> 1, hf = part & 1;
+        const int row1 = t * 128 + 32 * qd + lane;
+        const int last1 = row1 < p.M ? L - p.W + (row1 >> lg) : -1;
+        float m1 = -INFINITY, l1 = 0.f;
         uint32_t seq = 0;
         for (int kb = t0; kb < t1; ++kb, ++seq) {
             const int buf = seq & 1;
@@ -236,116 +253,92 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // every window row sees every key of the tile: no per-element mask
             // (keys <= L-W are visible to all rows, and L-W < L)
             const bool full_tile = (kb + 1) * kTcKeys - 1 <= L - p.W;
+            float v[64];
+            if (live) {
+                tmem_ld64(lane_base + buf * 256 + (PASS == 1 ? t * 128 + hf * 64 : part * 64), v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) v[j] = 0.f;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);   // the accumulator is in registers
             if (PASS == 1) {
-                // rows t*128 + 32*qd + lane; this warp reads keys hf*64 .. hf*64+63
+                float mx = m1;
+                bool any = true;
+                if (full_tile) {
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int row = t * 128 + 32 * qd + lane;
-                    float v[64];
-                    if (live) {
-                        tmem_ld64(lane_base + buf * 256 + t * 128 + hf * 64, v);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 64; ++j) v[j] = 0.f;
+                    for (int j = 0; j < 64; ++j) {
+                        v[j] *= p.scale_log2;
+                        mx = fmaxf(mx, v[j]);
                     }
-                    float mx = m[t];
-                    if (full_tile) {
+                } else {
+                    const int key0 = kb * kTcKeys + hf * 64;
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) {
-                            v[j] *= p.scale_log2;
-                            mx = fmaxf(mx, v[j]);
-                        }
-                    } else {
-                        const int last = row < p.M ? L - p.W + (row >> lg) : -1;
-                        const int key0 = kb * kTcKeys + hf * 64;
-#pragma unroll
-                        for (int j = 0; j < 64; ++j) {
-                            v[j] = key0 + j <= last ? v[j] * p.scale_log2 : -INFINITY;
-                            mx = fmaxf(mx, v[j]);
-                        }
-                        if (mx == -INFINITY) continue;
+                    for (int j = 0; j < 64; ++j) {
+                        v[j] = key0 + j <= last1 ? v[j] * p.scale_log2 : -INFINITY;
+                        mx = fmaxf(mx, v[j]);
                     }
-                    float acc = l[t] * ex2_approx(m[t] - mx);
+                    any = mx != -INFINITY;
+                }
+                if (any) {
+                    float acc = l1 * ex2_approx(m1 - mx);
 #pragma unroll
                     for (int j = 0; j < 64; ++j) acc += ex2_approx(v[j] - mx);
-                    l[t] = acc;
-                    m[t] = mx;
+                    l1 = acc;
+                    m1 = mx;
                 }
             } else {
-                // key kb*128 + 32*qd + lane; this warp reads rows hf*128 .. hf*128+127
+                // key kb*128 + 32*qd + lane against rows part*64 .. part*64+63
                 const int key = kb * kTcKeys + 32 * qd + lane;
+                const float4* nl4 = reinterpret_cast<const float4*>(nlse2 + part * 64);
                 float acc = 0.f;
                 if (full_tile) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        float v[64];
-                        if (live) tmem_ld64(lane_base + buf * 256 + hf * 128 + c * 64, v);
-                        else
-#pragma unroll
-                            for (int j = 0; j < 64; ++j) v[j] = 0.f;
-                        const float4* nl4 = reinterpret_cast<const float4*>(nlse2 + hf * 128 + c * 64);
-#pragma unroll
-                        for (int j4 = 0; j4 < 16; ++j4) {
-                            const float4 nl = nl4[j4];
-                            acc += ex2_approx(fmaf(v[4 * j4], p.scale_log2, nl.x));
-                            acc += ex2_approx(fmaf(v[4 * j4 + 1], p.scale_log2, nl.y));
-                            acc += ex2_approx(fmaf(v[4 * j4 + 2], p.scale_log2, nl.z));
-                            acc += ex2_approx(fmaf(v[4 * j4 + 3], p.scale_log2, nl.w));
-                        }
+                    for (int j4 = 0; j4 < 16; ++j4) {
+                        const float4 nl = nl4[j4];
+                        acc += ex2_approx(fmaf(v[4 * j4], p.scale_log2, nl.x));
+                        acc += ex2_approx(fmaf(v[4 * j4 + 1], p.scale_log2, nl.y));
+                        acc += ex2_approx(fmaf(v[4 * j4 + 2], p.scale_log2, nl.z));
+                        acc += ex2_approx(fmaf(v[4 * j4 + 3], p.scale_log2, nl.w));
                     }
                 } else {
                     // row r sees this key iff key <= L-W + r/G, i.e. r >= G*max(0, key-(L-W))
                     const int min_row = key < L ? max(0, key - (L - p.W)) << lg : kTcRows;
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        float v[64];
-                        if (live) tmem_ld64(lane_base + buf * 256 + hf * 128 + c * 64, v);
-                        else
-#pragma unroll
-                            for (int j = 0; j < 64; ++j) v[j] = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 64; ++j) {
-                            const int row = hf * 128 + c * 64 + j;
-                            const float e = ex2_approx(fmaf(v[j], p.scale_log2, nlse2[row]));
-                            acc += row >= min_row ? e : 0.f;
-                        }
+                    for (int j = 0; j < 64; ++j) {
+                        const int row = part * 64 + j;
+                        const float e = ex2_approx(fmaf(v[j], p.scale_log2, nlse2[row]));
+                        acc += row >= min_row ? e : 0.f;
                     }
                 }
-                // the two row halves meet in shared memory (double-buffered by
+                // the four row quarters meet in shared memory (double-buffered by
                 // tile parity, so one barrier per tile suffices)
-                float* hb = halfbuf + buf * 128;
-                if (hf == 1) hb[32 * qd + lane] = acc;
+                float* hb = halfbuf + buf * 512;
+                if (part != 0) hb[part * 128 + 32 * qd + lane] = acc;
                 epi_bar();
-                if (hf == 0 && key < L) p.colsum[(int64_t)u * p.max_ctx + key] = acc + hb[32 * qd + lane];
+                if (part == 0 && key < L) {
+                    const int i = 32 * qd + lane;
+                    p.colsum[(int64_t)u * p.max_ctx + key] = acc + hb[128 + i] + hb[256 + i] + hb[384 + i];
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
         }
         if (PASS == 1) {
             // merge the two key halves of each row, then store (max, sum)
             if (hf == 1) {
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int row = t * 128 + 32 * qd + lane;
-                    halfbuf[2 * row] = m[t];
-                    halfbuf[2 * row + 1] = l[t];
-                }
+                halfbuf[2 * row1] = m1;
+                halfbuf[2 * row1 + 1] = l1;
             }
             epi_bar();
             if (hf == 0) {
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int row = t * 128 + 32 * qd + lane;
-                    const float m2 = halfbuf[2 * row], l2 = halfbuf[2 * row + 1];
-                    float mm = m[t], ll = l[t];
-                    const float mn = fmaxf(mm, m2);
-                    if (mn != -INFINITY) {
-                        ll = ll * exp2f(mm - mn) + l2 * exp2f(m2 - mn);
-                        mm = mn;
-                    }
-                    p.part[((int64_t)u * p.splits + split) * kTcRows + row] = make_float2(mm, ll);
+                const float m2 = halfbuf[2 * row1], l2 = halfbuf[2 * row1 + 1];
+                float mm = m1, ll = l1;
+                const float mn = fmaxf(mm, m2);
+                if (mn != -INFINITY) {
+                    ll = ll * exp2f(mm - mn) + l2 * exp2f(m2 - mn);
+                    mm = mn;
                 }
+                p.part[((int64_t)u * p.splits + split) * kTcRows + row1] = make_float2(mm, ll);
             }
         }
     }
