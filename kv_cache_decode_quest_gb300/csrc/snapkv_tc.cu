@@ -264,29 +264,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);   // the accumulator is in registers
             if (PASS == 1) {
-                float mx = m1;
-                bool any = true;
-                if (full_tile) {
+                float mx;
+                if (full_tile && p.scale_log2 > 0.f) {
+                    // max over the raw logits (the scale is positive), four chains
+                    float r4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        v[j] *= p.scale_log2;
-                        mx = fmaxf(mx, v[j]);
-                    }
-                } else {
-                    const int key0 = kb * kTcKeys + hf * 64;
+                    for (int j = 4; j < 64; ++j) r4[j & 3] = fmaxf(r4[j & 3], v[j]);
+                    mx = fmaxf(m1, fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3])) * p.scale_log2);
+                    const float nmx = -mx;
+                    float a4[4] = {l1 * ex2_approx(m1 - mx), 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        v[j] = key0 + j <= last1 ? v[j] * p.scale_log2 : -INFINITY;
-                        mx = fmaxf(mx, v[j]);
-                    }
-                    any = mx != -INFINITY;
-                }
-                if (any) {
-                    float acc = l1 * ex2_approx(m1 - mx);
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) acc += ex2_approx(v[j] - mx);
-                    l1 = acc;
+                    for (int j = 0; j < 64; ++j) a4[j & 3] += ex2_approx(fmaf(v[j], p.scale_log2, nmx));
+                    l1 = (a4[0] + a4[1]) + (a4[2] + a4[3]);
                     m1 = mx;
+                } else {
+                    // masked tile (or a non-positive scale): scale first, then mask
+                    const int key0 = kb * kTcKeys + hf * 64;
+                    float r4[4] = {m1, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        v[j] = (full_tile || key0 + j <= last1) ? v[j] * p.scale_log2 : -INFINITY;
+                        r4[j & 3] = fmaxf(r4[j & 3], v[j]);
+                    }
+                    mx = fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3]));
+                    if (mx != -INFINITY) {
+                        float a4[4] = {l1 * ex2_approx(m1 - mx), 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) a4[j & 3] += ex2_approx(v[j] - mx);
+                        l1 = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+                        m1 = mx;
+                    }
                 }
             } else {
                 // key kb*128 + 32*qd + lane against rows part*64 .. part*64+63
