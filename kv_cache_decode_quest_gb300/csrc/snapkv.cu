@@ -358,6 +358,7 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
     __shared__ int hist[256];
     __shared__ int tmp[33];
     __shared__ int sel[2];
+    __shared__ int wgt[32], weq[32];
     const int H = p.kv.num_kv_heads;
     const int u = blockIdx.x, b = u / H, h = u % H;
     int L = p.kv.ctx_len[b];
@@ -371,13 +372,38 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
     const int rad = p.pool_kernel / 2;
     const float* A = p.colsum + (int64_t)u * p.max_ctx;
     uint32_t* ky = p.keys_in_smem ? skeys : p.keys + (int64_t)u * p.max_ctx;
-    for (int j = threadIdx.x; j < ncand; j += blockDim.x) {
-        float mx = A[j];
-        for (int t = 1; t <= rad; ++t) {
-            if (j - t >= 0) mx = fmaxf(mx, A[j - t]);
-            if (j + t < ncand) mx = fmaxf(mx, A[j + t]);
+    const int nw = blockDim.x >> 5, wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // max-pool over [j-rad, j+rad] clipped to the candidates: a warp takes 32
+    // consecutive positions, one per lane, and its 2*rad neighbours by shuffle
+    // (lanes < rad also hold the halo on either side; rad <= 31)
+    constexpr int kPB = 8;                        // chunks whose loads are in flight together
+    for (int jb = wid * 32; jb < ncand; jb += nw * 32 * kPB) {
+        float x[kPB], hl[kPB], hr[kPB];
+#pragma unroll
+        for (int q = 0; q < kPB; ++q) {
+            const int j0 = jb + q * nw * 32, j = j0 + lane;
+            x[q] = j < ncand ? A[j] : -INFINITY;
+            hl[q] = -INFINITY;
+            hr[q] = -INFINITY;
+            if (lane < rad) {
+                const int jl = j0 - rad + lane, jr = j0 + 32 + lane;
+                if (jl >= 0 && jl < ncand) hl[q] = A[jl];
+                if (jr < ncand) hr[q] = A[jr];
+            }
         }
-        ky[j] = float_key(mx);
+#pragma unroll
+        for (int q = 0; q < kPB; ++q) {
+            const int j = jb + q * nw * 32 + lane;
+            float mx = x[q];
+            for (int t = 1; t <= rad; ++t) {
+                const float li = __shfl_sync(0xffffffffu, x[q], (lane - t) & 31);
+                const float lh = __shfl_sync(0xffffffffu, hl[q], (lane - t + rad) & 31);
+                const float ri = __shfl_sync(0xffffffffu, x[q], (lane + t) & 31);
+                const float rh = __shfl_sync(0xffffffffu, hr[q], (lane + t - 32) & 31);
+                mx = fmaxf(mx, fmaxf(lane >= t ? li : lh, lane + t < 32 ? ri : rh));
+            }
+            if (j < ncand) ky[j] = float_key(mx);
+        }
     }
     __syncthreads();
 
@@ -397,23 +423,59 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
             int need_eq;
             const uint32_t T = block_radix_select([&](int i) { return ky[i]; }, ncand, K, hist, tmp,
                                                   sel, &need_eq);
-            const int per = (ncand + blockDim.x - 1) / blockDim.x;
-            const int i0 = min(ncand, threadIdx.x * per), i1 = min(ncand, i0 + per);
+            // emit in ascending position: warp w owns a contiguous chunk read
+            // with a lane stride; ballots rank the kept keys inside the warp and
+            // a scan over the warps places each warp's run.
+            const int chunk = ((ncand + nw - 1) / nw + 31) & ~31;
+            const int c0 = min(ncand, wid * chunk), c1 = min(ncand, c0 + chunk);
             int gt = 0, eq = 0;
-            for (int i = i0; i < i1; ++i) {
-                gt += ky[i] > T;
-                eq += ky[i] == T;
-            }
-            int t1, t2;
-            int eq_before = block_exclusive_scan(eq, tmp, &t1);
-            const int take_eq = max(0, min(eq, need_eq - eq_before));
-            int o = block_exclusive_scan(gt + take_eq, tmp, &t2);
-            for (int i = i0; i < i1; ++i) {
+            for (int i = c0 + lane; i < c1; i += 32) {
                 const uint32_t kk = ky[i];
-                if (kk > T || (kk == T && eq_before++ < need_eq)) {
-                    if (o < cap) pos[o] = i;
-                    ++o;
+                gt += kk > T;
+                eq += kk == T;
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                gt += __shfl_xor_sync(0xffffffffu, gt, o);
+                eq += __shfl_xor_sync(0xffffffffu, eq, o);
+            }
+            if (lane == 0) {
+                wgt[wid] = gt;
+                weq[wid] = eq;
+            }
+            __syncthreads();
+            // lane l summarises warp l: equal keys before it, then its output offset
+            const int g_l = lane < nw ? wgt[lane] : 0, e_l = lane < nw ? weq[lane] : 0;
+            int e_incl = e_l;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, e_incl, o);
+                if (lane >= o) e_incl += y;
+            }
+            const int take_l = max(0, min(e_l, need_eq - (e_incl - e_l)));
+            int o_incl = g_l + take_l;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, o_incl, o);
+                if (lane >= o) o_incl += y;
+            }
+            int eq_seen = __shfl_sync(0xffffffffu, e_incl - e_l, wid);
+            int o = __shfl_sync(0xffffffffu, o_incl - g_l - take_l, wid);
+            const uint32_t lt = (1u << lane) - 1u;
+            for (int i0 = c0; i0 < c1; i0 += 32) {
+                const int i = i0 + lane;
+                const uint32_t kk = i < c1 ? ky[i] : 0u;
+                const bool is_eq = i < c1 && kk == T;
+                const uint32_t meq = __ballot_sync(0xffffffffu, is_eq);
+                const bool take = (i < c1 && kk > T) ||
+                                  (is_eq && eq_seen + __popc(meq & lt) < need_eq);
+                const uint32_t mt = __ballot_sync(0xffffffffu, take);
+                if (take) {
+                    const int at = o + __popc(mt & lt);
+                    if (at < cap) pos[at] = i;
                 }
+                o += __popc(mt);
+                eq_seen += __popc(meq);
             }
         }
         for (int t = threadIdx.x; t < R; t += blockDim.x)
