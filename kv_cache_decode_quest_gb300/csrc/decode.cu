@@ -41,7 +41,9 @@ struct DecShape {
     static constexpr int kStages = D == 64 ? 16 : 8;
     static_assert(kStages % kConsumerWarps == 0, "stage ownership needs kStages % 4 == 0");
     static constexpr int kHeads = NT * 8;                  // padded group
-    static constexpr int kMergeFloats = kConsumerWarps * kHeads * (D + 2);
+    // per warp: m, l and O (kHeads x D); then per-warp head weights and the LSE
+    static constexpr int kMergeFloats =
+        kConsumerWarps * kHeads * (D + 2) + (kConsumerWarps + 1) * kHeads;
     static constexpr size_t kSmem = 1024 /* alignment slack */ + (size_t)kStages * kStageBytes +
                                     (size_t)kStages * 16 /* full, empty */ +
                                     (size_t)kStages * 4 /* ntok */ + 16 /* abort */ +
@@ -375,32 +377,55 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 }
         consumer_bar();
         const int slot = item.w;
-        for (int idx = ctid; idx < G * D; idx += kConsumerWarps * 32) {
-            const int g = idx / D, d = idx % D;
+        // per head: the four warps' weights exp2(m_w - M) / L and the LSE, once
+        float* wf = mw + kConsumerWarps * S::kHeads * 2 + kConsumerWarps * S::kHeads * D;
+        if (ctid < G) {
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w * S::kHeads + g]);
-            float L = 0.f, O = 0.f;
-            if (M != -INFINITY) {
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w * S::kHeads + ctid]);
+            float f[kConsumerWarps], L = 0.f;
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float f = exp2f(mw[w * S::kHeads + g] - M);
-                    L += lw[w * S::kHeads + g] * f;
-                    O += ow[(w * S::kHeads + g) * D + d] * f;
-                }
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                f[w] = M == -INFINITY ? 0.f : exp2f(mw[w * S::kHeads + ctid] - M);
+                L += lw[w * S::kHeads + ctid] * f[w];
             }
-            const float val = L > 0.f ? O / L : 0.f;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) wf[w * S::kHeads + ctid] = f[w] * inv;
             const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
+            wf[kConsumerWarps * S::kHeads + ctid] = lse2;
+            const int64_t hq = (int64_t)b * p.Hq + h * G + ctid;
+            if (slot < 0) {
+                if (p.lse_out) p.lse_out[hq] = lse2 * kLn2;
+            } else {
+                p.lse_part[(int64_t)slot * G + ctid] = lse2;
+            }
+        }
+        consumer_bar();
+        for (int idx = ctid; idx < G * D / 4; idx += kConsumerWarps * 32) {
+            const int g = idx / (D / 4), d = (idx % (D / 4)) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float f = wf[w * S::kHeads + g];
+                const float4 x = *reinterpret_cast<const float4*>(ow + (w * S::kHeads + g) * D + d);
+                acc.x += f * x.x;
+                acc.y += f * x.y;
+                acc.z += f * x.z;
+                acc.w += f * x.w;
+            }
             const int64_t hq = (int64_t)b * p.Hq + h * G + g;
             if (slot < 0) {
-                if (p.out_f32)
-                    static_cast<float*>(p.out)[hq * D + d] = val;
-                else
-                    static_cast<uint16_t*>(p.out)[hq * D + d] = to_bf16_bits(val);
-                if (d == 0 && p.lse_out) p.lse_out[hq] = lse2 * kLn2;
+                if (p.out_f32) {
+                    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + hq * D + d) = acc;
+                } else {
+                    uint2 o2;
+                    o2.x = pack_bf16(acc.x, acc.y);
+                    o2.y = pack_bf16(acc.z, acc.w);
+                    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + hq * D + d) = o2;
+                }
             } else {
-                p.o_part[((int64_t)slot * G + g) * D + d] = val;
-                if (d == 0) p.lse_part[(int64_t)slot * G + g] = lse2;
+                *reinterpret_cast<float4*>(p.o_part + ((int64_t)slot * G + g) * D + d) = acc;
             }
         }
         consumer_bar();
@@ -423,34 +448,25 @@ __global__ void __launch_bounds__(kDecodeThreads)
             }
             consumer_bar();
             if (*last) {
+                // each thread recomputes its head's piece weights from the LSEs
+                // (n is small) while its partial rows are in flight
                 const int n = min(ui.y, SE_MAX_SPLITS);
-                float* wv = ow;                         // [n][G] weights, then [G] M and L
-                for (int i = ctid; i < n * G; i += kConsumerWarps * 32)
-                    wv[i] = __ldcg(p.lse_part + (int64_t)ui.x * G + i);
-                consumer_bar();
-                if (ctid < G) {
-                    float M = -INFINITY, L = 0.f;
-                    for (int i = 0; i < n; ++i) M = fmaxf(M, wv[i * G + ctid]);
-                    for (int i = 0; i < n; ++i) {
-                        const float f = M == -INFINITY ? 0.f : exp2f(wv[i * G + ctid] - M);
-                        wv[i * G + ctid] = f;
-                        L += f;
-                    }
-                    wv[n * G + ctid] = M;
-                    wv[n * G + G + ctid] = L;
-                }
-                consumer_bar();
                 for (int idx = ctid; idx < G * D / 4; idx += kConsumerWarps * 32) {
                     const int g = idx / (D / 4), d = (idx % (D / 4)) * 4;
-                    const float L = wv[n * G + G + g];
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float* lsrc = p.lse_part + (int64_t)ui.x * G + g;
                     const float4* src =
                         reinterpret_cast<const float4*>(p.o_part + ((int64_t)ui.x * G + g) * D + d);
                     const int64_t step = (int64_t)G * D / 4;
-#pragma unroll 8
+                    float M = -INFINITY;
+                    for (int i = 0; i < n; ++i) M = fmaxf(M, __ldcg(lsrc + (int64_t)i * G));
+                    float L = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
                     for (int i = 0; i < n; ++i) {
+                        const float x2 = __ldcg(lsrc + (int64_t)i * G);
                         const float4 x = __ldcg(src + i * step);
-                        const float f = wv[i * G + g];
+                        const float f = M == -INFINITY ? 0.f : exp2f(x2 - M);
+                        L += f;
                         acc.x += f * x.x;
                         acc.y += f * x.y;
                         acc.z += f * x.z;
@@ -462,13 +478,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
                         *reinterpret_cast<float4*>(static_cast<float*>(p.out) + hq * D + d) =
                             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
                     } else {
-                        uint2 o;
-                        o.x = pack_bf16(acc.x * inv, acc.y * inv);
-                        o.y = pack_bf16(acc.z * inv, acc.w * inv);
-                        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + hq * D + d) = o;
+                        uint2 o2;
+                        o2.x = pack_bf16(acc.x * inv, acc.y * inv);
+                        o2.y = pack_bf16(acc.z * inv, acc.w * inv);
+                        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + hq * D + d) = o2;
                     }
                     if (d == 0 && p.lse_out)
-                        p.lse_out[hq] = L > 0.f ? (wv[n * G + g] + log2f(L)) * kLn2 : -INFINITY;
+                        p.lse_out[hq] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
                 }
             }
             consumer_bar();
