@@ -19,17 +19,18 @@
 namespace se {
 namespace {
 
-constexpr int kSelWarps = 8;
-constexpr int kSelThreads = kSelWarps * 32;
-constexpr int kSelUnroll = 8;              // 16-byte loads in flight per lane
-constexpr int kSelMinBlocks = 4;           // resident scoring CTAs per SM
+constexpr int kSelWarps = 8;               // scoring warps
+constexpr int kSelThreads = (kSelWarps + 1) * 32;   // + the copy warp
+constexpr int kSelChunk = 16384;           // bytes per ring stage
+constexpr int kSelStages = 6;
+constexpr int kSelMinBlocks = 2;           // resident scoring CTAs per SM
 constexpr int kTopkThreads = 256;
+constexpr size_t kSelSmemFixed = 128 /* alignment slack */ + (size_t)kSelStages * kSelChunk +
+                                 (size_t)kSelStages * 16 /* full, empty */ + 16 /* abort */;
 
 template <int D>
 struct SelShape {
-    static constexpr int kLpp = D / 4;                 // lanes per page-head summary (512 B at D=128)
-    static constexpr int kPpw = 32 / kLpp;             // summaries per warp-wide load
-    static constexpr int kPerIter = kSelWarps * kPpw * kSelUnroll;   // summaries per CTA iteration
+    static constexpr int kSumBytes = 2 * D * 2;        // one (page, head) summary: kmin then kmax
 };
 
 __device__ __forceinline__ int clamp_ctx(int ctx, int cap, int* status, bool report) {
@@ -40,22 +41,47 @@ __device__ __forceinline__ int clamp_ctx(int ctx, int cap, int* status, bool rep
     return ctx;
 }
 
-// grid (CTAs per sequence, batch), 256 threads, one resident wave.  The page
-// summaries of a sequence are stored in logical page order, all KV heads of a
-// page together, so a CTA's range of candidate pages is one contiguous block
-// that it streams with coalesced 16-byte loads (kSelUnroll in flight per lane)
-// -- no block-table indirection.  Each (page, head) bound
-// U = sum_d Q-[d]*kmin[d] + Q+[d]*kmax[d] becomes an order-preserving key in
-// keys[unit][page].
-template <int D>
+// grid (CTAs per sequence, batch), one resident wave.  The page summaries of a
+// sequence are stored in logical page order, all KV heads of a page together,
+// so a CTA's range of candidate pages is one contiguous block of bytes: its
+// copy warp streams the block through a ring of shared-memory stages with 1-D
+// bulk copies (mbarrier completion, no block-table indirection) while the
+// scoring warps first fold the queries into Q-/Q+ and then turn each
+// (page, head) summary into U = sum_d Q-[d]*kmin[d] + Q+[d]*kmax[d] and an
+// order-preserving key in keys[unit][page].
+template <int D, int VPL, bool REG>
 __global__ void __launch_bounds__(kSelThreads, kSelMinBlocks)
     quest_score_kernel(se_paged_kv kv, const uint16_t* __restrict__ q, int Hq,
                        const int32_t* __restrict__ budget, uint32_t* __restrict__ keys_ws,
                        int* status) {
     using S = SelShape<D>;
-    extern __shared__ float coef[];                       // [H][2][D]: Q- then Q+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                               ~static_cast<uintptr_t>(127));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kSelStages * kSelChunk);
+    uint64_t* empty = full + kSelStages;
+    volatile int* abort_flag = reinterpret_cast<int*>(empty + kSelStages);
+    float* coef = reinterpret_cast<float*>(empty + kSelStages) + 4;   // [H][2][D]: Q- then Q+
     const int b = blockIdx.y, x = blockIdx.x;
     const int H = kv.num_kv_heads, G = Hq / H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // The query loads of the Q-/Q+ fold are the first memory requests of the
+    // kernel, ahead of every CTA's stage copies.  lane = g * kNdv + dv loads 8
+    // query values of group member g for d-block (task % tph) * kNdv + dv.
+    const int kNdv = 32 / G;                              // d-blocks of 8 per warp task
+    const int tph = (D / 8 + kNdv - 1) / kNdv;            // warp tasks per head
+    constexpr int kQPre = 4;                              // tasks per warp loaded up front
+    uint4 qv[kQPre];
+    auto q_load = [&](int task) {
+        const int h = task / tph, d8 = (task % tph) * kNdv + lane % kNdv, g = lane / kNdv;
+        return d8 < D / 8 ? *reinterpret_cast<const uint4*>(q + ((int64_t)b * Hq + h * G + g) * D + d8 * 8)
+                          : make_uint4(0, 0, 0, 0);
+    };
+#pragma unroll
+    for (int i = 0; i < kQPre; ++i) {
+        const int task = warp + i * kSelWarps;
+        qv[i] = (warp < kSelWarps && task < H * tph) ? q_load(task) : make_uint4(0, 0, 0, 0);
+    }
     const int stride = kv.max_pages_per_seq;
     const int ctx = clamp_ctx(kv.ctx_len[b], stride * kPage, status, threadIdx.x == 0 && x == 0);
     const int n = (ctx + kPage - 1) / kPage;
@@ -66,55 +92,163 @@ __global__ void __launch_bounds__(kSelThreads, kSelMinBlocks)
     const int per = (m + gridDim.x - 1) / gridDim.x;
     const int p_begin = x * per, p_end = min(m, p_begin + per);
     if (p_begin >= p_end) return;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < H * D; i += blockDim.x) {
-        const int h = i / D, d = i % D;
-        float lo = 0.f, hi = 0.f;
-        for (int g = 0; g < G; ++g) {
-            const uint16_t v = q[((int64_t)b * Hq + h * G + g) * D + d];
-            const float f = __uint_as_float(static_cast<uint32_t>(v) << 16);
-            lo += fminf(f, 0.f);
-            hi += fmaxf(f, 0.f);
+    const int64_t bytes = (int64_t)(p_end - p_begin) * H * S::kSumBytes;
+    const uint8_t* src = static_cast<const uint8_t*>(kv.meta) +
+                         ((int64_t)b * stride + p_begin) * H * S::kSumBytes;
+    const int nchunks = static_cast<int>((bytes + kSelChunk - 1) / kSelChunk);
+    if (warp == kSelWarps) {
+        // ------------------------------ copy warp ------------------------------
+        // It initialises the barriers, releases the scoring warps (named barrier
+        // 2, arrive only) and starts copying without waiting for them.
+        if (lane == 0) {
+            for (int s = 0; s < kSelStages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kSelWarps);
+            }
+            *abort_flag = 0;
+            fence_barrier_init();
         }
-        coef[(h * 2) * D + d] = lo;
-        coef[(h * 2 + 1) * D + d] = hi;
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" ::"r"(kSelThreads) : "memory");
+        if (lane == 0) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % kSelStages;
+                const uint32_t ph = (c / kSelStages) & 1;
+                if (!*abort_flag && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+                    *abort_flag = 1;
+                    flag(status, SE_DEV_TIMEOUT);
+                }
+                const uint32_t sz = static_cast<uint32_t>(min(static_cast<int64_t>(kSelChunk), bytes - (int64_t)c * kSelChunk));
+                if (!*abort_flag) {
+                    mbar_arrive_expect_tx(&full[s], sz);
+                    bulk_g2s(ring + s * kSelChunk, src + (int64_t)c * kSelChunk, sz, &full[s]);
+                } else {
+                    mbar_arrive(&full[s]);
+                }
+            }
+            // every copy lands before the CTA may exit
+            const int first = max(0, nchunks - kSelStages);
+            volatile int never = 0;
+            for (int c = first; c < nchunks; ++c)
+                mbar_wait(&full[c % kSelStages], (c / kSelStages) & 1, &never);
+        }
+        return;
     }
-    __syncthreads();
-    const int sub = lane % S::kLpp;                       // 16-byte segment of the summary
-    const int items = (p_end - p_begin) * H;              // page-head summaries, page-major
-    const uint4* src = static_cast<const uint4*>(kv.meta) +
-                       ((int64_t)b * stride + p_begin) * H * (D / 4);
-    for (int t0 = warp * S::kPpw * kSelUnroll; t0 < items; t0 += S::kPerIter) {
-        uint4 w[kSelUnroll];
+
+    // ------------------------------ scoring warps ------------------------------
+    asm volatile("bar.sync 2, %0;" ::"r"(kSelThreads) : "memory");   // barriers initialised
+    // Q- / Q+ per (head, d): the sums over the group are xor-shuffles across
+    // the lanes of one d-block.
+    {
+        const int g = lane / kNdv, dv = lane % kNdv;
+        int i = 0;
+        for (int task = warp; task < H * tph; task += kSelWarps, ++i) {
+            const int h = task / tph, d8 = (task % tph) * kNdv + dv;
+            uint4 v = make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int j = 0; j < kSelUnroll; ++j) {
-            const int t = t0 + j * S::kPpw + lane / S::kLpp;
-            w[j] = t < items ? __ldg(src + (int64_t)t * (D / 4) + sub) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < kSelUnroll; ++j) {
-            const int t = t0 + j * S::kPpw + lane / S::kLpp;
-            const int h = t % H, pl = t / H;
-            const float* c = coef + h * 2 * D + sub * 8;  // segments 0..D/8-1 = kmin, then kmax
-            const uint32_t a[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-            float acc = 0.f;
+            for (int j = 0; j < kQPre; ++j)
+                if (i == j) v = qv[j];
+            if (i >= kQPre) v = q_load(task);
+            const uint32_t a4[4] = {v.x, v.y, v.z, v.w};
+            float lo[8], hi[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                acc = fmaf(c[2 * i], bf_lo(a[i]), acc);
-                acc = fmaf(c[2 * i + 1], bf_hi(a[i]), acc);
+                const float f0 = bf_lo(a4[i]), f1 = bf_hi(a4[i]);
+                lo[2 * i] = fminf(f0, 0.f);
+                lo[2 * i + 1] = fminf(f1, 0.f);
+                hi[2 * i] = fmaxf(f0, 0.f);
+                hi[2 * i + 1] = fmaxf(f1, 0.f);
             }
+            for (int o = kNdv; o < 32; o <<= 1) {
 #pragma unroll
-            for (int o = S::kLpp / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (sub == 0 && t < items)
-                keys_ws[((int64_t)b * H + h) * stride + p_begin + pl] = float_key(acc);
+                for (int e = 0; e < 8; ++e) {
+                    lo[e] += __shfl_xor_sync(0xffffffffu, lo[e], o);
+                    hi[e] += __shfl_xor_sync(0xffffffffu, hi[e], o);
+                }
+            }
+            if (g == 0 && d8 < D / 8) {
+                float4* cl = reinterpret_cast<float4*>(coef + (h * 2) * D + d8 * 8);
+                float4* ch = reinterpret_cast<float4*>(coef + (h * 2 + 1) * D + d8 * 8);
+                cl[0] = make_float4(lo[0], lo[1], lo[2], lo[3]);
+                cl[1] = make_float4(lo[4], lo[5], lo[6], lo[7]);
+                ch[0] = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                ch[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
+            }
         }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kSelWarps * 32) : "memory");
+    // Each summary is read by kLps lanes, kVpl 16-byte vectors each; vector j
+    // of lane `sub` is vector j*kLps + sub of the summary (conflict-free
+    // shared-memory reads).  One warp-wide read covers kR summaries.
+    constexpr int kU4 = D / 4;                            // 16-byte vectors per summary
+    constexpr int kLps = kU4 / VPL;
+    constexpr int kR = 32 / kLps;
+    constexpr int kPerChunk = kSelChunk / S::kSumBytes;   // summaries per full stage
+    const int sub = lane % kLps, slot = lane / kLps;
+    // vector v of a summary multiplies coef[h][0][v*8..] (v < D/8: kmin by Q-)
+    // or coef[h][1][(v-D/8)*8..] (kmax by Q+): coef + h*2*D + v*8 in both cases
+    float cr[REG ? VPL * 8 : 1];
+    if (REG) {
+        const int h = slot % H;                           // fixed: kR is a multiple of H
+#pragma unroll
+        for (int j = 0; j < VPL; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cr[REG ? j * 8 + e : 0] = coef[h * 2 * D + (j * kLps + sub) * 8 + e];
+    }
+    int32_t abort_seen = 0;
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kSelStages;
+        const uint32_t ph = (c / kSelStages) & 1;
+        if (lane == 0) {
+            abort_seen = *abort_flag;
+            if (!abort_seen && !mbar_wait(&full[s], ph, abort_flag)) {
+                *abort_flag = 1;
+                flag(status, SE_DEV_TIMEOUT);
+                abort_seen = 1;
+            }
+        }
+        abort_seen = __shfl_sync(0xffffffffu, abort_seen, 0);
+        const int nsum = static_cast<int>(min(static_cast<int64_t>(kSelChunk),
+                                              bytes - (int64_t)c * kSelChunk)) /
+                         S::kSumBytes;
+        if (!abort_seen) {
+            const uint8_t* st = ring + s * kSelChunk;
+            for (int t0 = warp * kR; t0 < nsum; t0 += kSelWarps * kR) {
+                const int tl = t0 + slot;                  // summary within the stage
+                const int t = c * kPerChunk + tl;          // summary within the CTA's range
+                const int h = t % H, pl = t / H;
+                float acc = 0.f;
+                if (tl < nsum) {
+                    const uint4* sv = reinterpret_cast<const uint4*>(st + tl * S::kSumBytes);
+#pragma unroll
+                    for (int j = 0; j < VPL; ++j) {
+                        const uint4 w = sv[j * kLps + sub];
+                        const uint32_t a4[4] = {w.x, w.y, w.z, w.w};
+                        const float* cf = coef + h * 2 * D + (j * kLps + sub) * 8;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float c0 = REG ? cr[REG ? j * 8 + 2 * i : 0] : cf[2 * i];
+                            const float c1 = REG ? cr[REG ? j * 8 + 2 * i + 1 : 0] : cf[2 * i + 1];
+                            acc = fmaf(c0, bf_lo(a4[i]), acc);
+                            acc = fmaf(c1, bf_hi(a4[i]), acc);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int o = kLps / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (sub == 0 && tl < nsum)
+                    keys_ws[((int64_t)b * H + h) * stride + p_begin + pl] = float_key(acc);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
 }
 
 // One CTA (256 threads) per unit: exact top-(k-1) of pages 0..n-2 by
 // (score desc, page asc) -- four 8-bit radix passes over the unit's keys
-// staged in shared memory -- then the pages in page order (each thread owns a
-// contiguous run of candidates: two block scans place them), plus the last
+// staged in shared memory -- then the pages in page order (ballots rank them
+// inside a warp, a scan over the warps places each warp's run), plus the last
 // page, which is always selected and never scored; the AttentionView chunk of
 // each selected page is its physical page of this KV head.
 __global__ void __launch_bounds__(kTopkThreads)
@@ -125,6 +259,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     __shared__ int hist[256];
     __shared__ int tmp[33];
     __shared__ int stat[2];
+    __shared__ int wgt[32], weq[32];
     const int u = blockIdx.x, tid = threadIdx.x;
     const int H = kv.num_kv_heads;
     const int b = u / H, h = u % H;
@@ -164,20 +299,55 @@ __global__ void __launch_bounds__(kTopkThreads)
         int need_eq = 0;
         const uint32_t T = block_radix_select([&](int i) { return skeys[i]; }, m, K, hist, tmp,
                                               stat, &need_eq);
-        const int per = (m + blockDim.x - 1) / blockDim.x;
-        const int i0 = min(m, tid * per), i1 = min(m, i0 + per);
+        // pages in ascending order: warp w owns a contiguous chunk read with a
+        // lane stride; ballots rank the kept pages inside the warp and a scan
+        // over the warps places each warp's run
+        const int nw = blockDim.x >> 5, wid = tid >> 5, lane = tid & 31;
+        const int chunk = ((m + nw - 1) / nw + 31) & ~31;
+        const int c0 = min(m, wid * chunk), c1 = min(m, c0 + chunk);
         int gt = 0, eq = 0;
-        for (int i = i0; i < i1; ++i) {
-            gt += skeys[i] > T;
-            eq += skeys[i] == T;
-        }
-        int t1, t2;
-        int eq_before = block_exclusive_scan(eq, tmp, &t1);
-        const int take_eq = max(0, min(eq, need_eq - eq_before));
-        int out = block_exclusive_scan(gt + take_eq, tmp, &t2);
-        for (int i = i0; i < i1; ++i) {
+        for (int i = c0 + lane; i < c1; i += 32) {
             const uint32_t kk = skeys[i];
-            if (kk > T || (kk == T && eq_before++ < need_eq)) emit(out++, i);
+            gt += kk > T;
+            eq += kk == T;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            gt += __shfl_xor_sync(0xffffffffu, gt, o);
+            eq += __shfl_xor_sync(0xffffffffu, eq, o);
+        }
+        if (lane == 0) {
+            wgt[wid] = gt;
+            weq[wid] = eq;
+        }
+        __syncthreads();
+        const int g_l = lane < nw ? wgt[lane] : 0, e_l = lane < nw ? weq[lane] : 0;
+        int e_incl = e_l;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, e_incl, o);
+            if (lane >= o) e_incl += y;
+        }
+        const int take_l = max(0, min(e_l, need_eq - (e_incl - e_l)));
+        int o_incl = g_l + take_l;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, o_incl, o);
+            if (lane >= o) o_incl += y;
+        }
+        int eq_seen = __shfl_sync(0xffffffffu, e_incl - e_l, wid);
+        int out = __shfl_sync(0xffffffffu, o_incl - g_l - take_l, wid);
+        const uint32_t lt = (1u << lane) - 1u;
+        for (int i0 = c0; i0 < c1; i0 += 32) {
+            const int i = i0 + lane;
+            const uint32_t kk = i < c1 ? skeys[i] : 0u;
+            const bool is_eq = i < c1 && kk == T;
+            const uint32_t meq = __ballot_sync(0xffffffffu, is_eq);
+            const bool take = (i < c1 && kk > T) || (is_eq && eq_seen + __popc(meq & lt) < need_eq);
+            const uint32_t mt = __ballot_sync(0xffffffffu, take);
+            if (take) emit(out + __popc(mt & lt), i);
+            out += __popc(mt);
+            eq_seen += __popc(meq);
         }
     }
     if (tid == 0) {
@@ -202,21 +372,23 @@ cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch,
     // scoring: one resident wave of kSelMinBlocks CTAs per SM shared by the sequences
     const int per_seq = max(1, min((num_sms() * kSelMinBlocks) / batch, kv.max_pages_per_seq));
     dim3 grid(per_seq, batch);
-    const int kScoreDyn = kv.num_kv_heads * 2 * kv.head_dim * 4;
+    const int smem = static_cast<int>(kSelSmemFixed) + kv.num_kv_heads * 2 * kv.head_dim * 4;
+    // register coefficients when a warp-wide read (4 summaries at D=128 with 4
+    // vectors per lane, 8 at D=64) is a multiple of the KV head count
+    const int H = kv.num_kv_heads;
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e2 != cudaSuccess) return e2;
+        kern<<<grid, kSelThreads, smem, s>>>(kv, static_cast<const uint16_t*>(q), num_q_heads,
+                                             budget, keys, status);
+        return cudaSuccess;
+    };
     cudaError_t e;
-    if (kv.head_dim == 128) {
-        e = cudaFuncSetAttribute(quest_score_kernel<128>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreDyn);
-        if (e != cudaSuccess) return e;
-        quest_score_kernel<128><<<grid, kSelThreads, kScoreDyn, s>>>(
-            kv, static_cast<const uint16_t*>(q), num_q_heads, budget, keys, status);
-    } else {
-        e = cudaFuncSetAttribute(quest_score_kernel<64>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreDyn);
-        if (e != cudaSuccess) return e;
-        quest_score_kernel<64><<<grid, kSelThreads, kScoreDyn, s>>>(
-            kv, static_cast<const uint16_t*>(q), num_q_heads, budget, keys, status);
-    }
+    if (kv.head_dim == 128)
+        e = (4 % H == 0) ? go(quest_score_kernel<128, 4, true>) : go(quest_score_kernel<128, 1, false>);
+    else
+        e = (8 % H == 0) ? go(quest_score_kernel<64, 4, true>) : go(quest_score_kernel<64, 1, false>);
+    if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int topk_smem = kv.max_pages_per_seq * 8;

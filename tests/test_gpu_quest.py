@@ -101,8 +101,11 @@ def test_ragged_multi_step_outliers(out_dtype):
     run_and_check(w, out_dtype=out_dtype)
 
 
+# (hkv 8 at d 128 and hkv 3 at d 64 take the scoring path with coefficients in
+# shared memory; the others keep them in registers)
 @pytest.mark.parametrize("hq,hkv,d", [(4, 4, 128), (8, 4, 64), (32, 4, 128), (32, 2, 64),
-                                       (64, 4, 128), (16, 4, 64)])
+                                       (64, 4, 128), (16, 4, 64), (64, 8, 128), (6, 3, 64),
+                                       (16, 1, 128)])
 def test_group_sizes_and_head_dims(hq, hkv, d):
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name=f"quest_g{hq // hkv}_d{d}", batch=2, num_q_heads=hq,
