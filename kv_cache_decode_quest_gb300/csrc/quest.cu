@@ -245,6 +245,78 @@ __global__ void __launch_bounds__(kSelThreads, kSelMinBlocks)
     }
 }
 
+// Threshold of the top K of m order-preserving keys in shared memory (256
+// threads).  Bits above the highest bit in which the largest and smallest key
+// differ are common to all keys, so the 8-bit radix digits start there; a pass
+// ends the search early when every key of the boundary digit is kept.  On
+// return, under *mask: keys above *T are kept, and so are the first *need keys
+// equal to *T.
+__device__ void topk_threshold(const uint32_t* sk, int m, int K, int* hist, int* tmp,
+                               uint32_t* red, int* sel, uint32_t* T, uint32_t* mask, int* need) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int i = tid; i < m; i += blockDim.x) {
+        const uint32_t k = sk[i];
+        lo = min(lo, k);
+        hi = max(hi, k);
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) {
+        red[wid] = lo;
+        red[8 + wid] = hi;
+    }
+    __syncthreads();
+    lo = red[0];
+    hi = red[8];
+#pragma unroll
+    for (int w = 1; w < kTopkThreads / 32; ++w) {
+        lo = min(lo, red[w]);
+        hi = max(hi, red[8 + w]);
+    }
+    const uint32_t diff = lo ^ hi;
+    if (diff == 0u) {                                     // every key is equal
+        *T = hi;
+        *mask = 0xffffffffu;
+        *need = K;
+        return;
+    }
+    const int top = 31 - __clz(diff);                     // highest differing bit
+    uint32_t msk = top == 31 ? 0u : ~((2u << top) - 1u);
+    uint32_t prefix = hi & msk;
+    int remaining = K;
+    int low = top + 1;                                    // bits [low, 32) are decided
+    while (low > 0) {
+        const int w = min(8, low), shift = low - w;
+        const uint32_t dm = (1u << w) - 1u;
+        hist[tid] = 0;
+        __syncthreads();
+        for (int i = tid; i < m; i += blockDim.x) {
+            const uint32_t k = sk[i];
+            if ((k & msk) == prefix) atomicAdd(&hist[(k >> shift) & dm], 1);
+        }
+        __syncthreads();
+        const int v = hist[255 - tid];                    // digits in descending order
+        const int incl = scan256(v, tmp);
+        if (incl - v < remaining && incl >= remaining) {
+            sel[0] = 255 - tid;
+            sel[1] = incl - v;
+            sel[2] = v;
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(sel[0]) << shift;
+        msk |= dm << shift;
+        remaining -= sel[1];
+        low = shift;
+        const bool whole_bin = sel[2] == remaining;
+        __syncthreads();                                  // sel is rewritten by the next pass
+        if (whole_bin) break;
+    }
+    *T = prefix;
+    *mask = msk;
+    *need = remaining;
+}
+
 // One CTA (256 threads) per unit: exact top-(k-1) of pages 0..n-2 by
 // (score desc, page asc) -- four 8-bit radix passes over the unit's keys
 // staged in shared memory -- then the pages in page order (ballots rank them
@@ -258,7 +330,8 @@ __global__ void __launch_bounds__(kTopkThreads)
     extern __shared__ uint32_t skeys[];                   // [max_pages_per_seq] keys, then block table
     __shared__ int hist[256];
     __shared__ int tmp[33];
-    __shared__ int stat[2];
+    __shared__ int stat[3];
+    __shared__ uint32_t red[16];
     __shared__ int wgt[32], weq[32];
     const int u = blockIdx.x, tid = threadIdx.x;
     const int H = kv.num_kv_heads;
@@ -269,7 +342,30 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int bud = budget[b];
     const int k = max(1, (bud < 0 ? 0 : bud) / kPage);
     int32_t* bts = reinterpret_cast<int32_t*>(skeys + stride);   // block-table row in shared memory
-    for (int i = tid; i < n; i += blockDim.x) bts[i] = kv.block_table[(int64_t)b * stride + i];
+    const uint32_t* keys = keys_ws + (int64_t)u * stride;
+    const int m = n - 1;
+    // the block-table row and the candidate keys are staged with all loads
+    // of a thread in flight together
+    {
+        constexpr int kU = 8;
+        const int32_t* btr = kv.block_table + (int64_t)b * stride;
+        for (int base = tid; base < n; base += kTopkThreads * kU) {
+            int32_t bv[kU];
+            uint32_t kv2[kU];
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+                const int i = base + j * kTopkThreads;
+                bv[j] = i < n ? btr[i] : 0;
+                kv2[j] = (i < m && n > k) ? keys[i] : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+                const int i = base + j * kTopkThreads;
+                if (i < n) bts[i] = bv[j];
+                if (i < m && n > k) skeys[i] = kv2[j];
+            }
+        }
+    }
     int32_t* sel = sel_pages + (int64_t)u * stride;
     int32_t* crow = view.chunk_row + (int64_t)u * view.max_chunks;
     auto emit = [&](int c, int page) {
@@ -291,14 +387,12 @@ __global__ void __launch_bounds__(kTopkThreads)
         }
         return;
     }
-    const int m = n - 1, K = k - 1;
-    const uint32_t* keys = keys_ws + (int64_t)u * stride;
-    for (int i = tid; i < m; i += blockDim.x) skeys[i] = keys[i];
+    const int K = k - 1;
     __syncthreads();
     if (K > 0) {
         int need_eq = 0;
-        const uint32_t T = block_radix_select([&](int i) { return skeys[i]; }, m, K, hist, tmp,
-                                              stat, &need_eq);
+        uint32_t T = 0, msk = 0;
+        topk_threshold(skeys, m, K, hist, tmp, red, stat, &T, &msk, &need_eq);
         // pages in ascending order: warp w owns a contiguous chunk read with a
         // lane stride; ballots rank the kept pages inside the warp and a scan
         // over the warps places each warp's run
@@ -307,7 +401,7 @@ __global__ void __launch_bounds__(kTopkThreads)
         const int c0 = min(m, wid * chunk), c1 = min(m, c0 + chunk);
         int gt = 0, eq = 0;
         for (int i = c0 + lane; i < c1; i += 32) {
-            const uint32_t kk = skeys[i];
+            const uint32_t kk = skeys[i] & msk;
             gt += kk > T;
             eq += kk == T;
         }
@@ -340,7 +434,7 @@ __global__ void __launch_bounds__(kTopkThreads)
         const uint32_t lt = (1u << lane) - 1u;
         for (int i0 = c0; i0 < c1; i0 += 32) {
             const int i = i0 + lane;
-            const uint32_t kk = i < c1 ? skeys[i] : 0u;
+            const uint32_t kk = i < c1 ? skeys[i] & msk : 0u;
             const bool is_eq = i < c1 && kk == T;
             const uint32_t meq = __ballot_sync(0xffffffffu, is_eq);
             const bool take = (i < c1 && kk > T) || (is_eq && eq_seen + __popc(meq & lt) < need_eq);
