@@ -151,7 +151,9 @@ typedef struct se_decode_opts {
                                  scale*q.k of every attended token, view order */
     int32_t logits_stride;    /* tokens per unit in logits_out */
     void* ev_kernel_begin;    /* NULL or a cudaEvent_t recorded right before / */
-    void* ev_kernel_end;      /* right after the attention kernel (timing only) */
+    void* ev_kernel_end;      /* right after the attention kernel (timing only;
+                                 during a stream capture they are captured as
+                                 external event-record nodes of the graph) */
 } se_decode_opts;
 
 /* ---- library ------------------------------------------------------------ */

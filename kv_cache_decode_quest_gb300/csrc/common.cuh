@@ -86,6 +86,16 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may become resident before the kernel ahead of it in the
+// stream has finished: pdl_wait() returns once that kernel has completed and
+// its memory operations are visible (at once when launched without the
+// attribute), so it comes before the first global-memory access;
+// pdl_trigger() allows the next kernel in the stream to be launched.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
     const int it_begin = p.cta_first[blockIdx.x], it_end = p.cta_first[blockIdx.x + 1];
 
@@ -508,6 +510,8 @@ __global__ void __launch_bounds__(1024)
                 int* __restrict__ n_items, int* __restrict__ counters, int* status) {
     __shared__ int tmp[33];
     __shared__ int s_max;
+    pdl_wait();
+    pdl_trigger();
     const int lim = max_chunks * kPage;
     auto chunks_of = [&](int u) {
         int n = n_tokens[u];
@@ -629,8 +633,7 @@ cudaError_t run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(S::kSmem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kDecodeThreads, S::kSmem, s>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kDecodeThreads), S::kSmem, s, tk, tv, p);
 }
 
 template <int D, int NT>
@@ -694,10 +697,10 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
     const int max_items = units * max_splits;
     const int grid = max(1, min(kMaxGrid, min(max_items, num_sms() * cps)));
 
-    plan_kernel<<<1, 1024, 0, s>>>(view.n_tokens, units, view.max_chunks, max_splits, grid, w.items,
-                                   w.gstart, w.unit_items, w.cta_first, w.n_items, w.counters,
-                                   w.status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s,
+                               static_cast<const int32_t*>(view.n_tokens), units, view.max_chunks,
+                               max_splits, grid, w.items, w.gstart, w.unit_items, w.cta_first,
+                               w.n_items, w.counters, w.status);
     if (e != cudaSuccess) return e;
 
     DecodeParams p;
@@ -724,8 +727,18 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
     p.total_rows = total_rows;
     p.status = w.status;
 
+    // Inside a stream capture the timing events become event-record nodes of
+    // the graph (external records), so a replayed graph times its own kernel.
+    auto record = [&](cudaEvent_t ev) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e2 = cudaStreamIsCapturing(s, &cs);
+        if (e2 != cudaSuccess) return e2;
+        return cs == cudaStreamCaptureStatusActive
+                   ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                   : cudaEventRecord(ev, s);
+    };
     if (ev_begin) {
-        e = cudaEventRecord(ev_begin, s);
+        e = record(ev_begin);
         if (e != cudaSuccess) return e;
     }
     const bool two = out_dtype == 1;
@@ -742,7 +755,7 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
     }
     if (e != cudaSuccess) return e;
     if (ev_end) {
-        e = cudaEventRecord(ev_end, s);
+        e = record(ev_end);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

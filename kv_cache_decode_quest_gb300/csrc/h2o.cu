@@ -33,6 +33,8 @@ struct EvictParams {
 };
 
 __global__ void __launch_bounds__(1024) h2o_evict_kernel(const EvictParams p) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float s_lse[16];
     __shared__ int hist[256];
     __shared__ int tmp[33];

@@ -11,6 +11,28 @@
 
 namespace se {
 
+// Launches `kern` with programmatic stream serialization: its blocks may
+// become resident while the previous kernel in the stream runs, and wait in
+// pdl_wait() (which every kernel launched this way calls before touching
+// global memory) for that kernel to complete.  Used for the decode plan and
+// the decode kernel, small enough or resident late enough not to crowd the
+// kernel ahead of them (early-resident top-k blocks slowed the page scoring).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 int num_sms();
 
 // ---- meta.cu ----

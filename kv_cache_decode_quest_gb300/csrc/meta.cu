@@ -71,6 +71,8 @@ __global__ void page_meta_build_kernel(se_paged_kv kv, int* status) {
 
 __global__ void kv_append_kernel(se_paged_kv kv, const uint4* k_new, const uint4* v_new,
                                  int* status) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int H = kv.num_kv_heads, D = kv.head_dim, segs = D / 8;
     __shared__ int s_pos;
@@ -123,6 +125,8 @@ __global__ void kv_append_kernel(se_paged_kv kv, const uint4* k_new, const uint4
 
 __global__ void varlen_append_kernel(se_varlen_kv kv, const uint4* k_new, const uint4* v_new,
                                      int* status) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int H = kv.num_kv_heads, D = kv.head_dim, segs = D / 8;
     __shared__ int s_pos;
@@ -164,6 +168,8 @@ __global__ void varlen_append_kernel(se_varlen_kv kv, const uint4* k_new, const 
 }
 
 __global__ void view_segments_kernel(se_varlen_kv kv, se_view view, int* status) {
+    pdl_wait();
+    pdl_trigger();
     const int u = blockIdx.x;
     int len = kv.seg_len[u];
     const int lim = min(kv.seg_cap, view.max_chunks * kPage);

@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kSelThreads, kSelMinBlocks)
     const int b = blockIdx.y, x = blockIdx.x;
     const int H = kv.num_kv_heads, G = Hq / H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();
     // The query loads of the Q-/Q+ fold are the first memory requests of the
     // kernel, ahead of every CTA's stage copies.  lane = g * kNdv + dv loads 8
     // query values of group member g for d-block (task % tph) * kNdv + dv.
@@ -334,6 +336,8 @@ __global__ void __launch_bounds__(kTopkThreads)
     __shared__ uint32_t red[16];
     __shared__ int wgt[32], weq[32];
     const int u = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int H = kv.num_kv_heads;
     const int b = u / H, h = u % H;
     const int stride = kv.max_pages_per_seq;
