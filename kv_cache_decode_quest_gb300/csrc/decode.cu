@@ -625,6 +625,118 @@ __global__ void __launch_bounds__(1024)
     if (threadIdx.x == 0) *n_items = n;
 }
 
+// The same plan computed by one warp (no block barriers), for up to
+// kWarpPlanUnits units: warp scans over 32 units at a time, and cta_first
+// scattered from the items (item i starts every CTA c with
+// gstart[i-1] < c*per <= gstart[i]) instead of searched.
+constexpr int kWarpPlanUnits = 512;
+__global__ void __launch_bounds__(32)
+    plan_warp_kernel(const int32_t* __restrict__ n_tokens, int units, int max_chunks,
+                     int max_splits, int grid, int4* __restrict__ items, int* __restrict__ gstart,
+                     int2* __restrict__ unit_items, int* __restrict__ cta_first,
+                     int* __restrict__ n_items, int* __restrict__ counters, int* status) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x;
+    const int lim = max_chunks * kPage;
+    auto chunks_of = [&](int u) {
+        int n = n_tokens[u];
+        if (n < 0 || n > lim) {
+            flag(status, SE_DEV_BAD_LENGTH);
+            n = n < 0 ? 0 : lim;
+        }
+        return (n + kPage - 1) / kPage;
+    };
+    auto excl_scan = [&](int v, int* sum) {
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        *sum = __shfl_sync(0xffffffffu, x, 31);
+        return x - v;
+    };
+    int total = 0, s_max = 0;
+    for (int base = 0; base < units; base += 32) {
+        const int u = base + lane;
+        const int nc = u < units ? chunks_of(u) : 0;
+        if (u < units) counters[u] = 0;
+        total += __reduce_add_sync(0xffffffffu, nc);
+        s_max = max(s_max, __reduce_max_sync(0xffffffffu, nc));
+    }
+    auto one_each_pieces = [&](int nc) {
+        return nc == 0 ? 1
+                       : max(1, min(max_splits, min(nc, (int)((int64_t)nc * grid / max(1, total)))));
+    };
+    int fit = 0;
+    for (int base = 0; base < units; base += 32) {
+        const int u = base + lane;
+        fit += __reduce_add_sync(0xffffffffu, u < units ? one_each_pieces(chunks_of(u)) : 0);
+    }
+    const bool one_each = fit <= grid;
+    const bool streamk = !one_each && max_splits >= 3;
+    int per = max(1, (total + grid - 1) / max(1, grid));
+    if (streamk) per = max(per, (s_max + max_splits - 3) / (max_splits - 2));
+
+    int run_items = 0, run_chunks = 0;
+    for (int base = 0; base < units; base += 32) {
+        const int u = base + lane;
+        const int nc = u < units ? chunks_of(u) : 0;
+        int t_chunks, t_items;
+        const int P = run_chunks + excl_scan(nc, &t_chunks);
+        int pieces = 0;
+        if (u < units) {
+            if (nc == 0)
+                pieces = 1;
+            else if (one_each)
+                pieces = one_each_pieces(nc);
+            else if (streamk)
+                pieces = (P + nc - 1) / per - P / per + 1;
+            else
+                pieces = min(max_splits, nc);
+        }
+        const int off = run_items + excl_scan(pieces, &t_items);
+        if (u < units) {
+            unit_items[u] = make_int2(off, pieces);
+            for (int k = 0; k < pieces; ++k) {
+                int c0, c1;
+                if (nc == 0) {
+                    c0 = c1 = 0;
+                } else if (streamk) {
+                    const int g0 = k == 0 ? P : (P / per + k) * per;
+                    const int g1 = min(P + nc, (P / per + k + 1) * per);
+                    c0 = g0 - P;
+                    c1 = g1 - P;
+                } else {
+                    c0 = (int)((int64_t)nc * k / pieces);
+                    c1 = (int)((int64_t)nc * (k + 1) / pieces);
+                }
+                items[off + k] = make_int4(u, c0, c1, pieces == 1 ? -1 : off + k);
+                gstart[off + k] = P + c0;
+            }
+        }
+        run_items += t_items;
+        run_chunks += t_chunks;
+    }
+    __syncwarp();                                         // gstart is read back by other lanes
+    const int n = run_items;
+    if (one_each) {
+        for (int c = lane; c <= grid; c += 32) cta_first[c] = min(c, n);
+    } else {
+        for (int i = lane; i < n; i += 32) {
+            const int g = gstart[i];
+            const int c_lo = i == 0 ? 0 : gstart[i - 1] / per + 1;
+            const int c_hi = min(grid - 1, g / per);
+            for (int c = c_lo; c <= c_hi; ++c) cta_first[c] = i;
+        }
+        const int c_tail = n == 0 ? 0 : min(grid, gstart[n - 1] / per + 1);
+        for (int c = c_tail + lane; c <= grid; c += 32) cta_first[c] = n;
+        if (lane == 0 && n > 0) cta_first[0] = 0;
+    }
+    if (lane == 0) *n_items = n;
+}
+
 template <int D, int NT, bool TWO>
 cudaError_t run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, cudaStream_t s) {
@@ -697,10 +809,11 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
     const int max_items = units * max_splits;
     const int grid = max(1, min(kMaxGrid, min(max_items, num_sms() * cps)));
 
-    cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s,
-                               static_cast<const int32_t*>(view.n_tokens), units, view.max_chunks,
-                               max_splits, grid, w.items, w.gstart, w.unit_items, w.cta_first,
-                               w.n_items, w.counters, w.status);
+    const bool small = units <= kWarpPlanUnits;
+    cudaError_t e = launch_pdl(small ? plan_warp_kernel : plan_kernel, dim3(1), dim3(small ? 32 : 1024),
+                               0, s, static_cast<const int32_t*>(view.n_tokens), units,
+                               view.max_chunks, max_splits, grid, w.items, w.gstart, w.unit_items,
+                               w.cta_first, w.n_items, w.counters, w.status);
     if (e != cudaSuccess) return e;
 
     DecodeParams p;

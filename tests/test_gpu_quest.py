@@ -128,6 +128,27 @@ def test_split_count_does_not_change_results(max_splits):
     run_and_check(w, out_dtype=1, max_splits=max_splits)
 
 
+def test_many_units_block_plan():
+    """640 units (more than the single-warp plan takes): the block-wide plan,
+    with short ragged contexts so that some units are split and some not."""
+    base = synth.workloads()["quest_32k"]
+    B = 160
+    ctx = tuple(int(x) for x in (np.arange(B) * 37 % 900 + 20))
+    w = synth.scaled(base, name="quest_many_units", batch=B, ctx=ctx, budget=(256,) * B, steps=1)
+    run_and_check(w, units=range(0, B * 4, 7))
+
+
+def test_stream_k_plan():
+    """One 30K-token sequence among 99 short ones, every page attended: the
+    proportional one-piece-per-CTA plan does not fit the grid, so the units
+    are cut stream-K (equal chunk ranges per CTA, pieces merged by LSE)."""
+    base = synth.workloads()["quest_32k"]
+    B = 100
+    w = synth.scaled(base, name="quest_streamk", batch=B, ctx=(30000,) + (40,) * (B - 1),
+                     budget=(U32,) * B, steps=1)
+    run_and_check(w, out_dtype=1, units=[0, 1, 2, 3, 4, 5, 100, 399])
+
+
 def test_ragged_long_scaled():
     base = synth.workloads()["ragged_quest_128k"]
     w = synth.scaled(base, name="ragged_small", batch=4, ctx=(2300, 4100, 3333, 2900),
