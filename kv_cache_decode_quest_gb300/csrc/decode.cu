@@ -657,22 +657,34 @@ __global__ void __launch_bounds__(32)
         *sum = __shfl_sync(0xffffffffu, x, 31);
         return x - v;
     };
+    // Short code on purpose: right after an L2 flush every instruction line
+    // of a kernel this small is a cold fetch, so loops stay rolled.  The chunk
+    // counts are kept in shared memory between the passes.
+    __shared__ int s_nc[kWarpPlanUnits];
     int total = 0, s_max = 0;
+#pragma unroll 1
     for (int base = 0; base < units; base += 32) {
         const int u = base + lane;
         const int nc = u < units ? chunks_of(u) : 0;
-        if (u < units) counters[u] = 0;
+        if (u < units) {
+            counters[u] = 0;
+            s_nc[u] = nc;
+        }
         total += __reduce_add_sync(0xffffffffu, nc);
         s_max = max(s_max, __reduce_max_sync(0xffffffffu, nc));
     }
+    // nc * grid / total in 32-bit arithmetic when the product fits (grid <= 2048)
+    const unsigned tot1 = static_cast<unsigned>(max(1, total));
     auto one_each_pieces = [&](int nc) {
-        return nc == 0 ? 1
-                       : max(1, min(max_splits, min(nc, (int)((int64_t)nc * grid / max(1, total)))));
+        const int share = nc < (1 << 20) ? static_cast<int>(static_cast<unsigned>(nc) * grid / tot1)
+                                         : static_cast<int>((int64_t)nc * grid / tot1);
+        return nc == 0 ? 1 : max(1, min(max_splits, min(nc, share)));
     };
     int fit = 0;
+#pragma unroll 1
     for (int base = 0; base < units; base += 32) {
         const int u = base + lane;
-        fit += __reduce_add_sync(0xffffffffu, u < units ? one_each_pieces(chunks_of(u)) : 0);
+        fit += __reduce_add_sync(0xffffffffu, u < units ? one_each_pieces(s_nc[u]) : 0);
     }
     const bool one_each = fit <= grid;
     const bool streamk = !one_each && max_splits >= 3;
@@ -680,9 +692,10 @@ __global__ void __launch_bounds__(32)
     if (streamk) per = max(per, (s_max + max_splits - 3) / (max_splits - 2));
 
     int run_items = 0, run_chunks = 0;
+#pragma unroll 1
     for (int base = 0; base < units; base += 32) {
         const int u = base + lane;
-        const int nc = u < units ? chunks_of(u) : 0;
+        const int nc = u < units ? s_nc[u] : 0;
         int t_chunks, t_items;
         const int P = run_chunks + excl_scan(nc, &t_chunks);
         int pieces = 0;
@@ -699,21 +712,28 @@ __global__ void __launch_bounds__(32)
         const int off = run_items + excl_scan(pieces, &t_items);
         if (u < units) {
             unit_items[u] = make_int2(off, pieces);
+            // piece k covers chunks [floor(k*nc/pieces), floor((k+1)*nc/pieces)) in
+            // the proportional cut, stepped as k*q + floor(k*r/pieces) with
+            // nc = q*pieces + r; stream-K cuts at the multiples of per
+            const int q = nc / pieces, r = nc - q * pieces;
+            const int pb = streamk ? P / per : 0;
+            int c0 = 0, acc = 0;
+#pragma unroll 1
             for (int k = 0; k < pieces; ++k) {
-                int c0, c1;
+                int c1;
                 if (nc == 0) {
-                    c0 = c1 = 0;
+                    c1 = 0;
                 } else if (streamk) {
-                    const int g0 = k == 0 ? P : (P / per + k) * per;
-                    const int g1 = min(P + nc, (P / per + k + 1) * per);
-                    c0 = g0 - P;
-                    c1 = g1 - P;
+                    c0 = k == 0 ? 0 : (pb + k) * per - P;
+                    c1 = min(P + nc, (pb + k + 1) * per) - P;
                 } else {
-                    c0 = (int)((int64_t)nc * k / pieces);
-                    c1 = (int)((int64_t)nc * (k + 1) / pieces);
+                    acc += r;
+                    c1 = c0 + q + (acc >= pieces ? 1 : 0);
+                    if (acc >= pieces) acc -= pieces;
                 }
                 items[off + k] = make_int4(u, c0, c1, pieces == 1 ? -1 : off + k);
                 gstart[off + k] = P + c0;
+                c0 = c1;
             }
         }
         run_items += t_items;
@@ -722,6 +742,7 @@ __global__ void __launch_bounds__(32)
     __syncwarp();                                         // gstart is read back by other lanes
     const int n = run_items;
     if (one_each) {
+#pragma unroll 1
         for (int c = lane; c <= grid; c += 32) cta_first[c] = min(c, n);
     } else {
         for (int i = lane; i < n; i += 32) {
