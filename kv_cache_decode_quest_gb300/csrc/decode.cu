@@ -38,12 +38,15 @@ struct DecShape {
     static constexpr int kStageBytes = 2 * kChunkBytes;    // K chunk then V chunk
     // Stage s is always consumed by warp s % 4 (kStages is a multiple of 4), so a
     // warp never waits on a stage more than one phase ahead of its own use.
-    static constexpr int kStages = D == 64 ? 16 : 8;
+    // 192 KB of stages in flight per SM at two CTAs per SM (96 KB at G = 16,
+    // head_dim 128, where the merge area is twice as large)
+    static constexpr int kStages = D == 64 ? 24 : (NT == 1 ? 12 : 8);
     static_assert(kStages % kConsumerWarps == 0, "stage ownership needs kStages % 4 == 0");
     static constexpr int kHeads = NT * 8;                  // padded group
-    // per warp: m, l and O (kHeads x D); then per-warp head weights and the LSE
+    // per warp m and l; two weighted O slots (kHeads x D); per-warp head
+    // weights and the LSE
     static constexpr int kMergeFloats =
-        kConsumerWarps * kHeads * (D + 2) + (kConsumerWarps + 1) * kHeads;
+        kConsumerWarps * kHeads * 2 + 2 * kHeads * D + (kConsumerWarps + 1) * kHeads;
     static constexpr size_t kSmem = 1024 /* alignment slack */ + (size_t)kStages * kStageBytes +
                                     (size_t)kStages * 16 /* full, empty */ +
                                     (size_t)kStages * 4 /* ntok */ + 16 /* abort */ +
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int G = p.G;
     float* mw = merge;                                      // [4][kHeads]
     float* lw = merge + kConsumerWarps * S::kHeads;         // [4][kHeads]
-    float* ow = merge + 2 * kConsumerWarps * S::kHeads;     // [4][kHeads][D]
+    float* ow = merge + 2 * kConsumerWarps * S::kHeads;     // [2][kHeads][D]
     // ldmatrix lane roles
     const int lj = lane >> 3, lr = lane & 7;
     const int k_tok = (lj & 1) * 8 + lr, k_dof = (lj >> 1) * 8;   // K as A (token x d)
@@ -367,20 +370,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
                     lw[warp * S::kHeads + nt * 8 + 2 * cq + j] = l[nt][j];
                 }
         }
-#pragma unroll
-        for (int mt = 0; mt < KSTEPS; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int head = nt * 8 + 2 * cq + (e & 1);
-                    const int d = mt * 16 + r + ((e >> 1) << 3);
-                    ow[(warp * S::kHeads + head) * D + d] = o[mt][nt][e];
-                }
         consumer_bar();
         const int slot = item.w;
         // per head: the four warps' weights exp2(m_w - M) / L and the LSE, once
-        float* wf = mw + kConsumerWarps * S::kHeads * 2 + kConsumerWarps * S::kHeads * D;
+        float* wf = mw + kConsumerWarps * S::kHeads * 2 + 2 * S::kHeads * D;
         if (ctid < G) {
             float M = -INFINITY;
 #pragma unroll
@@ -404,18 +397,38 @@ __global__ void __launch_bounds__(kDecodeThreads)
             }
         }
         consumer_bar();
+        // weighted O in two rounds through two slots: warps 2 and 3 store
+        // theirs, warps 0 and 1 add theirs in place (half the merge area)
+        {
+            float f[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) f[nt][j] = wf[warp * S::kHeads + nt * 8 + 2 * cq + j];
+            for (int round = 0; round < 2; ++round) {
+                if ((warp >> 1) == 1 - round) {
+                    float* dst = ow + (warp & 1) * S::kHeads * D;
+#pragma unroll
+                    for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int head = nt * 8 + 2 * cq + (e & 1);
+                                const int d = mt * 16 + r + ((e >> 1) << 3);
+                                const float v = o[mt][nt][e] * f[nt][e & 1];
+                                float* at = dst + head * D + d;
+                                *at = round == 0 ? v : *at + v;
+                            }
+                }
+                consumer_bar();
+            }
+        }
         for (int idx = ctid; idx < G * D / 4; idx += kConsumerWarps * 32) {
             const int g = idx / (D / 4), d = (idx % (D / 4)) * 4;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = wf[w * S::kHeads + g];
-                const float4 x = *reinterpret_cast<const float4*>(ow + (w * S::kHeads + g) * D + d);
-                acc.x += f * x.x;
-                acc.y += f * x.y;
-                acc.z += f * x.z;
-                acc.w += f * x.w;
-            }
+            const float4 x0 = *reinterpret_cast<const float4*>(ow + g * D + d);
+            const float4 x1 = *reinterpret_cast<const float4*>(ow + (S::kHeads + g) * D + d);
+            const float4 acc = make_float4(x0.x + x1.x, x0.y + x1.y, x0.z + x1.z, x0.w + x1.w);
             const int64_t hq = (int64_t)b * p.Hq + h * G + g;
             if (slot < 0) {
                 if (p.out_f32) {
