@@ -135,9 +135,14 @@ __global__ void __launch_bounds__(kDecodeThreads)
         // dependent round trips
         int4 nitem = make_int4(0, 0, 0, 0);
         int nntok = 0, nrow = -1;
+        // item blockIdx.x is this CTA's first item whenever cta_first says so
+        // (the one-piece-per-CTA plan): it is loaded alongside cta_first, which
+        // saves a dependent round trip before the first copy (the items array
+        // holds at least grid entries, so the read stays in bounds)
+        const int4 spec = p.items[blockIdx.x];
         auto fetch = [&](int it) {
             if (it >= it_end) return;
-            nitem = p.items[it];
+            nitem = it == static_cast<int>(blockIdx.x) ? spec : p.items[it];
             nntok = unit_tokens(p, nitem.x);
             const int32_t* c = p.chunk_row + (int64_t)nitem.x * p.max_chunks;
             nrow = nitem.y + lane < nitem.z ? c[nitem.y + lane] : -1;
@@ -210,8 +215,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int v_tok = (lj >> 1) * 8 + lr, v_dof = (lj & 1) * 8;   // V^T as A (d x token)
 
     uint32_t seq = 0;
+    const int4 spec_c = p.items[blockIdx.x];               // as in the producer
     for (int it = it_begin; it < it_end; ++it) {
-        const int4 item = p.items[it];
+        const int4 item = it == static_cast<int>(blockIdx.x) ? spec_c : p.items[it];
         const int u = item.x;
         const int b = u / p.Hkv, h = u % p.Hkv;
         const int ntok = unit_tokens(p, u);
@@ -472,20 +478,23 @@ __global__ void __launch_bounds__(kDecodeThreads)
                     const float4* src =
                         reinterpret_cast<const float4*>(p.o_part + ((int64_t)ui.x * G + g) * D + d);
                     const int64_t step = (int64_t)G * D / 4;
-                    float M = -INFINITY;
-                    for (int i = 0; i < n; ++i) M = fmaxf(M, __ldcg(lsrc + (int64_t)i * G));
-                    float L = 0.f;
+                    // one pass with a running maximum: each piece's LSE and
+                    // rows are loaded together (four pieces in flight)
+                    float M = -INFINITY, L = 0.f;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
                     for (int i = 0; i < n; ++i) {
                         const float x2 = __ldcg(lsrc + (int64_t)i * G);
                         const float4 x = __ldcg(src + i * step);
-                        const float f = M == -INFINITY ? 0.f : exp2f(x2 - M);
-                        L += f;
-                        acc.x += f * x.x;
-                        acc.y += f * x.y;
-                        acc.z += f * x.z;
-                        acc.w += f * x.w;
+                        if (x2 == -INFINITY) continue;            // an empty piece
+                        const float mn = fmaxf(M, x2);
+                        const float a = exp2f(M - mn), f = exp2f(x2 - mn);
+                        L = L * a + f;
+                        acc.x = acc.x * a + f * x.x;
+                        acc.y = acc.y * a + f * x.y;
+                        acc.z = acc.z * a + f * x.z;
+                        acc.w = acc.w * a + f * x.w;
+                        M = mn;
                     }
                     const float inv = L > 0.f ? 1.f / L : 0.f;
                     const int64_t hq = (int64_t)b * p.Hq + h * G + g;
