@@ -435,7 +435,7 @@ def run_ours(args):
                                "Quest budget 2048 tokens per KV head, K with 4 outlier channels x8",
                    "global_batch": B * ws, "seq_len": 32768, "parallelism": f"replicas x{ws}",
                    "l2": "flushed (512 MiB write) before every timed step",
-                   "step": "append + Quest select (score, top-k, view) + split-K decode + merge",
+                   "step": "Quest select with the token append fused (score, top-k + append, view) + split-K decode + merge",
                    "launch": "one CUDA graph per step index, replayed"},
         "roofline": {"bound": "hbm", "kernel": "decode_kernel",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -449,7 +449,7 @@ def run_ours(args):
                      "step_frac": round(step_gbs / peak, 4)},
         "e2e": {"value": round(e2e_value, 1), "unit": "queries/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 4 * args.steps,          # score, top-k (with the append), plan, decode
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }

@@ -205,6 +205,22 @@ int se_quest_select(const se_paged_kv* kv, const void* q, int batch, int num_q_h
                     const int32_t* budget_tokens, int32_t* sel_pages, int32_t* n_sel,
                     const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);
 
+/* The decode step's append fused into the selection: the same effect as
+ * se_kv_append(kv, k_new, v_new, batch) followed by se_quest_select(...) on the
+ * same stream, in one kernel fewer.  The new token belongs to the last page,
+ * which is always selected and never scored, so the scoring only needs the
+ * new length; each top-k block writes its KV head's row and summary fold, and
+ * the last block of a sequence to finish stores ctx_len[b] + 1.
+ * k_new, v_new bf16 [batch][num_kv_heads][head_dim], 16-byte aligned; the other
+ * arguments, limits and workspace are those of se_quest_select.  No token room
+ * (ctx_len = max_pages_per_seq*16): SE_DEV_CAPACITY and nothing is appended.
+ * A block-table entry that names no page for the new token: SE_DEV_BAD_INDEX,
+ * nothing is appended and the selection for that sequence is unspecified. */
+int se_quest_select_append(const se_paged_kv* kv, const void* k_new, const void* v_new,
+                           const void* q, int batch, int num_q_heads,
+                           const int32_t* budget_tokens, int32_t* sel_pages, int32_t* n_sel,
+                           const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);
+
 /* View of whole varlen segments: chunk c of unit u starts at row seg_off[u] + 16c;
  * n_tokens[u] = seg_len[u].  Needs view->max_chunks >= ceil(seg_cap / 16).
  * Workspace: se_small_workspace(). */

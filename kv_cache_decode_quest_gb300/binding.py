@@ -67,6 +67,8 @@ SIGNATURES = {
     "se_page_meta_build": (_I, [_VP, _I, _VP, _SZ, _VP]),
     "se_kv_append": (_I, [_VP, _VP, _VP, _I, _VP, _SZ, _VP]),
     "se_quest_select": (_I, [_VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "se_quest_select_append": (_I, [_VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ,
+                                    _VP]),
     "se_view_from_segments": (_I, [_VP, _I, _VP, _VP, _SZ, _VP]),
     "se_sparse_decode": (_I, [_VP, _VP, _I64, _VP, _VP, _I, _I, _I, _I, _F, _VP, _VP, _VP,
                               _VP, _SZ, _VP]),
@@ -258,6 +260,15 @@ def se_quest_select(kv: PagedKV, q, batch: int, num_q_heads: int, budget_tokens,
     _check(load().se_quest_select(ctypes.byref(c), _p(q), batch, num_q_heads, _p(budget_tokens),
                                   _p(sel_pages), _p(n_sel), ctypes.byref(vc), _p(ws), ws.numel(),
                                   _stream(stream)), "se_quest_select")
+
+
+def se_quest_select_append(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads: int,
+                           budget_tokens, sel_pages, n_sel, view: View, ws, stream=None):
+    c, vc = kv.c, view.c
+    _check(load().se_quest_select_append(ctypes.byref(c), _p(k_new), _p(v_new), _p(q), batch,
+                                         num_q_heads, _p(budget_tokens), _p(sel_pages),
+                                         _p(n_sel), ctypes.byref(vc), _p(ws), ws.numel(),
+                                         _stream(stream)), "se_quest_select_append")
 
 
 def se_view_from_segments(kv: VarlenKV, batch: int, view: View, ws, stream=None):

@@ -46,9 +46,12 @@ cudaError_t launch_view_from_segments(const se_varlen_kv& kv, int batch, const s
 
 // ---- quest.cu ----
 size_t quest_ws_bytes(int units, int max_pages);
+// k_new / v_new non-null: the decode-step append of the new token is fused in
+// (same result as launch_kv_append followed by the selection).
 cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch, int num_q_heads,
                                 const int32_t* budget, int32_t* sel_pages, int32_t* n_sel,
-                                const se_view& view, void* ws, int* status, cudaStream_t s);
+                                const se_view& view, const void* k_new, const void* v_new,
+                                void* ws, int* status, cudaStream_t s);
 
 // ---- decode.cu ----
 struct DecodeWs {

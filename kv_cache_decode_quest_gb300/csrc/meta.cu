@@ -6,31 +6,12 @@
 // (tokendh.com article on SparseEngine, section "历史太长,会撑爆什么");
 // pages of 16 tokens with a token->page table follow the paged KV layout of
 // "长程 agent 把显存撑爆以后", section "四、为什么进不了 vLLM 一类的引擎".
+#include "append.cuh"
 #include "common.cuh"
 #include "internal.h"
 
 namespace se {
 namespace {
-
-// Each task covers 8 channels (one 16-byte vector) of one KV head.
-struct Bf8 {
-    float x[8];
-};
-__device__ __forceinline__ Bf8 unpack8(uint4 w) {
-    Bf8 r;
-    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        r.x[2 * i] = bf_lo(a[i]);
-        r.x[2 * i + 1] = bf_hi(a[i]);
-    }
-    return r;
-}
-__device__ __forceinline__ uint4 pack8(const Bf8& v) {
-    // Values are bf16-representable (min/max of bf16 inputs): rounding is exact.
-    return make_uint4(pack_bf16(v.x[0], v.x[1]), pack_bf16(v.x[2], v.x[3]),
-                      pack_bf16(v.x[4], v.x[5]), pack_bf16(v.x[6], v.x[7]));
-}
 
 __global__ void page_meta_build_kernel(se_paged_kv kv, int* status) {
     const int b = blockIdx.y, p = blockIdx.x;
@@ -74,12 +55,12 @@ __global__ void kv_append_kernel(se_paged_kv kv, const uint4* k_new, const uint4
     pdl_wait();
     pdl_trigger();
     const int b = blockIdx.x;
-    const int H = kv.num_kv_heads, D = kv.head_dim, segs = D / 8;
+    const int H = kv.num_kv_heads;
     __shared__ int s_pos;
     if (threadIdx.x == 0) s_pos = kv.ctx_len[b];
     __syncthreads();
     const int pos = s_pos;
-    const int p = pos / kPage, slot = pos % kPage;
+    const int p = pos / kPage;
     bool ok = pos >= 0 && p < kv.max_pages_per_seq;
     int phys = -1;
     if (ok) {
@@ -92,32 +73,11 @@ __global__ void kv_append_kernel(se_paged_kv kv, const uint4* k_new, const uint4
         flag(status, pos < 0 ? SE_DEV_BAD_LENGTH : SE_DEV_CAPACITY);
     }
     if (ok) {
-        uint4* K = static_cast<uint4*>(kv.k);
-        uint4* V = static_cast<uint4*>(kv.v);
-        uint4* M = static_cast<uint4*>(kv.meta);
-        for (int t = threadIdx.x; t < H * segs; t += blockDim.x) {
-            const int h = t / segs, sg = t % segs;
-            const uint4 kw = k_new[((int64_t)b * H + h) * segs + sg];
-            const uint4 vw = v_new[((int64_t)b * H + h) * segs + sg];
-            const int64_t row = ((int64_t)phys * H + h) * kPage + slot;
-            K[row * segs + sg] = kw;
-            V[row * segs + sg] = vw;
-            const int64_t m0 = (((int64_t)b * kv.max_pages_per_seq + p) * H + h) * 2;
-            if (slot == 0) {
-                M[m0 * segs + sg] = kw;
-                M[(m0 + 1) * segs + sg] = kw;
-            } else {
-                Bf8 mn = unpack8(M[m0 * segs + sg]), mx = unpack8(M[(m0 + 1) * segs + sg]);
-                const Bf8 x = unpack8(kw);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    mn.x[i] = fminf(mn.x[i], x.x[i]);
-                    mx.x[i] = fmaxf(mx.x[i], x.x[i]);
-                }
-                M[m0 * segs + sg] = pack8(mn);
-                M[(m0 + 1) * segs + sg] = pack8(mx);
-            }
-        }
+        // each head's vectors are split over blockDim / H threads
+        const int nthr = static_cast<int>(blockDim.x);
+        const int per_head = max(1, nthr / H), heads_at_once = nthr / per_head;
+        for (int h = threadIdx.x / per_head; h < H; h += heads_at_once)
+            append_head(kv, b, h, pos, phys, k_new, v_new, threadIdx.x % per_head, per_head);
     }
     __syncthreads();
     if (threadIdx.x == 0 && ok) kv.ctx_len[b] = pos + 1;

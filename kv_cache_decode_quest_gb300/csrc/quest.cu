@@ -13,6 +13,7 @@
 // so U[p] = sum_d Q+[d]*kmax[p,d] + Q-[d]*kmin[p,d] with Q+ = sum_g max(q_g,0)
 // and Q- = sum_g min(q_g,0): one 2*D-long dot product per (page, KV head),
 // which keeps the scoring a pure stream over the 2*D*2-byte page summaries.
+#include "append.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -53,7 +54,7 @@ template <int D, int VPL, bool REG>
 __global__ void __launch_bounds__(kSelThreads, kSelMinBlocks)
     quest_score_kernel(se_paged_kv kv, const uint16_t* __restrict__ q, int Hq,
                        const int32_t* __restrict__ budget, uint32_t* __restrict__ keys_ws,
-                       int* status) {
+                       int pending, int32_t* __restrict__ tickets, int* status) {
     using S = SelShape<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -85,7 +86,13 @@ __global__ void __launch_bounds__(kSelThreads, kSelMinBlocks)
         qv[i] = (warp < kSelWarps && task < H * tph) ? q_load(task) : make_uint4(0, 0, 0, 0);
     }
     const int stride = kv.max_pages_per_seq;
-    const int ctx = clamp_ctx(kv.ctx_len[b], stride * kPage, status, threadIdx.x == 0 && x == 0);
+    int ctx = clamp_ctx(kv.ctx_len[b], stride * kPage, status, threadIdx.x == 0 && x == 0);
+    // a pending append (written by the top-k kernel) counts when it fits; its
+    // page is the last one, which is never scored
+    if (pending) {
+        if (ctx < stride * kPage) ++ctx;
+        if (x == 0 && tid == 0) tickets[b] = 0;
+    }
     const int n = (ctx + kPage - 1) / kPage;
     const int bud = budget[b];
     const int k = max(1, (bud < 0 ? 0 : bud) / kPage);
@@ -328,7 +335,8 @@ __device__ void topk_threshold(const uint32_t* sk, int m, int K, int* hist, int*
 __global__ void __launch_bounds__(kTopkThreads)
     quest_topk_kernel(se_paged_kv kv, const int32_t* __restrict__ budget,
                       const uint32_t* __restrict__ keys_ws, int32_t* __restrict__ sel_pages,
-                      int32_t* __restrict__ n_sel, se_view view, int* status) {
+                      int32_t* __restrict__ n_sel, se_view view, const uint4* __restrict__ k_new,
+                      const uint4* __restrict__ v_new, int32_t* __restrict__ tickets, int* status) {
     extern __shared__ uint32_t skeys[];                   // [max_pages_per_seq] keys, then block table
     __shared__ int hist[256];
     __shared__ int tmp[33];
@@ -341,7 +349,13 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int H = kv.num_kv_heads;
     const int b = u / H, h = u % H;
     const int stride = kv.max_pages_per_seq;
-    const int ctx = clamp_ctx(kv.ctx_len[b], stride * kPage, status, tid == 0 && h == 0);
+    const int held = clamp_ctx(kv.ctx_len[b], stride * kPage, status, tid == 0 && h == 0);
+    // fused append (k_new given): this CTA writes head h's new row at position
+    // `held`, the sequence's last CTA to finish commits ctx_len = held + 1
+    const bool pending = k_new != nullptr;
+    const bool room = pending && held < stride * kPage;
+    if (pending && !room && tid == 0 && h == 0) flag(status, SE_DEV_CAPACITY);
+    const int ctx = room ? held + 1 : held;
     const int n = (ctx + kPage - 1) / kPage;
     const int bud = budget[b];
     const int k = max(1, (bud < 0 ? 0 : bud) / kPage);
@@ -370,6 +384,25 @@ __global__ void __launch_bounds__(kTopkThreads)
             }
         }
     }
+    __syncthreads();
+    bool appended = false;
+    if (room) {
+        const int phys = bts[held / kPage];
+        appended = phys >= 0 && phys < kv.num_pages;
+        if (appended)
+            append_head(kv, b, h, held, phys, k_new, v_new, tid, kTopkThreads);
+        else if (tid == 0 && h == 0)
+            flag(status, SE_DEV_BAD_INDEX);
+    }
+    // every CTA of sequence b has read ctx_len before it arrives here
+    auto commit = [&]() {
+        if (!pending || tid != 0) return;
+        __threadfence();
+        if (atomicAdd(&tickets[b], 1) == H - 1) {
+            tickets[b] = 0;
+            if (appended) kv.ctx_len[b] = held + 1;
+        }
+    };
     int32_t* sel = sel_pages + (int64_t)u * stride;
     int32_t* crow = view.chunk_row + (int64_t)u * view.max_chunks;
     auto emit = [&](int c, int page) {
@@ -383,16 +416,15 @@ __global__ void __launch_bounds__(kTopkThreads)
         }
     };
     if (n <= k) {
-        __syncthreads();
         for (int c = tid; c < n; c += blockDim.x) emit(c, c);
         if (tid == 0) {
             n_sel[u] = n;
             view.n_tokens[u] = ctx;
         }
+        commit();
         return;
     }
     const int K = k - 1;
-    __syncthreads();
     if (K > 0) {
         int need_eq = 0;
         uint32_t T = 0, msk = 0;
@@ -453,20 +485,28 @@ __global__ void __launch_bounds__(kTopkThreads)
         n_sel[u] = k;
         view.n_tokens[u] = kPage * (k - 1) + (ctx - kPage * (n - 1));
     }
+    commit();
 }
 
 }  // namespace
 
+// Workspace: status header | keys [units][max_pages] | append tickets [units]
 size_t quest_ws_bytes(int units, int max_pages) {
-    return 256 + (((size_t)units * max_pages * sizeof(uint32_t) + 255) & ~(size_t)255);
+    return 256 + (((size_t)units * max_pages * sizeof(uint32_t) + 255) & ~(size_t)255) +
+           (((size_t)units * sizeof(int32_t) + 255) & ~(size_t)255);
 }
 
 cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch, int num_q_heads,
                                 const int32_t* budget, int32_t* sel_pages, int32_t* n_sel,
-                                const se_view& view, void* ws, int* status, cudaStream_t s) {
+                                const se_view& view, const void* k_new, const void* v_new,
+                                void* ws, int* status, cudaStream_t s) {
     const int units = batch * kv.num_kv_heads;
     if (units == 0) return cudaSuccess;
     uint32_t* keys = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256);
+    int32_t* tickets = reinterpret_cast<int32_t*>(
+        static_cast<uint8_t*>(ws) + 256 +
+        (((size_t)units * kv.max_pages_per_seq * sizeof(uint32_t) + 255) & ~(size_t)255));
+    const int pending = k_new != nullptr;
     // scoring: one resident wave of kSelMinBlocks CTAs per SM shared by the sequences
     const int per_seq = max(1, min((num_sms() * kSelMinBlocks) / batch, kv.max_pages_per_seq));
     dim3 grid(per_seq, batch);
@@ -478,7 +518,7 @@ cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch,
         cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e2 != cudaSuccess) return e2;
         kern<<<grid, kSelThreads, smem, s>>>(kv, static_cast<const uint16_t*>(q), num_q_heads,
-                                             budget, keys, status);
+                                             budget, keys, pending, tickets, status);
         return cudaSuccess;
     };
     cudaError_t e;
@@ -493,8 +533,9 @@ cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch,
     e = cudaFuncSetAttribute(quest_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              topk_smem);
     if (e != cudaSuccess) return e;
-    quest_topk_kernel<<<units, kTopkThreads, topk_smem, s>>>(kv, budget, keys, sel_pages, n_sel,
-                                                            view, status);
+    quest_topk_kernel<<<units, kTopkThreads, topk_smem, s>>>(
+        kv, budget, keys, sel_pages, n_sel, view, static_cast<const uint4*>(k_new),
+        static_cast<const uint4*>(v_new), tickets, status);
     return cudaGetLastError();
 }
 

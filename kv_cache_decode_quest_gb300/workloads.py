@@ -45,8 +45,9 @@ class QuestRun:
     """Paged KV + Quest selection + split-K decode, one appended token per step."""
 
     def __init__(self, w: synth.QuestWorkload, inputs: dict, out_dtype: int = 0,
-                 max_splits: int | None = None, device="cuda"):
+                 max_splits: int | None = None, device="cuda", fused: bool = True):
         self.w = w
+        self.fused = fused
         B, Hq, Hkv, D, S = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.steps
         self.B, self.Hq, self.Hkv, self.D, self.S = B, Hq, Hkv, D, S
         self.G = Hq // Hkv
@@ -93,6 +94,12 @@ class QuestRun:
         se.se_quest_select(self.kv, self.q[s], self.B, self.Hq, self.budget, self.sel, self.n_sel,
                            self.view, self.ws_sel)
 
+    def append_select(self, s: int):
+        """The step's append fused into the selection (one kernel fewer)."""
+        se.se_quest_select_append(self.kv, self.k_new[s], self.v_new[s], self.q[s], self.B,
+                                  self.Hq, self.budget, self.sel, self.n_sel, self.view,
+                                  self.ws_sel)
+
     def decode(self, s: int, out=None, lse=None, ev_begin=None, ev_end=None):
         se.se_sparse_decode(self.kv.k, self.kv.v, self.view, self.q[s], self.B, self.Hq, self.Hkv,
                             self.D, self.scale, self.out if out is None else out,
@@ -102,8 +109,11 @@ class QuestRun:
 
     def step(self, s: int, out=None, lse=None, ev_begin=None, ev_end=None):
         """One decode step: append the step's token, select pages, attend."""
-        self.append(s)
-        self.select(s)
+        if self.fused:
+            self.append_select(s)
+        else:
+            self.append(s)
+            self.select(s)
         self.decode(s, out, lse, ev_begin, ev_end)
 
     def status(self) -> int:

@@ -72,9 +72,9 @@ def check_step(run, inputs, s, units=None):
     return worst, allowed
 
 
-def run_and_check(w, out_dtype=0, max_splits=None, steps=None, units=None):
+def run_and_check(w, out_dtype=0, max_splits=None, steps=None, units=None, fused=True):
     inputs = synth.quest_inputs(w)
-    run = QuestRun(w, inputs, out_dtype=out_dtype, max_splits=max_splits)
+    run = QuestRun(w, inputs, out_dtype=out_dtype, max_splits=max_splits, fused=fused)
     worst = 0.0
     for s in range(w.steps):
         run.step(s)
@@ -91,6 +91,37 @@ def test_tiny_quest_single_query():
     w = synth.workloads()["tiny_quest"]
     run_and_check(w)
     run_and_check(w, out_dtype=1)
+    run_and_check(w, fused=False)
+
+
+def test_fused_append_select_matches_separate_calls():
+    """se_quest_select_append == se_kv_append + se_quest_select, bit for bit:
+    selections, view, lengths, cache rows, page summaries and the attention
+    output, over steps that open new pages (contexts 15, 16, 31 and 1000 tokens
+    at the start) and a sequence whose pages are all selected."""
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name="quest_fused", batch=5, ctx=(15, 16, 31, 1000, 2047),
+                     budget=(64, 64, 256, 128, U32), steps=20)
+    inputs = synth.quest_inputs(w)
+    a = QuestRun(w, inputs, fused=True)
+    b = QuestRun(w, inputs, fused=False)
+    for s in range(w.steps):
+        a.step(s)
+        b.step(s)
+        torch.cuda.synchronize()
+        n = b.n_sel.cpu()
+        assert torch.equal(a.n_sel.cpu(), n), f"step {s}"
+        for u in range(len(n)):
+            k = int(n[u])
+            assert torch.equal(a.sel[u, :k].cpu(), b.sel[u, :k].cpu()), f"step {s} unit {u}"
+            assert torch.equal(a.view.chunk_row[u, :k].cpu(), b.view.chunk_row[u, :k].cpu())
+        assert torch.equal(a.view.n_tokens.cpu(), b.view.n_tokens.cpu())
+        assert torch.equal(a.kv.ctx_len.cpu(), b.kv.ctx_len.cpu())
+        assert torch.equal(a.out.cpu(), b.out.cpu())
+    assert torch.equal(a.kv.k.cpu(), b.kv.k.cpu())
+    assert torch.equal(a.kv.v.cpu(), b.kv.v.cpu())
+    assert torch.equal(a.kv.meta.cpu(), b.kv.meta.cpu())
+    assert a.status() == 0 and b.status() == 0
 
 
 @pytest.mark.parametrize("out_dtype", [0, 1])
