@@ -14,7 +14,8 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(se_\w+)\s*\(", text, flags=re.M)
     return sorted(set(n for n in names if not n.endswith("_t")))

@@ -15,7 +15,8 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
                                      ("snapkv_tiny", make_golden.snapkv_case),
                                      ("h2o_tiny", make_golden.h2o_case)])
 def test_fixture_matches_oracle(name, fn):
-    stored = json.load(open(os.path.join(GOLDEN, name + ".json")))
+    with open(os.path.join(GOLDEN, name + ".json")) as f:
+        stored = json.load(f)
     fresh = fn()
     for key, want in stored["expected"].items():
         got = fresh["expected"][key]

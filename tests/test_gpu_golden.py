@@ -18,7 +18,8 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 def load(name):
-    return json.load(open(os.path.join(GOLDEN, name + ".json")))
+    with open(os.path.join(GOLDEN, name + ".json")) as f:
+        return json.load(f)
 
 
 def bf16(x):
