@@ -159,12 +159,20 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 const int row_l = row_next;
                 row_next = cb + 32 + lane < item.z ? crow[cb + 32 + lane] : -1;
                 const int nb = min(32, item.z - cb);
-                for (int j = 0; j < nb; ++j, ++seq) {
-                    const int row = __shfl_sync(0xffffffffu, row_l, j);
-                    if (lane == 0) {
+                // four chunks per iteration: chunk t = lane / 4 of the group is
+                // led by lane 4t (waits for its stage, arms its barrier); then
+                // lanes 4t..4t+3 issue that chunk's K and V boxes together
+                for (int j0 = 0; j0 < nb; j0 += 4) {
+                    const int t = lane >> 2, q = lane & 3;
+                    const int j = j0 + t;
+                    const bool mine = t < 4 && j < nb;
+                    const int row = __shfl_sync(0xffffffffu, row_l, min(j, 31));
+                    const uint32_t sq = seq + t;
+                    const int s = sq % NS;
+                    int go = 0;
+                    if (mine && q == 0) {
                         const int c = cb + j;
-                        const int s = seq % NS;
-                        const uint32_t ph = (seq / NS) & 1;
+                        const uint32_t ph = (sq / NS) & 1;
                         if (!*abort_flag && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
                             *abort_flag = 1;
                             flag(p.status, SE_DEV_TIMEOUT);
@@ -175,20 +183,19 @@ __global__ void __launch_bounds__(kDecodeThreads)
                             cnt = 0;
                         }
                         stage_ntok[s] = cnt;
-                        if (cnt > 0 && !*abort_flag) {
-                            uint8_t* kdst = stages + s * S::kStageBytes;
+                        go = cnt > 0 && !*abort_flag;
+                        if (go)
                             mbar_arrive_expect_tx(&full[s], S::kStageBytes);
-#pragma unroll
-                            for (int bx = 0; bx < S::kBoxes; ++bx) {
-                                tma_load_2d(kdst + bx * 2048, &tk, &full[s], 64 * bx, row);
-                                tma_load_2d(kdst + S::kChunkBytes + bx * 2048, &tv, &full[s],
-                                            64 * bx, row);
-                            }
-                        } else {
+                        else
                             mbar_arrive(&full[s]);
-                        }
                     }
-                    __syncwarp();
+                    go = __shfl_sync(0xffffffffu, go, lane & ~3);
+                    if (mine && go && q < 2 * S::kBoxes) {
+                        uint8_t* dst = stages + s * S::kStageBytes + (q & 1) * S::kChunkBytes +
+                                       (q >> 1) * 2048;
+                        tma_load_2d(dst, (q & 1) ? &tv : &tk, &full[s], 64 * (q >> 1), row);
+                    }
+                    seq += min(4, nb - j0);
                 }
             }
         }
@@ -271,21 +278,31 @@ __global__ void __launch_bounds__(kDecodeThreads)
                     __syncwarp();
                 }
                 // ---- S^T = K Q^T ----
-                float sacc[NT][4];
+                // two accumulators (even / odd k-steps) halve the dependent
+                // chain of mma's; all K fragments are loaded up front
+                float sacc[NT][4], sacc2[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) sacc[nt][e] = sacc2[nt][e] = 0.f;
                 const uint32_t kbase = smem_u32(kb);
+                uint32_t kf[KSTEPS][4];
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const int d = kk * 16 + k_dof;
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kbase + (d >> 6) * 2048 + swz128(k_tok, (d & 63) >> 3), a0, a1, a2, a3);
+                    ldsm_x4(kbase + (d >> 6) * 2048 + swz128(k_tok, (d & 63) >> 3), kf[kk][0],
+                            kf[kk][1], kf[kk][2], kf[kk][3]);
+                }
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma_16816(sacc[nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
-                }
+                        mma_16816((kk & 1) ? sacc2[nt] : sacc[nt], kf[kk][0], kf[kk][1], kf[kk][2],
+                                  kf[kk][3], qf[kk][nt][0], qf[kk][nt][1]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
                 // ---- mask, optional logits, online softmax (exp2 domain) ----
                 const int tok_base = c * kPage;
                 float pr[NT][4];
@@ -311,8 +328,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                         const float m_new = fmaxf(m[nt][j], mx);
                         const float base = m_new == -INFINITY ? 0.f : m_new;
-                        const float alpha = exp2f(m[nt][j] - base);
-                        const float p0 = exp2f(sv[j] - base), p1 = exp2f(sv[j + 2] - base);
+                        const float alpha = ex2_approx(m[nt][j] - base);
+                        const float p0 = ex2_approx(sv[j] - base), p1 = ex2_approx(sv[j + 2] - base);
                         l[nt][j] = l[nt][j] * alpha + p0 + p1;
                         m[nt][j] = m_new;
                         pr[nt][j] = p0;
