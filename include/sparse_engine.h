@@ -236,7 +236,10 @@ int se_view_from_segments(const se_varlen_kv* kv, int batch, const se_view* view
  * k_rows, v_rows bf16 [total_rows][head_dim]; q bf16 [batch][num_q_heads][head_dim];
  * out bf16 or fp32 [batch][num_q_heads][head_dim]; lse fp32 [batch][num_q_heads] or NULL.
  * A chunk row outside [0, total_rows) sets SE_DEV_BAD_INDEX and counts as empty.
- * Workspace: se_sparse_decode_workspace(num_units, G, head_dim, max_splits). */
+ * Workspace: se_sparse_decode_workspace(num_units, G, head_dim, max_splits),
+ * zero-filled before its first use: it holds the arrival counters of split
+ * units, which every call leaves at zero (clear it again after a call that set
+ * a device error bit). */
 int se_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
                      const se_view* view, const void* q, int batch, int num_q_heads,
                      int num_kv_heads, int head_dim, float scale, const se_decode_opts* opts,
@@ -304,7 +307,8 @@ int se_snapkv_compact(const se_paged_kv* prefill, const void* q_win, int batch, 
  *      position goes to evicted_pos[u] (else -1) and the segment's last token
  *      moves into its slot.
  * seq_len[b] is incremented.  Positions must be unique per unit.
- * Workspace: se_h2o_workspace(batch, num_kv_heads, num_q_heads, head_dim, seg_cap). */
+ * Workspace: se_h2o_workspace(batch, num_kv_heads, num_q_heads, head_dim, seg_cap),
+ * zero-filled before its first use (it contains a decode workspace). */
 int se_h2o_step(const se_h2o_state* st, const void* q, const void* k_new, const void* v_new,
                 int batch, int num_q_heads, float scale, int out_dtype, void* out, float* lse,
                 int32_t* evicted_pos, void* ws, size_t ws_bytes, se_stream_t stream);

@@ -63,6 +63,8 @@ struct DecodeParams {
     const int4* items;
     const int* cta_first;     // [grid+1]: CTA c runs items cta_first[c] .. cta_first[c+1]-1
     const int2* unit_items;
+    // self_plan: no plan kernel ran; each CTA derives its one piece (units <= grid)
+    int self_plan, num_units, max_splits;
     int* counters;
     float* o_part;
     float* lse_part;
@@ -76,6 +78,68 @@ struct DecodeParams {
 };
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// One piece per CTA, computed by one warp of every CTA (no plan kernel): unit
+// u gets pieces_u = max(1, min(max_splits, nc_u, floor(nc_u * share / total)))
+// pieces of nc_u * k / pieces_u chunks, with share = grid lowered until the
+// pieces fit the grid (share 0 gives one piece per unit, which fits since
+// units <= grid).  Piece k of unit u is item off_u + k, run by CTA off_u + k.
+// Writes this CTA's item (unit, first chunk, end chunk, partial slot or -1)
+// and its unit's (first item, pieces); *has = 0 when the CTA runs none.
+__device__ __noinline__ void plan_own_piece(const DecodeParams& p, int lane, int4* item,
+                                            int2* uitem, int* has) {
+    const int units = p.num_units, grid = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x), lim = p.max_chunks * kPage;
+    auto chunks_of = [&](int u) {
+        int n = p.n_tokens[u];
+        n = n < 0 ? 0 : (n > lim ? lim : n);               // the consumers flag bad lengths
+        return (n + kPage - 1) / kPage;
+    };
+    int total = 0;
+#pragma unroll 1
+    for (int base = 0; base < units; base += 32)
+        total += __reduce_add_sync(0xffffffffu, base + lane < units ? chunks_of(base + lane) : 0);
+    const int64_t tot = max(1, total);
+    auto pieces_of = [&](int nc, int share) {
+        return nc == 0 ? 1 : max(1, min(p.max_splits, min(nc, (int)((int64_t)nc * share / tot))));
+    };
+    int share = grid;
+#pragma unroll 1
+    for (int iter = 0; iter < 4 && share > 0; ++iter) {
+        int fit = 0;
+#pragma unroll 1
+        for (int base = 0; base < units; base += 32)
+            fit += __reduce_add_sync(0xffffffffu,
+                                     base + lane < units ? pieces_of(chunks_of(base + lane), share) : 0);
+        if (fit <= grid) break;
+        share = iter == 3 ? 0 : max(0, share - (fit - grid));
+    }
+    if (lane == 0) *has = 0;
+    __syncwarp();
+    int run = 0;
+#pragma unroll 1
+    for (int base = 0; base < units; base += 32) {
+        const int u = base + lane;
+        const int nc = u < units ? chunks_of(u) : 0;
+        const int pc = u < units ? pieces_of(nc, share) : 0;
+        int x = pc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        const int off = run + x - pc;
+        if (u < units && c >= off && c < off + pc) {
+            const int k = c - off;
+            const int c0 = (int)((int64_t)nc * k / pc), c1 = (int)((int64_t)nc * (k + 1) / pc);
+            *item = make_int4(u, c0, c1, pc == 1 ? -1 : c);
+            *uitem = make_int2(off, pc);
+            *has = 1;
+        }
+        run += __shfl_sync(0xffffffffu, x, 31);
+        if (run > c) break;
+    }
+}
 
 __device__ __forceinline__ int unit_tokens(const DecodeParams& p, int u) {
     int n = p.n_tokens[u];
@@ -117,8 +181,21 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     pdl_wait();
     pdl_trigger();
+    // this CTA's items: [it_begin, it_end) of the plan's list, or its own
+    // piece (item index blockIdx.x) when it plans for itself
+    __shared__ int4 s_item;
+    __shared__ int2 s_uitem;
+    __shared__ int s_has;
+    if (p.self_plan && warp == kConsumerWarps) plan_own_piece(p, lane, &s_item, &s_uitem, &s_has);
     __syncthreads();
-    const int it_begin = p.cta_first[blockIdx.x], it_end = p.cta_first[blockIdx.x + 1];
+    int it_begin, it_end;
+    if (p.self_plan) {
+        it_begin = static_cast<int>(blockIdx.x);
+        it_end = it_begin + s_has;
+    } else {
+        it_begin = p.cta_first[blockIdx.x];
+        it_end = p.cta_first[blockIdx.x + 1];
+    }
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
@@ -139,7 +216,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         // (the one-piece-per-CTA plan): it is loaded alongside cta_first, which
         // saves a dependent round trip before the first copy (the items array
         // holds at least grid entries, so the read stays in bounds)
-        const int4 spec = p.items[blockIdx.x];
+        const int4 spec = p.self_plan ? s_item : p.items[blockIdx.x];
         auto fetch = [&](int it) {
             if (it >= it_end) return;
             nitem = it == static_cast<int>(blockIdx.x) ? spec : p.items[it];
@@ -222,7 +299,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int v_tok = (lj >> 1) * 8 + lr, v_dof = (lj & 1) * 8;   // V^T as A (d x token)
 
     uint32_t seq = 0;
-    const int4 spec_c = p.items[blockIdx.x];               // as in the producer
+    const int4 spec_c = p.self_plan ? s_item : p.items[blockIdx.x];   // as in the producer
     for (int it = it_begin; it < it_end; ++it) {
         const int4 item = it == static_cast<int>(blockIdx.x) ? spec_c : p.items[it];
         const int u = item.x;
@@ -471,7 +548,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
             // The last piece of unit u to finish merges all of u's pieces by
             // their LSE (an arrival counter, no waiting on other CTAs).
             volatile int* last = stage_ntok + NS + 1;
-            const int2 ui = p.unit_items[u];
+            const int2 ui = p.self_plan ? s_uitem : p.unit_items[u];
             if (ctid == 0) {
                 // the CTA barrier above orders the other threads' partial writes
                 // before this thread's release; the acquire half orders the last
@@ -664,138 +741,9 @@ __global__ void __launch_bounds__(1024)
     if (threadIdx.x == 0) *n_items = n;
 }
 
-// The same plan computed by one warp (no block barriers), for up to
-// kWarpPlanUnits units: warp scans over 32 units at a time, and cta_first
-// scattered from the items (item i starts every CTA c with
-// gstart[i-1] < c*per <= gstart[i]) instead of searched.
-constexpr int kWarpPlanUnits = 512;
-__global__ void __launch_bounds__(32)
-    plan_warp_kernel(const int32_t* __restrict__ n_tokens, int units, int max_chunks,
-                     int max_splits, int grid, int4* __restrict__ items, int* __restrict__ gstart,
-                     int2* __restrict__ unit_items, int* __restrict__ cta_first,
-                     int* __restrict__ n_items, int* __restrict__ counters, int* status) {
-    pdl_wait();
-    pdl_trigger();
-    const int lane = threadIdx.x;
-    const int lim = max_chunks * kPage;
-    auto chunks_of = [&](int u) {
-        int n = n_tokens[u];
-        if (n < 0 || n > lim) {
-            flag(status, SE_DEV_BAD_LENGTH);
-            n = n < 0 ? 0 : lim;
-        }
-        return (n + kPage - 1) / kPage;
-    };
-    auto excl_scan = [&](int v, int* sum) {
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        *sum = __shfl_sync(0xffffffffu, x, 31);
-        return x - v;
-    };
-    // Short code on purpose: right after an L2 flush every instruction line
-    // of a kernel this small is a cold fetch, so loops stay rolled.  The chunk
-    // counts are kept in shared memory between the passes.
-    __shared__ int s_nc[kWarpPlanUnits];
-    int total = 0, s_max = 0;
-#pragma unroll 1
-    for (int base = 0; base < units; base += 32) {
-        const int u = base + lane;
-        const int nc = u < units ? chunks_of(u) : 0;
-        if (u < units) {
-            counters[u] = 0;
-            s_nc[u] = nc;
-        }
-        total += __reduce_add_sync(0xffffffffu, nc);
-        s_max = max(s_max, __reduce_max_sync(0xffffffffu, nc));
-    }
-    // nc * grid / total in 32-bit arithmetic when the product fits (grid <= 2048)
-    const unsigned tot1 = static_cast<unsigned>(max(1, total));
-    auto one_each_pieces = [&](int nc) {
-        const int share = nc < (1 << 20) ? static_cast<int>(static_cast<unsigned>(nc) * grid / tot1)
-                                         : static_cast<int>((int64_t)nc * grid / tot1);
-        return nc == 0 ? 1 : max(1, min(max_splits, min(nc, share)));
-    };
-    int fit = 0;
-#pragma unroll 1
-    for (int base = 0; base < units; base += 32) {
-        const int u = base + lane;
-        fit += __reduce_add_sync(0xffffffffu, u < units ? one_each_pieces(s_nc[u]) : 0);
-    }
-    const bool one_each = fit <= grid;
-    const bool streamk = !one_each && max_splits >= 3;
-    int per = max(1, (total + grid - 1) / max(1, grid));
-    if (streamk) per = max(per, (s_max + max_splits - 3) / (max_splits - 2));
-
-    int run_items = 0, run_chunks = 0;
-#pragma unroll 1
-    for (int base = 0; base < units; base += 32) {
-        const int u = base + lane;
-        const int nc = u < units ? s_nc[u] : 0;
-        int t_chunks, t_items;
-        const int P = run_chunks + excl_scan(nc, &t_chunks);
-        int pieces = 0;
-        if (u < units) {
-            if (nc == 0)
-                pieces = 1;
-            else if (one_each)
-                pieces = one_each_pieces(nc);
-            else if (streamk)
-                pieces = (P + nc - 1) / per - P / per + 1;
-            else
-                pieces = min(max_splits, nc);
-        }
-        const int off = run_items + excl_scan(pieces, &t_items);
-        if (u < units) {
-            unit_items[u] = make_int2(off, pieces);
-            // piece k covers chunks [floor(k*nc/pieces), floor((k+1)*nc/pieces)) in
-            // the proportional cut, stepped as k*q + floor(k*r/pieces) with
-            // nc = q*pieces + r; stream-K cuts at the multiples of per
-            const int q = nc / pieces, r = nc - q * pieces;
-            const int pb = streamk ? P / per : 0;
-            int c0 = 0, acc = 0;
-#pragma unroll 1
-            for (int k = 0; k < pieces; ++k) {
-                int c1;
-                if (nc == 0) {
-                    c1 = 0;
-                } else if (streamk) {
-                    c0 = k == 0 ? 0 : (pb + k) * per - P;
-                    c1 = min(P + nc, (pb + k + 1) * per) - P;
-                } else {
-                    acc += r;
-                    c1 = c0 + q + (acc >= pieces ? 1 : 0);
-                    if (acc >= pieces) acc -= pieces;
-                }
-                items[off + k] = make_int4(u, c0, c1, pieces == 1 ? -1 : off + k);
-                gstart[off + k] = P + c0;
-                c0 = c1;
-            }
-        }
-        run_items += t_items;
-        run_chunks += t_chunks;
-    }
-    __syncwarp();                                         // gstart is read back by other lanes
-    const int n = run_items;
-    if (one_each) {
-#pragma unroll 1
-        for (int c = lane; c <= grid; c += 32) cta_first[c] = min(c, n);
-    } else {
-        for (int i = lane; i < n; i += 32) {
-            const int g = gstart[i];
-            const int c_lo = i == 0 ? 0 : gstart[i - 1] / per + 1;
-            const int c_hi = min(grid - 1, g / per);
-            for (int c = c_lo; c <= c_hi; ++c) cta_first[c] = i;
-        }
-        const int c_tail = n == 0 ? 0 : min(grid, gstart[n - 1] / per + 1);
-        for (int c = c_tail + lane; c <= grid; c += 32) cta_first[c] = n;
-        if (lane == 0 && n > 0) cta_first[0] = 0;
-    }
-    if (lane == 0) *n_items = n;
-}
+// Up to this many units (and no more than the grid) the decode CTAs plan for
+// themselves; above it the block-wide plan kernel runs first.
+constexpr int kSelfPlanUnits = 512;
 
 template <int D, int NT, bool TWO>
 cudaError_t run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
@@ -869,12 +817,17 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
     const int max_items = units * max_splits;
     const int grid = max(1, min(kMaxGrid, min(max_items, num_sms() * cps)));
 
-    const bool small = units <= kWarpPlanUnits;
-    cudaError_t e = launch_pdl(small ? plan_warp_kernel : plan_kernel, dim3(1), dim3(small ? 32 : 1024),
-                               0, s, static_cast<const int32_t*>(view.n_tokens), units,
-                               view.max_chunks, max_splits, grid, w.items, w.gstart, w.unit_items,
-                               w.cta_first, w.n_items, w.counters, w.status);
-    if (e != cudaSuccess) return e;
+    // up to kSelfPlanUnits units (and no more than the grid), every decode CTA
+    // derives its own piece and no plan kernel runs
+    const bool self_plan = units <= kSelfPlanUnits && units <= grid;
+    cudaError_t e = cudaSuccess;
+    if (!self_plan) {
+        e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s,
+                       static_cast<const int32_t*>(view.n_tokens), units, view.max_chunks,
+                       max_splits, grid, w.items, w.gstart, w.unit_items, w.cta_first, w.n_items,
+                       w.counters, w.status);
+        if (e != cudaSuccess) return e;
+    }
 
     DecodeParams p;
     p.chunk_row = view.chunk_row;
@@ -889,6 +842,9 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
     p.items = w.items;
     p.cta_first = w.cta_first;
     p.unit_items = w.unit_items;
+    p.self_plan = self_plan ? 1 : 0;
+    p.num_units = units;
+    p.max_splits = max_splits;
     p.counters = w.counters;
     p.o_part = w.o_part;
     p.lse_part = w.lse_part;
