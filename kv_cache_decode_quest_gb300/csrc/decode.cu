@@ -103,41 +103,38 @@ __device__ __noinline__ void plan_own_piece(const DecodeParams& p, int lane, int
     auto pieces_of = [&](int nc, int share) {
         return nc == 0 ? 1 : max(1, min(p.max_splits, min(nc, (int)((int64_t)nc * share / tot))));
     };
+    // one pass per share: the scan over the pieces both finds this CTA's piece
+    // and totals them; a share whose pieces do not fit the grid is lowered
     int share = grid;
 #pragma unroll 1
-    for (int iter = 0; iter < 4 && share > 0; ++iter) {
-        int fit = 0;
+    for (int iter = 0; iter < 5; ++iter) {
+        if (lane == 0) *has = 0;
+        __syncwarp();
+        int run = 0;
 #pragma unroll 1
-        for (int base = 0; base < units; base += 32)
-            fit += __reduce_add_sync(0xffffffffu,
-                                     base + lane < units ? pieces_of(chunks_of(base + lane), share) : 0);
-        if (fit <= grid) break;
-        share = iter == 3 ? 0 : max(0, share - (fit - grid));
-    }
-    if (lane == 0) *has = 0;
-    __syncwarp();
-    int run = 0;
-#pragma unroll 1
-    for (int base = 0; base < units; base += 32) {
-        const int u = base + lane;
-        const int nc = u < units ? chunks_of(u) : 0;
-        const int pc = u < units ? pieces_of(nc, share) : 0;
-        int x = pc;
+        for (int base = 0; base < units; base += 32) {
+            const int u = base + lane;
+            const int nc = u < units ? chunks_of(u) : 0;
+            const int pc = u < units ? pieces_of(nc, share) : 0;
+            int x = pc;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int off = run + x - pc;
+            if (u < units && c >= off && c < off + pc) {
+                const int k = c - off;
+                const int c0 = (int)((int64_t)nc * k / pc), c1 = (int)((int64_t)nc * (k + 1) / pc);
+                *item = make_int4(u, c0, c1, pc == 1 ? -1 : c);
+                *uitem = make_int2(off, pc);
+                *has = 1;
+            }
+            run += __shfl_sync(0xffffffffu, x, 31);
         }
-        const int off = run + x - pc;
-        if (u < units && c >= off && c < off + pc) {
-            const int k = c - off;
-            const int c0 = (int)((int64_t)nc * k / pc), c1 = (int)((int64_t)nc * (k + 1) / pc);
-            *item = make_int4(u, c0, c1, pc == 1 ? -1 : c);
-            *uitem = make_int2(off, pc);
-            *has = 1;
-        }
-        run += __shfl_sync(0xffffffffu, x, 31);
-        if (run > c) break;
+        __syncwarp();                                   // *has / *item settled before a retry
+        if (run <= grid || share == 0) break;          // share 0: one piece per unit
+        share = iter == 3 ? 0 : max(0, share - (run - grid));
     }
 }
 

@@ -356,6 +356,10 @@ __global__ void __launch_bounds__(kTopkThreads)
     const bool room = pending && held < stride * kPage;
     if (pending && !room && tid == 0 && h == 0) flag(status, SE_DEV_CAPACITY);
     const int ctx = room ? held + 1 : held;
+    // the append's loads go out now; its stores come last
+    AppendRegs ar;
+    const int segs = kv.head_dim / 8;
+    if (room && tid < segs) append_load(kv, b, h, held, k_new, v_new, tid, ar);
     const int n = (ctx + kPage - 1) / kPage;
     const int bud = budget[b];
     const int k = max(1, (bud < 0 ? 0 : bud) / kPage);
@@ -386,19 +390,23 @@ __global__ void __launch_bounds__(kTopkThreads)
     }
     __syncthreads();
     bool appended = false;
+    const int phys_new = room ? bts[held / kPage] : -1;
     if (room) {
-        const int phys = bts[held / kPage];
-        appended = phys >= 0 && phys < kv.num_pages;
-        if (appended)
-            append_head(kv, b, h, held, phys, k_new, v_new, tid, kTopkThreads);
-        else if (tid == 0 && h == 0)
-            flag(status, SE_DEV_BAD_INDEX);
+        appended = phys_new >= 0 && phys_new < kv.num_pages;
+        if (!appended && tid == 0 && h == 0) flag(status, SE_DEV_BAD_INDEX);
     }
-    // every CTA of sequence b has read ctx_len before it arrives here
-    auto commit = [&]() {
-        if (!pending || tid != 0) return;
+    // The ticket is taken as soon as this CTA has read ctx_len (every CTA of
+    // sequence b takes one after its read, so the last taker stores the new
+    // length after all reads); its result is only used at the end, so the
+    // atomic's round trip overlaps the selection.
+    int ticket = -1;
+    if (pending && tid == 0) {
         __threadfence();
-        if (atomicAdd(&tickets[b], 1) == H - 1) {
+        ticket = atomicAdd(&tickets[b], 1);
+    }
+    auto commit = [&]() {
+        if (appended && tid < segs) append_store(kv, b, h, held, phys_new, tid, ar);
+        if (ticket == H - 1) {
             tickets[b] = 0;
             if (appended) kv.ctx_len[b] = held + 1;
         }
