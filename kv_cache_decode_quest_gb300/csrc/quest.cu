@@ -23,7 +23,7 @@ namespace {
 constexpr int kSelWarps = 8;               // scoring warps
 constexpr int kSelThreads = (kSelWarps + 1) * 32;   // + the copy warp
 constexpr int kSelChunk = 16384;           // bytes per ring stage
-constexpr int kSelStages = 6;
+constexpr int kSelStages = 4;
 constexpr int kSelMinBlocks = 2;           // resident scoring CTAs per SM
 constexpr int kTopkThreads = 256;
 constexpr size_t kSelSmemFixed = 128 /* alignment slack */ + (size_t)kSelStages * kSelChunk +
