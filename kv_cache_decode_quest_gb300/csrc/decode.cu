@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         // saves a dependent round trip before the first copy (the items array
         // holds at least grid entries, so the read stays in bounds)
         const int4 spec = p.self_plan ? s_item : p.items[blockIdx.x];
+        const uint64_t kv_policy = l2_evict_first();
         auto fetch = [&](int it) {
             if (it >= it_end) return;
             nitem = it == static_cast<int>(blockIdx.x) ? spec : p.items[it];
@@ -267,7 +268,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
                     if (mine && go && q < 2 * S::kBoxes) {
                         uint8_t* dst = stages + s * S::kStageBytes + (q & 1) * S::kChunkBytes +
                                        (q >> 1) * 2048;
-                        tma_load_2d(dst, (q & 1) ? &tv : &tk, &full[s], 64 * (q >> 1), row);
+                        // with logits saved, K/V (read once) leave L2 first so
+                        // that the logits stay there for the next kernel
+                        if (p.logits_out != nullptr)
+                            tma_load_2d_hint(dst, (q & 1) ? &tv : &tk, &full[s], 64 * (q >> 1),
+                                             row, kv_policy);
+                        else
+                            tma_load_2d(dst, (q & 1) ? &tv : &tk, &full[s], 64 * (q >> 1), row);
                     }
                     seq += min(4, nb - j0);
                 }
@@ -297,6 +304,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
     uint32_t seq = 0;
     const int4 spec_c = p.self_plan ? s_item : p.items[blockIdx.x];   // as in the producer
+    const uint64_t logit_policy = l2_evict_last();
     for (int it = it_begin; it < it_end; ++it) {
         const int4 item = it == static_cast<int>(blockIdx.x) ? spec_c : p.items[it];
         const int u = item.x;
@@ -390,8 +398,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
                         if (p.logits_out != nullptr && tok < cnt) {
                             const int g = nt * 8 + 2 * cq + (e & 1);
                             if (g < G)
-                                p.logits_out[((int64_t)u * p.logits_stride + tok_base + tok) * G + g] =
-                                    sacc[nt][e] * p.scale;
+                                st_global_hint(p.logits_out +
+                                                   ((int64_t)u * p.logits_stride + tok_base + tok) * G + g,
+                                               sacc[nt][e] * p.scale, logit_policy);
                         }
                     }
 #pragma unroll

@@ -32,9 +32,19 @@ struct EvictParams {
     int* status;
 };
 
-__global__ void __launch_bounds__(1024) h2o_evict_kernel(const EvictParams p) {
+// 512 threads: two blocks per SM, so one block per unit runs in a single wave.
+// STAGED: the unit's positions and scores are read once into shared memory
+// (all loads in flight), every later pass reads them there, and the updated
+// scores go back in one pass; used when 8 * seg_cap bytes fit kEvictStageMax.
+constexpr int kEvictThreads = 512;
+constexpr int kEvictStageMax = 96 * 1024;
+// G4 = G / 4 (a compile-time count of 16-byte logit vectors per token, so a
+// thread's loads for several tokens are issued together), or 0 for G = 1, 2.
+template <bool STAGED, int G4>
+__global__ void __launch_bounds__(kEvictThreads) h2o_evict_kernel(const EvictParams p) {
     pdl_wait();
     pdl_trigger();
+    extern __shared__ int32_t stage[];                  // STAGED: [seg_cap] pos, [seg_cap] score
     __shared__ float s_lse[16];
     __shared__ int hist[256];
     __shared__ int tmp[33];
@@ -57,16 +67,38 @@ __global__ void __launch_bounds__(1024) h2o_evict_kernel(const EvictParams p) {
     if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
 
-    // 1. score update with this step's normalised probabilities
-    float* score = p.kv.score + off;
-    int32_t* pos = p.kv.pos + off;
+    float* gscore = p.kv.score + off;
+    int32_t* gpos = p.kv.pos + off;
+    int32_t* pos = STAGED ? stage : gpos;
+    float* score = STAGED ? reinterpret_cast<float*>(stage + p.kv.seg_cap) : gscore;
+    // 1. score update with this step's normalised probabilities (a token's G
+    //    logits as 16-byte vectors when G % 4 == 0), positions staged alongside
     const float* lg = p.logits + (int64_t)u * p.stride * G;
+#pragma unroll 4
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
         float pr = 0.f;
-        for (int g = 0; g < G; ++g) pr += __expf(lg[(int64_t)t * G + g] - s_lse[g]);
-        score[t] += pr;
+        if (G4 > 0) {
+            const float4* l4 = reinterpret_cast<const float4*>(lg + (int64_t)t * G);
+#pragma unroll
+            for (int j = 0; j < G4; ++j) {
+                const float4 x = l4[j];
+                pr += __expf(x.x - s_lse[4 * j]) + __expf(x.y - s_lse[4 * j + 1]) +
+                      __expf(x.z - s_lse[4 * j + 2]) + __expf(x.w - s_lse[4 * j + 3]);
+            }
+        } else {
+            for (int g = 0; g < G; ++g) pr += __expf(lg[(int64_t)t * G + g] - s_lse[g]);
+        }
+        score[t] = gscore[t] + pr;
+        if (STAGED) pos[t] = gpos[t];
     }
+    __syncthreads();
+    // the updated scores go back to the cache (STAGED), after any move
+    auto write_back = [&](int count) {
+        if (STAGED)
+            for (int t = threadIdx.x; t < count; t += blockDim.x) gscore[t] = score[t];
+    };
     if (n <= p.budget) {
+        write_back(n);
         if (threadIdx.x == 0) p.evicted_pos[u] = -1;
         return;
     }
@@ -76,6 +108,7 @@ __global__ void __launch_bounds__(1024) h2o_evict_kernel(const EvictParams p) {
     const int new_pos = p.kv.seq_len[b] - 1;
     int thr = new_pos - p.recent;            // candidates: pos <= thr
     int c = 0;
+#pragma unroll 4
     for (int t = threadIdx.x; t < n; t += blockDim.x) c += pos[t] > thr;
     atomicAdd(&s_cnt, c);
     __syncthreads();
@@ -88,6 +121,7 @@ __global__ void __launch_bounds__(1024) h2o_evict_kernel(const EvictParams p) {
     }
     // 3. victim: lowest score, then the higher position
     unsigned long long best = ~0ull;
+#pragma unroll 4
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
         const int ps = pos[t];
         if (ps > thr) continue;
@@ -115,12 +149,14 @@ __global__ void __launch_bounds__(1024) h2o_evict_kernel(const EvictParams p) {
     __syncthreads();
     best = s_best[0];
     if (best == ~0ull) {   // no candidate (recent >= n): nothing can be evicted
+        write_back(n);
         if (threadIdx.x == 0) p.evicted_pos[u] = -1;
         return;
     }
     const int victim_pos = static_cast<int>(0x7fffffffu - static_cast<uint32_t>(best & 0xffffffffu));
     // 4. find the victim's slot, then move the last slot into it
     __shared__ int s_slot;
+#pragma unroll 4
     for (int t = threadIdx.x; t < n; t += blockDim.x)
         if (pos[t] == victim_pos) s_slot = t;
     __syncthreads();
@@ -135,8 +171,11 @@ __global__ void __launch_bounds__(1024) h2o_evict_kernel(const EvictParams p) {
         if (threadIdx.x == 0) {
             pos[v] = pos[last];
             score[v] = score[last];
+            if (STAGED) gpos[v] = pos[last];
         }
     }
+    __syncthreads();
+    write_back(n - 1);
     if (threadIdx.x == 0) {
         p.evicted_pos[u] = victim_pos;
         p.kv.seg_len[u] = n - 1;
@@ -204,8 +243,22 @@ cudaError_t launch_h2o_step(const se_h2o_state& st, const void* q, const void* k
     p.lse = lse_used;
     p.evicted_pos = evicted_pos;
     p.status = status;
-    h2o_evict_kernel<<<units, 1024, 0, s>>>(p);
-    return cudaGetLastError();
+    const size_t stage_bytes = (size_t)8 * kv.seg_cap;
+    const bool staged = stage_bytes <= kEvictStageMax;
+    auto go = [&](auto kern) -> cudaError_t {
+        const size_t smem = staged ? stage_bytes : 0;
+        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(smem));
+        if (e2 != cudaSuccess) return e2;
+        kern<<<units, kEvictThreads, smem, s>>>(p);
+        return cudaGetLastError();
+    };
+    switch (G) {
+        case 4:  return staged ? go(h2o_evict_kernel<true, 1>) : go(h2o_evict_kernel<false, 1>);
+        case 8:  return staged ? go(h2o_evict_kernel<true, 2>) : go(h2o_evict_kernel<false, 2>);
+        case 16: return staged ? go(h2o_evict_kernel<true, 4>) : go(h2o_evict_kernel<false, 4>);
+        default: return staged ? go(h2o_evict_kernel<true, 0>) : go(h2o_evict_kernel<false, 0>);
+    }
 }
 
 }  // namespace se

@@ -119,6 +119,16 @@ def test_config_shaped_h2o_steps_fp32():
     run_and_check(w, out_dtype=1)
 
 
+def test_large_budget_unstaged_eviction():
+    """A budget of 12300 tokens: the segment (12301 slots) is too large for the
+    shared-memory staging of the eviction, which then works on the cache in
+    global memory."""
+    base = synth.workloads()["h2o_16k"]
+    w = synth.scaled(base, name="h2o_large", batch=1, num_q_heads=8, num_kv_heads=2, head_dim=64,
+                     ctx=14000, budget=12300, recent=64, window=8, steps=4)
+    run_and_check(w)
+
+
 def test_cache_not_full_yet_then_evicting():
     base = synth.workloads()["h2o_16k"]
     w = synth.scaled(base, name="h2o_fill", batch=2, ctx=100, budget=110, recent=8, window=8,
