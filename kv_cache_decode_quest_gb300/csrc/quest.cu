@@ -256,10 +256,11 @@ __global__ void __launch_bounds__(kSelThreads, kSelMinBlocks)
 
 // Threshold of the top K of m order-preserving keys in shared memory (256
 // threads).  Bits above the highest bit in which the largest and smallest key
-// differ are common to all keys, so the 8-bit radix digits start there; a pass
+// differ are common to all keys, so the 11-bit radix digits start there; a pass
 // ends the search early when every key of the boundary digit is kept.  On
 // return, under *mask: keys above *T are kept, and so are the first *need keys
 // equal to *T.
+constexpr int kDigitBits = 11, kDigitBins = 1 << kDigitBits;   // 8 bins per thread of 256
 __device__ void topk_threshold(const uint32_t* sk, int m, int K, int* hist, int* tmp,
                                uint32_t* red, int* sel, uint32_t* T, uint32_t* mask, int* need) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -296,21 +297,32 @@ __device__ void topk_threshold(const uint32_t* sk, int m, int K, int* hist, int*
     int remaining = K;
     int low = top + 1;                                    // bits [low, 32) are decided
     while (low > 0) {
-        const int w = min(8, low), shift = low - w;
+        // 11-bit digits: thread t owns bins 2047-8t .. 2040-8t (descending)
+        const int w = min(kDigitBits, low), shift = low - w;
         const uint32_t dm = (1u << w) - 1u;
-        hist[tid] = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hist[tid * 8 + j] = 0;
         __syncthreads();
         for (int i = tid; i < m; i += blockDim.x) {
             const uint32_t k = sk[i];
             if ((k & msk) == prefix) atomicAdd(&hist[(k >> shift) & dm], 1);
         }
         __syncthreads();
-        const int v = hist[255 - tid];                    // digits in descending order
-        const int incl = scan256(v, tmp);
-        if (incl - v < remaining && incl >= remaining) {
-            sel[0] = 255 - tid;
-            sel[1] = incl - v;
-            sel[2] = v;
+        int v8[8], v = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            v8[j] = hist[kDigitBins - 1 - (tid * 8 + j)];
+            v += v8[j];
+        }
+        int run = scan256(v, tmp) - v;                    // digits above this thread's
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (run < remaining && run + v8[j] >= remaining) {
+                sel[0] = kDigitBins - 1 - (tid * 8 + j);
+                sel[1] = run;
+                sel[2] = v8[j];
+            }
+            run += v8[j];
         }
         __syncthreads();
         prefix |= static_cast<uint32_t>(sel[0]) << shift;
@@ -327,7 +339,7 @@ __device__ void topk_threshold(const uint32_t* sk, int m, int K, int* hist, int*
 }
 
 // One CTA (256 threads) per unit: exact top-(k-1) of pages 0..n-2 by
-// (score desc, page asc) -- four 8-bit radix passes over the unit's keys
+// (score desc, page asc) -- 11-bit radix passes over the unit's keys
 // staged in shared memory -- then the pages in page order (ballots rank them
 // inside a warp, a scan over the warps places each warp's run), plus the last
 // page, which is always selected and never scored; the AttentionView chunk of
@@ -338,7 +350,7 @@ __global__ void __launch_bounds__(kTopkThreads)
                       int32_t* __restrict__ n_sel, se_view view, const uint4* __restrict__ k_new,
                       const uint4* __restrict__ v_new, int32_t* __restrict__ tickets, int* status) {
     extern __shared__ uint32_t skeys[];                   // [max_pages_per_seq] keys, then block table
-    __shared__ int hist[256];
+    __shared__ int hist[kDigitBins];
     __shared__ int tmp[33];
     __shared__ int stat[3];
     __shared__ uint32_t red[16];
