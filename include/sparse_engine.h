@@ -273,6 +273,13 @@ int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t tot
 int se_varlen_append(const se_varlen_kv* kv, const void* k_new, const void* v_new, int batch,
                      void* ws, size_t ws_bytes, se_stream_t stream);
 
+/* se_varlen_append followed by se_view_from_segments on the same stream, in one
+ * kernel (one block per sequence appends every KV head's row, then writes the
+ * view of that sequence's whole segments).  Arguments, limits and errors are
+ * those of the two calls.  Workspace: se_small_workspace(). */
+int se_varlen_append_view(const se_varlen_kv* kv, const void* k_new, const void* v_new, int batch,
+                          const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);
+
 /* ---- (c) SnapKV compaction ([tokendh] SnapKV: the last few tokens' attention
  * over the history decides what is kept; the rest is deleted physically) ------------
  * For unit (b, h), L = ctx_len[b]: window row i = 0..window-1 (position L-window+i,

@@ -75,6 +75,7 @@ SIGNATURES = {
     "se_sparse_decode_noalloc": (_I, [_VP, _VP, _I64, _VP, _VP, _I, _I, _I, _I, _F, _I, _VP,
                                       _VP, _VP, _VP]),
     "se_varlen_append": (_I, [_VP, _VP, _VP, _I, _VP, _SZ, _VP]),
+    "se_varlen_append_view": (_I, [_VP, _VP, _VP, _I, _VP, _VP, _SZ, _VP]),
     "se_snapkv_compact": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _SZ, _VP]),
     "se_h2o_step": (_I, [_VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
 }
@@ -308,6 +309,13 @@ def se_varlen_append(kv: VarlenKV, k_new, v_new, batch: int, ws, stream=None):
     c = kv.c
     _check(load().se_varlen_append(ctypes.byref(c), _p(k_new), _p(v_new), batch, _p(ws),
                                    ws.numel(), _stream(stream)), "se_varlen_append")
+
+
+def se_varlen_append_view(kv: VarlenKV, k_new, v_new, batch: int, view: View, ws, stream=None):
+    c, vc = kv.c, view.c
+    _check(load().se_varlen_append_view(ctypes.byref(c), _p(k_new), _p(v_new), batch,
+                                        ctypes.byref(vc), _p(ws), ws.numel(), _stream(stream)),
+           "se_varlen_append_view")
 
 
 def se_snapkv_compact(prefill: PagedKV, q_win, batch: int, num_q_heads: int, window: int,

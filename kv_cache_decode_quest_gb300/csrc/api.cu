@@ -245,6 +245,21 @@ int se_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
         lse, w, static_cast<cudaStream_t>(stream)));
 }
 
+int se_varlen_append_view(const se_varlen_kv* kv, const void* k_new, const void* v_new, int batch,
+                          const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream) {
+    int rc = check_varlen(kv);
+    if (rc) return rc;
+    if (batch < 0 || (batch > 0 && (!k_new || !v_new))) return SE_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SE_ERR_INVALID_ARG;
+    if (!view || !view->chunk_row || !view->n_tokens) return SE_ERR_INVALID_ARG;
+    if (view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
+    if ((int64_t)view->max_chunks * SE_PAGE_SIZE < kv->seg_cap) return SE_ERR_CAPACITY;
+    if ((rc = check_ws(ws, ws_bytes, se_small_workspace()))) return rc;
+    return cuda_status(launch_varlen_append_view(*kv, k_new, v_new, batch, *view,
+                                                 static_cast<int*>(ws),
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 int se_varlen_append(const se_varlen_kv* kv, const void* k_new, const void* v_new, int batch,
                      void* ws, size_t ws_bytes, se_stream_t stream) {
     int rc = check_varlen(kv);

@@ -223,9 +223,7 @@ cudaError_t launch_h2o_step(const se_h2o_state& st, const void* q, const void* k
     DecodeWs w = decode_ws_carve(base + off, units, G, D, SE_MAX_SPLITS);
     w.status = status;
 
-    cudaError_t e = launch_varlen_append(kv, k_new, v_new, batch, status, s);
-    if (e != cudaSuccess) return e;
-    e = launch_view_from_segments(kv, batch, view, status, s);
+    cudaError_t e = launch_varlen_append_view(kv, k_new, v_new, batch, view, status, s);
     if (e != cudaSuccess) return e;
     float* lse_used = lse ? lse : lse_int;
     e = launch_sparse_decode(kv.k, kv.v, kv.total_rows, view, q, batch, Hq, Hkv, D, scale,

@@ -41,6 +41,10 @@ cudaError_t launch_kv_append(const se_paged_kv& kv, const void* k_new, const voi
                              int batch, int* status, cudaStream_t s);
 cudaError_t launch_varlen_append(const se_varlen_kv& kv, const void* k_new, const void* v_new,
                                  int batch, int* status, cudaStream_t s);
+// the varlen append and the segment view in one kernel (one block per sequence)
+cudaError_t launch_varlen_append_view(const se_varlen_kv& kv, const void* k_new,
+                                      const void* v_new, int batch, const se_view& view,
+                                      int* status, cudaStream_t s);
 cudaError_t launch_view_from_segments(const se_varlen_kv& kv, int batch, const se_view& view,
                                       int* status, cudaStream_t s);
 

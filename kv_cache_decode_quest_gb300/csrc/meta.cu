@@ -83,8 +83,11 @@ __global__ void kv_append_kernel(se_paged_kv kv, const uint4* k_new, const uint4
     if (threadIdx.x == 0 && ok) kv.ctx_len[b] = pos + 1;
 }
 
+// One block per sequence b: the new row of every KV head of b, then (with_view)
+// the AttentionView of b's whole segments, then seq_len[b] -- one block reads
+// and writes b's lengths, so there is no race between blocks.
 __global__ void varlen_append_kernel(se_varlen_kv kv, const uint4* k_new, const uint4* v_new,
-                                     int* status) {
+                                     se_view view, int with_view, int* status) {
     pdl_wait();
     pdl_trigger();
     const int b = blockIdx.x;
@@ -123,6 +126,23 @@ __global__ void varlen_append_kernel(se_varlen_kv kv, const uint4* k_new, const 
         const int64_t row = (int64_t)kv.seg_off[u] + len;
         if (len >= 0 && len < kv.seg_cap && kv.seg_off[u] >= 0 && row < kv.total_rows)
             kv.seg_len[u] = len + 1;
+    }
+    if (with_view) {
+        __syncthreads();                       // this block's seg_len updates are visible
+        const int lim = min(kv.seg_cap, view.max_chunks * kPage);
+        for (int h = 0; h < H; ++h) {
+            const int u = b * H + h;
+            int len = kv.seg_len[u];
+            if (len < 0 || len > lim) {
+                if (threadIdx.x == 0) flag(status, SE_DEV_BAD_LENGTH);
+                len = len < 0 ? 0 : lim;
+            }
+            const int off = kv.seg_off[u];
+            const int nc = (len + kPage - 1) / kPage;
+            for (int c = threadIdx.x; c < nc; c += blockDim.x)
+                view.chunk_row[(int64_t)u * view.max_chunks + c] = off + c * kPage;
+            if (threadIdx.x == 0) view.n_tokens[u] = len;
+        }
     }
     if (threadIdx.x == 0) kv.seq_len[b] = pos + 1;
 }
@@ -165,8 +185,18 @@ cudaError_t launch_kv_append(const se_paged_kv& kv, const void* k_new, const voi
 cudaError_t launch_varlen_append(const se_varlen_kv& kv, const void* k_new, const void* v_new,
                                  int batch, int* status, cudaStream_t s) {
     if (batch == 0) return cudaSuccess;
+    se_view none = {};
     varlen_append_kernel<<<batch, 128, 0, s>>>(kv, static_cast<const uint4*>(k_new),
-                                               static_cast<const uint4*>(v_new), status);
+                                               static_cast<const uint4*>(v_new), none, 0, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_append_view(const se_varlen_kv& kv, const void* k_new,
+                                      const void* v_new, int batch, const se_view& view,
+                                      int* status, cudaStream_t s) {
+    if (batch == 0) return cudaSuccess;
+    varlen_append_kernel<<<batch, 128, 0, s>>>(kv, static_cast<const uint4*>(k_new),
+                                               static_cast<const uint4*>(v_new), view, 1, status);
     return cudaGetLastError();
 }
 

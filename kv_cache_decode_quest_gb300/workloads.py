@@ -208,9 +208,13 @@ class SnapKVRun:
         se.se_snapkv_compact(prefill, q_win, self.B, self.Hq, w.window, w.pool_kernel, w.keep,
                              w.window, self.scale, self.group_slice(g), self.ws_snap)
 
-    def step(self, s, ev_begin=None, ev_end=None):
-        se.se_varlen_append(self.cache, self.k_new[s], self.v_new[s], self.Bt, self.ws_small)
-        se.se_view_from_segments(self.cache, self.Bt, self.view, self.ws_small)
+    def step(self, s, ev_begin=None, ev_end=None, fused=True):
+        if fused:
+            se.se_varlen_append_view(self.cache, self.k_new[s], self.v_new[s], self.Bt, self.view,
+                                     self.ws_small)
+        else:
+            se.se_varlen_append(self.cache, self.k_new[s], self.v_new[s], self.Bt, self.ws_small)
+            se.se_view_from_segments(self.cache, self.Bt, self.view, self.ws_small)
         se.se_sparse_decode(self.cache.k, self.cache.v, self.view, self.q[s], self.Bt, self.Hq,
                             self.Hkv, self.D, self.scale, self.out, self.lse, self.ws_dec,
                             max_splits=self.max_splits, ev_begin=ev_begin, ev_end=ev_end)

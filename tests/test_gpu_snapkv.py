@@ -155,6 +155,30 @@ def test_decode_over_compacted_caches_small():
     assert run.status() == 0
 
 
+def test_fused_varlen_append_view_matches_separate_calls():
+    """se_varlen_append_view == se_varlen_append + se_view_from_segments, bit
+    for bit: cache rows, positions, scores, lengths and the view, step by step."""
+    base = synth.workloads()["snapkv_32k"]
+    w = synth.scaled(base, name="snap_fused", batch=3, groups=1, ctx=700, keep=100, steps=18)
+    a = SnapKVRun(w, with_score=True)
+    b = SnapKVRun(w, with_score=True)
+    for s in range(w.steps):
+        a.step(s, fused=True)
+        b.step(s, fused=False)
+        torch.cuda.synchronize()
+        assert torch.equal(a.cache.seg_len.cpu(), b.cache.seg_len.cpu()), s
+        assert torch.equal(a.cache.seq_len.cpu(), b.cache.seq_len.cpu()), s
+        assert torch.equal(a.view.n_tokens.cpu(), b.view.n_tokens.cpu()), s
+        nt = b.view.n_tokens.cpu()
+        for u in range(len(nt)):
+            nc = -(-int(nt[u]) // 16)
+            assert torch.equal(a.view.chunk_row[u, :nc].cpu(), b.view.chunk_row[u, :nc].cpu())
+        assert torch.equal(a.out.cpu(), b.out.cpu()), s
+    for name in ("k", "v", "pos", "score"):
+        assert torch.equal(getattr(a.cache, name).cpu(), getattr(b.cache, name).cpu()), name
+    assert a.status() == 0 and b.status() == 0
+
+
 @pytest.mark.slow
 def test_full_size_snapkv_32k():
     """Compaction of 8 x 32K-context prefills (every unit checked), then all 64
