@@ -34,7 +34,16 @@ METRIC = "sparse decode-attn queries/s at 1 GB300; achieved HBM GB/s vs peak"
 HEADLINE = "quest_32k"
 FLUSH_BYTES = 512 << 20
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-DECODE_SRC = os.path.join(ROOT, "kv_cache_decode_quest_gb300", "csrc", "decode.cu")
+CSRC = os.path.join(ROOT, "kv_cache_decode_quest_gb300", "csrc")
+# the Quest step as the bench runs it: "step" = append, select and decode in one
+# kernel (se_quest_step); "fused" = se_quest_select_append + se_sparse_decode
+HEADLINE_MODE = "fused"
+RAGGED_MODE = "fused"
+# per mode: the dominant kernel, its source and its committed ncu traffic record
+KERNEL_OF_MODE = {
+    "step": ("quest_step_kernel", os.path.join(CSRC, "quest_step.cu"), "quest_step_kernel_{}.json"),
+    "fused": ("decode_kernel", os.path.join(CSRC, "decode.cu"), "decode_kernel_{}.json"),
+}
 
 
 # ---------------------------------------------------------------------------
@@ -188,13 +197,16 @@ class QuestBench:
     """Drives a QuestRun through timed steps, wrapping around its step inputs
     (restoring the page summaries and lengths, outside the timed region)."""
 
-    def __init__(self, name, device):
+    def __init__(self, name, device, mode="step", step_tuning=None):
         import torch
         from kv_cache_decode_quest_gb300 import synth, workloads
         self.torch = torch
+        self.name = name
+        self.mode = mode
         self.w = synth.workloads()[name]
         inputs = synth.quest_inputs(self.w)
-        self.run = workloads.QuestRun(self.w, inputs, device=device)
+        self.run = workloads.QuestRun(self.w, inputs, device=device, mode=mode,
+                                      step_tuning=step_tuning)
         del inputs
         self.meta0 = self.run.kv.meta.clone()
         self.ctx0 = self.run.kv.ctx_len.clone()
@@ -215,9 +227,19 @@ class QuestBench:
         ctx_now = np.asarray(self.w.ctx) + s + 1
         return self.run.algorithmic_bytes(ctx_now)
 
+    def kernel_bytes(self, s):
+        """Algorithmic bytes of the timed kernel: the whole step for the
+        one-kernel step; K/V of the selected tokens, q and the output for the
+        decode kernel."""
+        b = self.bytes_for(s)
+        return b["total"] if self.mode == "step" else b["kv"] + b["small"]
+
+    def launches_per_step(self):
+        return 1 if self.mode == "step" else 3   # score, top-k (+ append), decode
+
     def capture(self):
-        """One CUDA graph per step index (the step's five kernels); replaying
-        graph s runs step s without host launch overhead."""
+        """One CUDA graph per step index (the step's kernels); replaying graph s
+        runs step s without host launch overhead."""
         torch = self.torch
         s0 = self.next_index()                    # warm-up eager step, then rewind
         self.run.step(s0)
@@ -235,9 +257,10 @@ class QuestBench:
         torch.cuda.synchronize()
 
     def capture_kernel_timing(self):
-        """A second graph per step index, the decode kernel bracketed by event
-        nodes: replaying it times the kernel as the step graphs run it (no
-        host launch latency inside the interval)."""
+        """A second graph per step index, the dominant kernel (the step kernel,
+        or the decode kernel of the two-call step) bracketed by event nodes:
+        replaying it times the kernel as the step graphs run it (no host
+        launch latency inside the interval)."""
         torch = self.torch
         side = torch.cuda.Stream()
         self.kgraphs, self.kevents = [], []
@@ -255,7 +278,7 @@ class QuestBench:
         torch.cuda.synchronize()
 
     def timed_kernel(self, K, W):
-        """Decode kernel durations over K replays of the event-bracketed step
+        """Dominant kernel durations over K replays of the event-bracketed step
         graphs (L2 flushed before each), after W untimed ones."""
         torch = self.torch
         for _ in range(W):
@@ -409,7 +432,7 @@ def run_ours(args):
     cpu = cpu_baseline(HEADLINE, seconds=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None
 
     peak, peak_kind = peaks()
-    qb = QuestBench(HEADLINE, device)
+    qb = QuestBench(HEADLINE, device, mode=HEADLINE_MODE)
     B = qb.w.batch
     qb.capture()
     barrier(ws)
@@ -422,10 +445,10 @@ def run_ours(args):
     bytes_steps = [qb.bytes_for(s) for s in idx]
     step_gbs = sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9
 
-    # the decode kernel's own duration: event nodes around it in replayed step graphs
+    # the dominant kernel's own duration: event nodes around it in replayed step graphs
     qb.capture_kernel_timing()
     kern_ms, kidx = qb.timed_kernel(args.steps, args.warmup)
-    dec_bytes = [qb.bytes_for(s)["kv"] + qb.bytes_for(s)["small"] for s in kidx]
+    dec_bytes = [qb.kernel_bytes(s) for s in kidx]
     achieved = sum(dec_bytes) / (sum(kern_ms) / 1e3) / 1e9
 
     e2e_ms, h2d, d2h = qb.timed_e2e(args.steps, args.warmup)
@@ -438,7 +461,8 @@ def run_ours(args):
 
     if rank != 0:
         return
-    traffic = profiled_traffic("decode_kernel_quest_32k.json", DECODE_SRC)
+    kname, ksrc, krec = KERNEL_OF_MODE[HEADLINE_MODE]
+    traffic = profiled_traffic(krec.format(HEADLINE), ksrc)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -449,21 +473,25 @@ def run_ours(args):
                                "Quest budget 2048 tokens per KV head, K with 4 outlier channels x8",
                    "global_batch": B * ws, "seq_len": 32768, "parallelism": f"replicas x{ws}",
                    "l2": "flushed (512 MiB write) before every timed step",
-                   "step": "Quest select with the token append fused (score, top-k + append, view) + split-K decode + merge",
+                   "step": ("token append, Quest page scoring, per-KV-head top-k, view and "
+                            "split-K decode + LSE merge in one persistent kernel (se_quest_step)"
+                            if HEADLINE_MODE == "step" else
+                            "Quest select with the token append fused (score, top-k + append, "
+                            "view) + split-K decode + merge"),
                    "launch": "one CUDA graph per step index, replayed"},
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel",
+        "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": int(sum(dec_bytes) / len(dec_bytes)),
                      "kernel_ms_per_launch": round(sum(kern_ms) / len(kern_ms), 5),
-                     "kernel_timing": "CUDA event nodes around the decode kernel inside the "
+                     "kernel_timing": f"CUDA event nodes around {kname} inside the "
                                       "replayed step graphs, L2 flushed before each",
                      "step_algorithmic_gbs": round(step_gbs, 1),
                      "step_frac": round(step_gbs / peak, 4)},
         "e2e": {"value": round(e2e_value, 1), "unit": "queries/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,          # score, top-k (with the append), plan, decode
+        "gpu_launches": qb.launches_per_step() * args.steps,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
@@ -520,19 +548,20 @@ def run_extras(args, device, peak, only=None):
 
 def ragged(out, device, peak):
     import torch
-    qb = QuestBench("ragged_quest_128k", device)
+    qb = QuestBench("ragged_quest_128k", device, mode=RAGGED_MODE)
     K = min(16, qb.w.steps)
     qb.capture()
     step_ms, _, idx = qb.timed(K, 3, graphs=True)
     qb.capture_kernel_timing()
     kern_ms, kidx = qb.timed_kernel(K, 3)
     bytes_steps = [qb.bytes_for(s) for s in idx]
-    dec = sum(qb.bytes_for(s)["kv"] + qb.bytes_for(s)["small"] for s in kidx)
+    dec = sum(qb.kernel_bytes(s) for s in kidx)
     out["ragged_quest_128k"] = {
         "queries_per_s": round(qb.w.batch * K / (sum(step_ms) / 1e3), 1),
         "ms_per_step": round(sum(step_ms) / K, 5),
-        "decode_gbs": round(dec / (sum(kern_ms) / 1e3) / 1e9, 1),
-        "decode_frac": round(dec / (sum(kern_ms) / 1e3) / 1e9 / peak, 4),
+        "kernel": KERNEL_OF_MODE[RAGGED_MODE][0],
+        "kernel_gbs": round(dec / (sum(kern_ms) / 1e3) / 1e9, 1),
+        "kernel_frac": round(dec / (sum(kern_ms) / 1e3) / 1e9 / peak, 4),
         "step_gbs": round(sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9, 1),
         "steps": K, "warmup": 3}
     del qb

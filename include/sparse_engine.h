@@ -156,6 +156,24 @@ typedef struct se_decode_opts {
                                  external event-record nodes of the graph) */
 } se_decode_opts;
 
+/* Options of se_quest_step (optional; NULL means all defaults).  The four
+ * scheduling fields change only the speed, never the results beyond the
+ * rounding order of split pieces; 0 picks the library's value. */
+typedef struct se_quest_step_opts {
+    int32_t out_dtype;        /* 0 = bf16 output (default), 1 = fp32 output */
+    int32_t max_splits;       /* decode pieces per unit at most, 1..64 (0 = 64) */
+    void* ev_kernel_begin;    /* NULL or a cudaEvent_t recorded right before / */
+    void* ev_kernel_end;      /* right after the step kernel (timing only; captured
+                                 as external event-record nodes in a graph) */
+    int32_t tile_pages;       /* candidate pages per score item (0: ~128 KB of summaries) */
+    int32_t piece_chunks;     /* 16-token chunks per decode item (0: 16) */
+    int32_t lag_topk;         /* queue rounds from a sequence's score items to its
+                                 top-k items, <= 64 (0: 8) */
+    int32_t lag_dec;          /* ... to its decode items, <= 2048, raised to lag_topk
+                                 (0: batch - 1, every decode item after every
+                                 score item) */
+} se_quest_step_opts;
+
 /* ---- library ------------------------------------------------------------ */
 const char* se_status_str(int status);      /* static string, never NULL */
 int se_version(void);                       /* ABI version, currently 1 */
@@ -164,6 +182,8 @@ int se_version(void);                       /* ABI version, currently 1 */
 size_t se_small_workspace(void);            /* ops that need only the status word */
 size_t se_quest_select_workspace(int batch, int num_kv_heads, int max_pages_per_seq);
 size_t se_sparse_decode_workspace(int num_units, int group_size, int head_dim, int max_splits);
+size_t se_quest_step_workspace(int batch, int num_kv_heads, int num_q_heads, int head_dim,
+                               int max_pages_per_seq, int max_splits);
 size_t se_snapkv_workspace(int batch, int num_kv_heads, int num_q_heads, int window, int max_ctx);
 size_t se_h2o_workspace(int batch, int num_kv_heads, int num_q_heads, int head_dim, int seg_cap);
 
@@ -265,6 +285,30 @@ int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t tot
                              const se_view* view, const void* q, int batch, int num_q_heads,
                              int num_kv_heads, int head_dim, float scale, int out_dtype, void* out,
                              float* lse, int32_t* status_out, se_stream_t stream);
+
+/* One Quest decode step in one kernel: se_quest_select_append (or
+ * se_quest_select when k_new and v_new are NULL) followed by se_sparse_decode
+ * over the view it fills, with the same selection, view, n_sel, ctx_len update
+ * and outputs (up to the rounding order of the decode's split pieces).
+ *   q, budget_tokens, sel_pages, n_sel, view: as in se_quest_select;
+ *   k_new, v_new: as in se_quest_select_append, or both NULL (no append);
+ *   scale, out, lse: as in se_sparse_decode (out bf16 or fp32 by opts->out_dtype).
+ * The kernel is a queue of work items taken in order by persistent blocks:
+ * page-score tiles, per-(sequence, KV head) top-k, decode pieces; an item waits
+ * only for items before it, so the waits cannot deadlock; each wait is bounded
+ * (a wait that runs out sets SE_DEV_TIMEOUT and the results are invalid).  The
+ * page scoring, the selection and the decode overlap across sequences, which the
+ * separate calls cannot do.
+ * Limits: batch <= 1024 and max_pages_per_seq <= 16384, else SE_ERR_UNSUPPORTED.
+ * Workspace: se_quest_step_workspace(batch, num_kv_heads, num_q_heads, head_dim,
+ * max_pages_per_seq, max_splits), zero-filled before its first use: it holds the
+ * queue counters, which every call leaves at zero (clear it again after a call
+ * that set a device error bit). */
+int se_quest_step(const se_paged_kv* kv, const void* k_new, const void* v_new, const void* q,
+                  int batch, int num_q_heads, const int32_t* budget_tokens, float scale,
+                  const se_quest_step_opts* opts, int32_t* sel_pages, int32_t* n_sel,
+                  const se_view* view, void* out, float* lse, void* ws, size_t ws_bytes,
+                  se_stream_t stream);
 
 /* Varlen append for decode over compacted caches: writes k_new/v_new (bf16
  * [batch][num_kv_heads][head_dim]) at row seg_off[u] + seg_len[u] with

@@ -54,6 +54,13 @@ class DecodeOptsC(ctypes.Structure):
                 ("ev_kernel_begin", ctypes.c_void_p), ("ev_kernel_end", ctypes.c_void_p)]
 
 
+class QuestStepOptsC(ctypes.Structure):
+    _fields_ = [("out_dtype", ctypes.c_int32), ("max_splits", ctypes.c_int32),
+                ("ev_kernel_begin", ctypes.c_void_p), ("ev_kernel_end", ctypes.c_void_p),
+                ("tile_pages", ctypes.c_int32), ("piece_chunks", ctypes.c_int32),
+                ("lag_topk", ctypes.c_int32), ("lag_dec", ctypes.c_int32)]
+
+
 # C entry points: name -> (restype, argtypes)
 _VP, _I, _SZ, _F, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_int64
 SIGNATURES = {
@@ -62,6 +69,7 @@ SIGNATURES = {
     "se_small_workspace": (_SZ, []),
     "se_quest_select_workspace": (_SZ, [_I, _I, _I]),
     "se_sparse_decode_workspace": (_SZ, [_I, _I, _I, _I]),
+    "se_quest_step_workspace": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "se_snapkv_workspace": (_SZ, [_I, _I, _I, _I, _I]),
     "se_h2o_workspace": (_SZ, [_I, _I, _I, _I, _I]),
     "se_page_meta_build": (_I, [_VP, _I, _VP, _SZ, _VP]),
@@ -69,6 +77,8 @@ SIGNATURES = {
     "se_quest_select": (_I, [_VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "se_quest_select_append": (_I, [_VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ,
                                     _VP]),
+    "se_quest_step": (_I, [_VP, _VP, _VP, _VP, _I, _I, _VP, _F, _VP, _VP, _VP, _VP, _VP, _VP,
+                           _VP, _SZ, _VP]),
     "se_view_from_segments": (_I, [_VP, _I, _VP, _VP, _SZ, _VP]),
     "se_sparse_decode": (_I, [_VP, _VP, _I64, _VP, _VP, _I, _I, _I, _I, _F, _VP, _VP, _VP,
                               _VP, _SZ, _VP]),
@@ -235,6 +245,12 @@ def se_sparse_decode_workspace(num_units, group_size, head_dim, max_splits=64) -
     return load().se_sparse_decode_workspace(num_units, group_size, head_dim, max_splits)
 
 
+def se_quest_step_workspace(batch, num_kv_heads, num_q_heads, head_dim, max_pages_per_seq,
+                            max_splits=64) -> int:
+    return load().se_quest_step_workspace(batch, num_kv_heads, num_q_heads, head_dim,
+                                          max_pages_per_seq, max_splits)
+
+
 def se_snapkv_workspace(batch, num_kv_heads, num_q_heads, window, max_ctx) -> int:
     return load().se_snapkv_workspace(batch, num_kv_heads, num_q_heads, window, max_ctx)
 
@@ -270,6 +286,23 @@ def se_quest_select_append(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads
                                          num_q_heads, _p(budget_tokens), _p(sel_pages),
                                          _p(n_sel), ctypes.byref(vc), _p(ws), ws.numel(),
                                          _stream(stream)), "se_quest_select_append")
+
+
+def se_quest_step(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads: int, budget_tokens,
+                  scale: float, sel_pages, n_sel, view: View, out, lse, ws, out_dtype: int = 0,
+                  max_splits: int = 64, tile_pages: int = 0, piece_chunks: int = 0,
+                  lag_topk: int = 0, lag_dec: int = 0, ev_begin=None, ev_end=None, stream=None):
+    """One Quest decode step (append when k_new/v_new are given, select, decode)
+    in one kernel."""
+    c, vc = kv.c, view.c
+    opts = QuestStepOptsC(out_dtype, max_splits,
+                          ev_begin.cuda_event if ev_begin is not None else None,
+                          ev_end.cuda_event if ev_end is not None else None,
+                          tile_pages, piece_chunks, lag_topk, lag_dec)
+    _check(load().se_quest_step(ctypes.byref(c), _p(k_new), _p(v_new), _p(q), batch, num_q_heads,
+                                _p(budget_tokens), scale, ctypes.byref(opts), _p(sel_pages),
+                                _p(n_sel), ctypes.byref(vc), _p(out), _p(lse), _p(ws), ws.numel(),
+                                _stream(stream)), "se_quest_step")
 
 
 def se_view_from_segments(kv: VarlenKV, batch: int, view: View, ws, stream=None):

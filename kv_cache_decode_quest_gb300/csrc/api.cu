@@ -2,8 +2,8 @@
 // launches.  Every entry point validates its arguments on the host, returns a
 // negative status without launching when they are wrong, and otherwise
 // enqueues its kernels on the caller's stream.
-#include <atomic>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -195,6 +195,61 @@ int se_quest_select_append(const se_paged_kv* kv, const void* k_new, const void*
     return cuda_status(launch_quest_select(*kv, q, batch, num_q_heads, budget_tokens, sel_pages,
                                            n_sel, *view, k_new, v_new, ws, static_cast<int*>(ws),
                                            static_cast<cudaStream_t>(stream)));
+}
+
+size_t se_quest_step_workspace(int batch, int num_kv_heads, int num_q_heads, int head_dim,
+                               int max_pages_per_seq, int max_splits) {
+    if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 ||
+        max_pages_per_seq < 0 || max_splits <= 0 || num_q_heads % num_kv_heads)
+        return 0;
+    return quest_step_ws_bytes(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim,
+                               max_pages_per_seq, max_splits);
+}
+
+int se_quest_step(const se_paged_kv* kv, const void* k_new, const void* v_new, const void* q,
+                  int batch, int num_q_heads, const int32_t* budget_tokens, float scale,
+                  const se_quest_step_opts* opts, int32_t* sel_pages, int32_t* n_sel,
+                  const se_view* view, void* out, float* lse, void* ws, size_t ws_bytes,
+                  se_stream_t stream) {
+    if ((k_new == nullptr) != (v_new == nullptr)) return SE_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SE_ERR_INVALID_ARG;
+    int rc = check_paged(kv, true);
+    if (rc) return rc;
+    if (batch < 0 || num_q_heads <= 0) return SE_ERR_INVALID_ARG;
+    if (num_q_heads % kv->num_kv_heads || !group_ok(num_q_heads / kv->num_kv_heads))
+        return SE_ERR_UNSUPPORTED;
+    if (batch > 0 && (!q || !budget_tokens || !sel_pages || !n_sel || !view || !view->chunk_row ||
+                      !view->n_tokens || !out))
+        return SE_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16)) return SE_ERR_INVALID_ARG;
+    if (view && view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
+    if (view && view->max_chunks < kv->max_pages_per_seq) return SE_ERR_CAPACITY;
+    if (batch > 1024 || kv->max_pages_per_seq > 16384) return SE_ERR_UNSUPPORTED;
+    se_quest_step_opts o = {0, SE_MAX_SPLITS, nullptr, nullptr, 0, 0, 0, 0};
+    if (opts) {
+        o = *opts;
+        if (o.max_splits == 0) o.max_splits = SE_MAX_SPLITS;
+    }
+    if (o.out_dtype != 0 && o.out_dtype != 1) return SE_ERR_INVALID_ARG;
+    if (o.max_splits < 1 || o.max_splits > SE_MAX_SPLITS) return SE_ERR_INVALID_ARG;
+    if (o.tile_pages < 0 || o.piece_chunks < 0 || o.lag_topk < 0 || o.lag_dec < 0)
+        return SE_ERR_INVALID_ARG;
+    if (o.lag_topk > 64 || o.lag_dec > 2048) return SE_ERR_INVALID_ARG;
+    const int G = num_q_heads / kv->num_kv_heads;
+    const int lag_dec = std::max(std::max(o.lag_topk, 8), o.lag_dec > 0 ? o.lag_dec : batch - 1);
+    if (quest_step_smem_bytes(batch, kv->num_kv_heads, kv->head_dim, G, kv->max_pages_per_seq,
+                              lag_dec) > 227 * 1024)
+        return SE_ERR_UNSUPPORTED;
+    if ((rc = check_ws(ws, ws_bytes,
+                       se_quest_step_workspace(batch, kv->num_kv_heads, num_q_heads, kv->head_dim,
+                                               kv->max_pages_per_seq, o.max_splits))))
+        return rc;
+    if (batch == 0) return SE_OK;
+    const StepTuning tune = {o.tile_pages, o.piece_chunks, o.lag_topk, o.lag_dec};
+    return cuda_status(launch_quest_step(
+        *kv, k_new, v_new, q, batch, num_q_heads, budget_tokens, scale, o.out_dtype, o.max_splits,
+        tune, sel_pages, n_sel, *view, out, lse, ws, static_cast<cudaEvent_t>(o.ev_kernel_begin),
+        static_cast<cudaEvent_t>(o.ev_kernel_end), static_cast<cudaStream_t>(stream)));
 }
 
 int se_view_from_segments(const se_varlen_kv* kv, int batch, const se_view* view, void* ws,

@@ -57,6 +57,19 @@ cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch,
                                 const se_view& view, const void* k_new, const void* v_new,
                                 void* ws, int* status, cudaStream_t s);
 
+// ---- quest_step.cu ----
+struct StepTuning {
+    int tile_pages, piece_chunks, lag_topk, lag_dec;   // 0 / negative: defaults
+};
+size_t quest_step_ws_bytes(int batch, int H, int G, int D, int max_pages, int max_splits);
+size_t quest_step_smem_bytes(int batch, int H, int D, int G, int max_pages, int lag_dec);
+cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const void* v_new,
+                              const void* q, int batch, int num_q_heads, const int32_t* budget,
+                              float scale, int out_dtype, int max_splits, const StepTuning& tune,
+                              int32_t* sel_pages, int32_t* n_sel, const se_view& view, void* out,
+                              float* lse, void* ws, cudaEvent_t ev_begin, cudaEvent_t ev_end,
+                              cudaStream_t s);
+
 // ---- decode.cu ----
 struct DecodeWs {
     int* status;

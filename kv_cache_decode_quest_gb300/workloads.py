@@ -42,12 +42,23 @@ def paged_layout(seqs_k, seqs_v, lengths, block_table, num_pages, num_kv_heads, 
 
 
 class QuestRun:
-    """Paged KV + Quest selection + split-K decode, one appended token per step."""
+    """Paged KV + Quest selection + split-K decode, one appended token per step.
+
+    mode: "step"     -- se_quest_step: append, select and decode in one kernel;
+          "fused"    -- se_quest_select_append, then se_sparse_decode;
+          "separate" -- se_kv_append, se_quest_select, se_sparse_decode.
+    step_tuning: scheduling fields of se_quest_step_opts (mode "step")."""
+
+    MODES = ("step", "fused", "separate")
 
     def __init__(self, w: synth.QuestWorkload, inputs: dict, out_dtype: int = 0,
-                 max_splits: int | None = None, device="cuda", fused: bool = True):
+                 max_splits: int | None = None, device="cuda", mode: str = "step",
+                 step_tuning: dict | None = None):
+        if mode not in self.MODES:
+            raise ValueError(f"mode {mode!r} not in {self.MODES}")
         self.w = w
-        self.fused = fused
+        self.mode = mode
+        self.step_tuning = dict(step_tuning or {})
         B, Hq, Hkv, D, S = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.steps
         self.B, self.Hq, self.Hkv, self.D, self.S = B, Hq, Hkv, D, S
         self.G = Hq // Hkv
@@ -82,6 +93,8 @@ class QuestRun:
         self.ws_sel = se.workspace(se.se_quest_select_workspace(B, Hkv, maxp), device)
         self.ws_dec = se.workspace(se.se_sparse_decode_workspace(units, self.G, D, self.max_splits),
                                    device)
+        self.ws_step = se.workspace(se.se_quest_step_workspace(B, Hkv, Hq, D, maxp, self.max_splits),
+                                    device)
         odt = torch.float32 if out_dtype == 1 else torch.bfloat16
         self.out = torch.zeros(B, Hq, D, dtype=odt, device=device)
         self.lse = torch.zeros(B, Hq, dtype=torch.float32, device=device)
@@ -107,9 +120,20 @@ class QuestRun:
                             out_dtype=self.out_dtype, max_splits=self.max_splits,
                             ev_begin=ev_begin, ev_end=ev_end)
 
+    def one_kernel_step(self, s: int, out=None, lse=None, ev_begin=None, ev_end=None):
+        """Append, select and decode in one kernel (se_quest_step)."""
+        se.se_quest_step(self.kv, self.k_new[s], self.v_new[s], self.q[s], self.B, self.Hq,
+                         self.budget, self.scale, self.sel, self.n_sel, self.view,
+                         self.out if out is None else out, self.lse if lse is None else lse,
+                         self.ws_step, out_dtype=self.out_dtype, max_splits=self.max_splits,
+                         ev_begin=ev_begin, ev_end=ev_end, **self.step_tuning)
+
     def step(self, s: int, out=None, lse=None, ev_begin=None, ev_end=None):
         """One decode step: append the step's token, select pages, attend."""
-        if self.fused:
+        if self.mode == "step":
+            self.one_kernel_step(s, out, lse, ev_begin, ev_end)
+            return
+        if self.mode == "fused":
             self.append_select(s)
         else:
             self.append(s)
@@ -118,7 +142,7 @@ class QuestRun:
 
     def status(self) -> int:
         return se.status_word(self.ws_small) | se.status_word(self.ws_sel) | \
-            se.status_word(self.ws_dec)
+            se.status_word(self.ws_dec) | se.status_word(self.ws_step)
 
     def algorithmic_bytes(self, ctx_now: np.ndarray) -> dict:
         """Bytes one step must move at least, given each sequence's length after

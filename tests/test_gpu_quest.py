@@ -72,9 +72,11 @@ def check_step(run, inputs, s, units=None):
     return worst, allowed
 
 
-def run_and_check(w, out_dtype=0, max_splits=None, steps=None, units=None, fused=True):
+def run_and_check(w, out_dtype=0, max_splits=None, steps=None, units=None, mode="step",
+                  step_tuning=None):
     inputs = synth.quest_inputs(w)
-    run = QuestRun(w, inputs, out_dtype=out_dtype, max_splits=max_splits, fused=fused)
+    run = QuestRun(w, inputs, out_dtype=out_dtype, max_splits=max_splits, mode=mode,
+                   step_tuning=step_tuning)
     worst = 0.0
     for s in range(w.steps):
         run.step(s)
@@ -87,11 +89,11 @@ def run_and_check(w, out_dtype=0, max_splits=None, steps=None, units=None, fused
     return worst
 
 
-def test_tiny_quest_single_query():
+@pytest.mark.parametrize("mode", QuestRun.MODES)
+def test_tiny_quest_single_query(mode):
     w = synth.workloads()["tiny_quest"]
-    run_and_check(w)
-    run_and_check(w, out_dtype=1)
-    run_and_check(w, fused=False)
+    run_and_check(w, mode=mode)
+    run_and_check(w, out_dtype=1, mode=mode)
 
 
 def test_fused_append_select_matches_separate_calls():
@@ -103,8 +105,8 @@ def test_fused_append_select_matches_separate_calls():
     w = synth.scaled(base, name="quest_fused", batch=5, ctx=(15, 16, 31, 1000, 2047),
                      budget=(64, 64, 256, 128, U32), steps=20)
     inputs = synth.quest_inputs(w)
-    a = QuestRun(w, inputs, fused=True)
-    b = QuestRun(w, inputs, fused=False)
+    a = QuestRun(w, inputs, mode="fused")
+    b = QuestRun(w, inputs, mode="separate")
     for s in range(w.steps):
         a.step(s)
         b.step(s)
@@ -125,11 +127,54 @@ def test_fused_append_select_matches_separate_calls():
 
 
 @pytest.mark.parametrize("out_dtype", [0, 1])
-def test_ragged_multi_step_outliers(out_dtype):
+@pytest.mark.parametrize("mode", ["step", "fused"])
+def test_ragged_multi_step_outliers(out_dtype, mode):
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name="quest_ragged_small", batch=4, ctx=(1000, 2053, 300, 0),
                      budget=(256, 512, 4096, 64), steps=5)
-    run_and_check(w, out_dtype=out_dtype)
+    run_and_check(w, out_dtype=out_dtype, mode=mode)
+
+
+def test_one_kernel_step_matches_two_calls():
+    """se_quest_step == se_quest_select_append + se_sparse_decode: selections,
+    view, lengths, cache rows and page summaries bit for bit, outputs within
+    the bf16 rounding of their different split pieces; steps open new pages
+    (contexts 15, 16, 31, 1000 and 2047 tokens at the start, one sequence with
+    every page selected), and the scheduling knobs (tile, piece, lags) are
+    varied from step to step."""
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name="quest_step_eq", batch=5, ctx=(15, 16, 31, 1000, 2047),
+                     budget=(64, 64, 256, 128, U32), steps=12)
+    inputs = synth.quest_inputs(w)
+    a = QuestRun(w, inputs, mode="step", out_dtype=1)
+    b = QuestRun(w, inputs, mode="fused", out_dtype=1)
+    knobs = [{}, {"tile_pages": 1}, {"tile_pages": 3, "piece_chunks": 1},
+             {"lag_topk": 1, "lag_dec": 1}, {"lag_topk": 7, "lag_dec": 30},
+             {"piece_chunks": 2, "lag_topk": 2, "lag_dec": 3}]
+    for s in range(w.steps):
+        a.step_tuning = knobs[s % len(knobs)]
+        a.step(s)
+        b.step(s)
+        torch.cuda.synchronize()
+        n = b.n_sel.cpu()
+        assert torch.equal(a.n_sel.cpu(), n), f"step {s}"
+        for u in range(len(n)):
+            k = int(n[u])
+            assert torch.equal(a.sel[u, :k].cpu(), b.sel[u, :k].cpu()), f"step {s} unit {u}"
+            assert torch.equal(a.view.chunk_row[u, :k].cpu(), b.view.chunk_row[u, :k].cpu())
+        assert torch.equal(a.view.n_tokens.cpu(), b.view.n_tokens.cpu())
+        assert torch.equal(a.kv.ctx_len.cpu(), b.kv.ctx_len.cpu())
+        assert max_abs(a.out.double().cpu().numpy(), b.out.double().cpu().numpy()) <= 1e-4
+        assert max_abs(a.lse.cpu().numpy(), b.lse.cpu().numpy()) <= 1e-4
+    assert torch.equal(a.kv.k.cpu(), b.kv.k.cpu())
+    assert torch.equal(a.kv.v.cpu(), b.kv.v.cpu())
+    assert torch.equal(a.kv.meta.cpu(), b.kv.meta.cpu())
+    assert a.status() == 0 and b.status() == 0
+    # the queue words (item counter, finished CTAs, abort) follow the status
+    # header and the keys, and every call leaves them at zero
+    keys_bytes = a.B * a.Hkv * a.sel.shape[1] * 4
+    sync = (256 + (keys_bytes + 255) // 256 * 256) // 4
+    assert int(a.ws_step.view(torch.int32)[sync:sync + 3].abs().sum().item()) == 0, "queue not reset"
 
 
 # (hkv 8 at d 128 and hkv 3 at d 64 take the scoring path with coefficients in
@@ -137,26 +182,30 @@ def test_ragged_multi_step_outliers(out_dtype):
 @pytest.mark.parametrize("hq,hkv,d", [(4, 4, 128), (8, 4, 64), (32, 4, 128), (32, 2, 64),
                                        (64, 4, 128), (16, 4, 64), (64, 8, 128), (6, 3, 64),
                                        (16, 1, 128)])
-def test_group_sizes_and_head_dims(hq, hkv, d):
+@pytest.mark.parametrize("mode", ["step", "fused"])
+def test_group_sizes_and_head_dims(hq, hkv, d, mode):
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name=f"quest_g{hq // hkv}_d{d}", batch=2, num_q_heads=hq,
                      num_kv_heads=hkv, head_dim=d, ctx=(777, 1600), budget=(128, 256), steps=2)
-    run_and_check(w)
+    run_and_check(w, mode=mode)
 
 
-def test_budget_of_one_page_and_full_budget():
+@pytest.mark.parametrize("mode", ["step", "fused"])
+def test_budget_of_one_page_and_full_budget(mode):
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name="quest_edges", batch=3, ctx=(500, 129, 2000),
                      budget=(16, U32, U32), steps=2)
-    run_and_check(w, out_dtype=1)
+    run_and_check(w, out_dtype=1, mode=mode)
 
 
 @pytest.mark.parametrize("max_splits", [1, 3, 64])
-def test_split_count_does_not_change_results(max_splits):
+@pytest.mark.parametrize("mode", ["step", "fused"])
+def test_split_count_does_not_change_results(max_splits, mode):
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name="quest_splits", batch=2, ctx=(3000, 1234), budget=(U32, 1024),
                      steps=1)
-    run_and_check(w, out_dtype=1, max_splits=max_splits)
+    run_and_check(w, out_dtype=1, max_splits=max_splits, mode=mode,
+                  step_tuning={"piece_chunks": 4} if mode == "step" else None)
 
 
 def test_many_units_block_plan():
@@ -166,7 +215,8 @@ def test_many_units_block_plan():
     B = 160
     ctx = tuple(int(x) for x in (np.arange(B) * 37 % 900 + 20))
     w = synth.scaled(base, name="quest_many_units", batch=B, ctx=ctx, budget=(256,) * B, steps=1)
-    run_and_check(w, units=range(0, B * 4, 7))
+    run_and_check(w, units=range(0, B * 4, 7), mode="fused")
+    run_and_check(w, units=range(0, B * 4, 7), mode="step")
 
 
 def test_stream_k_plan():
@@ -177,14 +227,16 @@ def test_stream_k_plan():
     B = 100
     w = synth.scaled(base, name="quest_streamk", batch=B, ctx=(30000,) + (40,) * (B - 1),
                      budget=(U32,) * B, steps=1)
-    run_and_check(w, out_dtype=1, units=[0, 1, 2, 3, 4, 5, 100, 399])
+    run_and_check(w, out_dtype=1, units=[0, 1, 2, 3, 4, 5, 100, 399], mode="fused")
+    run_and_check(w, out_dtype=1, units=[0, 1, 2, 3, 4, 5, 100, 399], mode="step")
 
 
 def test_ragged_long_scaled():
     base = synth.workloads()["ragged_quest_128k"]
     w = synth.scaled(base, name="ragged_small", batch=4, ctx=(2300, 4100, 3333, 2900),
                      budget=(U32, 512, U32, 512), steps=3)
-    run_and_check(w)
+    run_and_check(w, mode="fused")
+    run_and_check(w, mode="step")
 
 
 @pytest.mark.slow
@@ -193,6 +245,7 @@ def test_full_size_quest_32k_sampled():
     launch configuration; the oracle checks steps 0, 31, 63 on every unit."""
     w = synth.workloads()["quest_32k"]
     run_and_check(w, steps={0, 31, 63})
+    run_and_check(w, steps={0, 63}, mode="fused")
 
 
 @pytest.mark.slow
@@ -200,4 +253,5 @@ def test_full_size_ragged_128k_sampled():
     """The ragged 64K-128K workload (half dense-equivalent), all 32 steps on
     the GPU; the oracle checks steps 0 and 31 on units of every sequence."""
     w = synth.workloads()["ragged_quest_128k"]
-    run_and_check(w, steps={0, 31}, units=list(range(0, 32, 3)))
+    run_and_check(w, steps={0, 31}, units=list(range(0, 32, 3)), mode="fused")
+    run_and_check(w, steps={0, 31}, units=list(range(0, 32, 3)), mode="step")
