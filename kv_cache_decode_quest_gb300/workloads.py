@@ -77,11 +77,18 @@ class QuestRun:
             ctx_len=torch.from_numpy(ctx.astype(np.int32)).to(device))
         del K, V
         # per-step inputs
-        self.q = to_dev_bf16(inputs["q"], device)                               # [S][B][Hq][D]
+        # per-step inputs, one contiguous row per step: q [B][Hq][D], then the
+        # appended k and v [B][Hkv][D] (a caller feeding the step from host
+        # memory copies one row per step)
         kn = np.stack([np.stack([inputs["k"][b][:, ctx[b] + s] for b in range(B)]) for s in range(S)])
         vn = np.stack([np.stack([inputs["v"][b][:, ctx[b] + s] for b in range(B)]) for s in range(S)])
-        self.k_new = to_dev_bf16(kn, device)                                     # [S][B][Hkv][D]
-        self.v_new = to_dev_bf16(vn, device)
+        nq, nk = B * Hq * D, B * Hkv * D
+        rows = np.concatenate([np.asarray(inputs["q"]).reshape(S, nq), kn.reshape(S, nk),
+                               vn.reshape(S, nk)], axis=1)
+        self.step_inputs = to_dev_bf16(rows, device)                             # [S][nq + 2 nk]
+        self.q = self.step_inputs[:, :nq].view(S, B, Hq, D)
+        self.k_new = self.step_inputs[:, nq:nq + nk].view(S, B, Hkv, D)
+        self.v_new = self.step_inputs[:, nq + nk:].view(S, B, Hkv, D)
         self.budget = torch.tensor([min(b, 2 ** 31 - 1) for b in w.budget], dtype=torch.int32,
                                    device=device)
         units = B * Hkv
