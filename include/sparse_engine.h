@@ -256,6 +256,7 @@ int se_view_from_segments(const se_varlen_kv* kv, int batch, const se_view* view
  * k_rows, v_rows bf16 [total_rows][head_dim]; q bf16 [batch][num_q_heads][head_dim];
  * out bf16 or fp32 [batch][num_q_heads][head_dim]; lse fp32 [batch][num_q_heads] or NULL.
  * A chunk row outside [0, total_rows) sets SE_DEV_BAD_INDEX and counts as empty.
+ * view->max_chunks <= 2^20 (16M tokens per unit), else SE_ERR_UNSUPPORTED.
  * Workspace: se_sparse_decode_workspace(num_units, G, head_dim, max_splits),
  * zero-filled before its first use: it holds the arrival counters of split
  * units, which every call leaves at zero (clear it again after a call that set

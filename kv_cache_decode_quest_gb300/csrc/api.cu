@@ -279,6 +279,7 @@ int se_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
     if (!aligned(k_rows, 16) || !aligned(v_rows, 16) || !aligned(q, 16) || !aligned(out, 16))
         return SE_ERR_INVALID_ARG;
     if (view->num_units != batch * num_kv_heads || view->max_chunks <= 0) return SE_ERR_INVALID_ARG;
+    if (view->max_chunks > (1 << 20)) return SE_ERR_UNSUPPORTED;
     const int G = num_q_heads / num_kv_heads;
     se_decode_opts o = {0, SE_MAX_SPLITS, nullptr, 0, nullptr, nullptr};
     if (opts) {

@@ -68,29 +68,35 @@ struct DecodeParams {
     int* status;
 };
 
+// Up to this many units (and no more than the grid) the decode CTAs plan for
+// themselves; above it the block-wide plan kernel runs first.
+constexpr int kSelfPlanUnits = 512;
+
 // One piece per CTA, computed by one warp of every CTA (no plan kernel): unit
 // u gets pieces_u = max(1, min(max_splits, nc_u, floor(nc_u * share / total)))
 // pieces of nc_u * k / pieces_u chunks, with share = grid lowered until the
 // pieces fit the grid (share 0 gives one piece per unit, which fits since
 // units <= grid).  Piece k of unit u is item off_u + k, run by CTA off_u + k.
-// Writes this CTA's item (unit, first chunk, end chunk, partial slot or -1)
-// and its unit's (first item, pieces); *has = 0 when the CTA runs none.
-__device__ __noinline__ void plan_own_piece(const DecodeParams& p, int lane, int4* item,
-                                            int2* uitem, int* has) {
+// tok: every unit's clamped token count, staged in shared memory by the whole
+// CTA in one round trip.  The loops stay rolled: the plan runs once per launch,
+// right after the previous kernel, when its instructions are not cached.
+// Writes this CTA's item (unit, first chunk, end chunk, partial slot or -1),
+// its unit's (first item, pieces) and token count; *has = 0 when the CTA runs
+// none.
+__device__ __noinline__ void plan_own_piece(const DecodeParams& p, const int* tok, int lane,
+                                            int4* item, int2* uitem, int* ntok, int* has) {
     const int units = p.num_units, grid = static_cast<int>(gridDim.x);
-    const int c = static_cast<int>(blockIdx.x), lim = p.max_chunks * kPage;
-    auto chunks_of = [&](int u) {
-        int n = p.n_tokens[u];
-        n = n < 0 ? 0 : (n > lim ? lim : n);               // the consumers flag bad lengths
-        return (n + kPage - 1) / kPage;
-    };
+    const int c = static_cast<int>(blockIdx.x);
     int total = 0;
 #pragma unroll 1
     for (int base = 0; base < units; base += 32)
-        total += __reduce_add_sync(0xffffffffu, base + lane < units ? chunks_of(base + lane) : 0);
-    const int64_t tot = max(1, total);
+        total += __reduce_add_sync(0xffffffffu,
+                                   base + lane < units ? (tok[base + lane] + kPage - 1) / kPage : 0);
+    // 32-bit products: nc <= max_chunks <= 2^20 (a host-side limit) and
+    // share, k <= 2048 keep nc * share and nc * k below 2^31
+    const int tot = max(1, total);
     auto pieces_of = [&](int nc, int share) {
-        return nc == 0 ? 1 : max(1, min(p.max_splits, min(nc, (int)((int64_t)nc * share / tot))));
+        return nc == 0 ? 1 : max(1, min(p.max_splits, min(nc, nc * share / tot)));
     };
     // one pass per share: the scan over the pieces both finds this CTA's piece
     // and totals them; a share whose pieces do not fit the grid is lowered
@@ -103,7 +109,8 @@ __device__ __noinline__ void plan_own_piece(const DecodeParams& p, int lane, int
 #pragma unroll 1
         for (int base = 0; base < units; base += 32) {
             const int u = base + lane;
-            const int nc = u < units ? chunks_of(u) : 0;
+            const int n = u < units ? tok[u] : 0;
+            const int nc = (n + kPage - 1) / kPage;
             const int pc = u < units ? pieces_of(nc, share) : 0;
             int x = pc;
 #pragma unroll
@@ -114,9 +121,9 @@ __device__ __noinline__ void plan_own_piece(const DecodeParams& p, int lane, int
             const int off = run + x - pc;
             if (u < units && c >= off && c < off + pc) {
                 const int k = c - off;
-                const int c0 = (int)((int64_t)nc * k / pc), c1 = (int)((int64_t)nc * (k + 1) / pc);
-                *item = make_int4(u, c0, c1, pc == 1 ? -1 : c);
+                *item = make_int4(u, nc * k / pc, nc * (k + 1) / pc, pc == 1 ? -1 : c);
                 *uitem = make_int2(off, pc);
+                *ntok = n;
                 *has = 1;
             }
             run += __shfl_sync(0xffffffffu, x, 31);
@@ -170,8 +177,19 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
     // piece (item index blockIdx.x) when it plans for itself
     __shared__ int4 s_item;
     __shared__ int2 s_uitem;
-    __shared__ int s_has;
-    if (p.self_plan && warp == kConsumerWarps) plan_own_piece(p, lane, &s_item, &s_uitem, &s_has);
+    __shared__ int s_ntok, s_has;
+    __shared__ int s_tok[kSelfPlanUnits];
+    if (p.self_plan) {
+        // every unit's token count, one load per thread (clamped: the
+        // consumers flag a bad length)
+        const int lim = p.max_chunks * kPage;
+        for (int u = threadIdx.x; u < p.num_units; u += blockDim.x) {
+            const int n = p.n_tokens[u];
+            s_tok[u] = n < 0 ? 0 : (n > lim ? lim : n);
+        }
+        __syncthreads();
+        if (warp == kConsumerWarps) plan_own_piece(p, s_tok, lane, &s_item, &s_uitem, &s_ntok, &s_has);
+    }
     __syncthreads();
     int it_begin, it_end;
     if (p.self_plan) {
@@ -206,9 +224,12 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
         auto fetch = [&](int it) {
             if (it >= it_end) return;
             nitem = it == static_cast<int>(blockIdx.x) ? spec : p.items[it];
-            nntok = unit_tokens(p, nitem.x);
+            // the chunk rows go out first; the planned piece's token count is
+            // already in shared memory (no second dependent round trip)
             const int32_t* c = p.chunk_row + (int64_t)nitem.x * p.max_chunks;
             nrow = nitem.y + lane < nitem.z ? c[nitem.y + lane] : -1;
+            nntok = (p.self_plan && it == static_cast<int>(blockIdx.x)) ? s_ntok
+                                                                          : unit_tokens(p, nitem.x);
         };
         fetch(it_begin);
         for (int it = it_begin; it < it_end; ++it) {
@@ -454,10 +475,6 @@ __global__ void __launch_bounds__(1024)
     if (threadIdx.x == 0) *n_items = n;
 }
 
-// Up to this many units (and no more than the grid) the decode CTAs plan for
-// themselves; above it the block-wide plan kernel runs first.
-constexpr int kSelfPlanUnits = 512;
-
 template <int D, int NT, bool TWO>
 cudaError_t run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, cudaStream_t s) {
@@ -472,7 +489,9 @@ cudaError_t run_decode(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
 template <int D, int NT>
 int ctas_per_sm() {
     using S = DecRing<D, NT>;
-    return S::kSmem * 2 + 2048 <= 228 * 1024 ? 2 : 1;
+    // dynamic ring + the kernel's static shared memory (plan staging), and the
+    // 1 KB the hardware reserves per CTA
+    return (S::kSmem + kSelfPlanUnits * 4 + 64) * 2 + 2048 <= 228 * 1024 ? 2 : 1;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -518,6 +537,7 @@ cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t
                                  const DecodeWs& w, cudaStream_t s) {
     const int units = batch * num_kv_heads;
     if (units == 0) return cudaSuccess;
+    if (view.max_chunks > (1 << 20)) return cudaErrorInvalidValue;   // the plan's 32-bit products
     const int G = num_q_heads / num_kv_heads;
     const int NT = G > 8 ? 2 : 1;
     CUtensorMap tk, tv;

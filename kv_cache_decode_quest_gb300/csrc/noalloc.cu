@@ -67,6 +67,7 @@ int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t tot
     if ((a & 15) || (reinterpret_cast<uintptr_t>(out) & 15)) return SE_ERR_INVALID_ARG;
     const int units = batch * num_kv_heads;
     if (view->num_units != units || view->max_chunks <= 0) return SE_ERR_INVALID_ARG;
+    if (view->max_chunks > (1 << 20)) return SE_ERR_UNSUPPORTED;
 
     // The most split-K pieces per unit whose partials fit the fixed scratch.
     int max_splits = SE_MAX_SPLITS;
