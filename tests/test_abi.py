@@ -103,3 +103,49 @@ def test_zero_batch_is_a_no_op(lib):
     view = binding.ViewC(None, None, 0, 0)
     assert lib.se_sparse_decode(None, None, 0, ctypes.byref(view), None, 0, 32, 4, 128, 0.1,
                                 None, None, None, None, 0, None) == 0
+
+
+def test_quest_step_workspace_and_host_validation(lib):
+    """se_quest_step: workspace size, and every argument error caught on the
+    host before a launch (fake, never dereferenced pointers)."""
+    w = lib.se_quest_step_workspace(16, 4, 32, 128, 2052, 64)
+    assert w % 256 == 0
+    assert w >= 16 * 4 * 2052 * 4 + 16 * 4 * 64 * 8 * 128 * 4     # keys + decode partials
+    assert lib.se_quest_step_workspace(16, 4, 30, 128, 2052, 64) == 0   # Hq not a multiple of Hkv
+    P = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 20)
+    kv = _paged()                                   # 4 KV heads, 4 pages per sequence
+    view = binding.ViewC(1 << 20, 1 << 20, 4, 8)
+
+    def call(k_new=P, v_new=P, batch=1, hq=32, view_=view, opts=None, ws_bytes=1 << 30, kv_=kv):
+        return lib.se_quest_step(ctypes.byref(kv_), k_new, v_new, P, batch, hq, P, 0.1,
+                                 None if opts is None else ctypes.byref(opts), P, P,
+                                 ctypes.byref(view_), P, None, ws, ws_bytes, None)
+
+    assert call(v_new=None) == -1                   # k_new without v_new
+    assert call(hq=12) == -2                        # group size 3
+    assert call(kv_=_paged(head_dim=96)) == -2
+    assert call(batch=2) == -1                      # view unit count mismatch
+    assert call(view_=binding.ViewC(1 << 20, 1 << 20, 4, 2)) == -5   # view narrower than the table
+    big = binding.ViewC(1 << 20, 1 << 20, 1025 * 4, 8)
+    assert call(batch=1025, view_=big) == -2        # batch limit
+    O = binding.QuestStepOptsC
+    assert call(opts=O(0, 65, None, None, 0, 0, 0, 0)) == -1         # max_splits
+    assert call(opts=O(2, 0, None, None, 0, 0, 0, 0)) == -1          # out_dtype
+    assert call(opts=O(0, 0, None, None, -1, 0, 0, 0)) == -1         # tile_pages
+    assert call(opts=O(0, 0, None, None, 0, 0, 65, 0)) == -1         # lag_topk
+    assert call(ws_bytes=1024) == -3                # workspace too small
+    # no append (k_new and v_new both NULL) is accepted up to the workspace check
+    assert call(k_new=None, v_new=None, ws_bytes=1024) == -3
+    # zero batch: nothing to do
+    assert lib.se_quest_step(ctypes.byref(kv), None, None, None, 0, 32, None, 0.1, None, None,
+                             None, None, None, None, ws, 1 << 30, None) == 0
+
+
+def test_decode_view_chunk_limit(lib):
+    """The split-K plan's 32-bit products bound view->max_chunks at 2^20."""
+    args = [ctypes.c_void_p(1 << 20)] * 2
+    view = binding.ViewC(1 << 20, 1 << 20, 4, (1 << 20) + 1)
+    assert lib.se_sparse_decode(*args, 100, ctypes.byref(view), ctypes.c_void_p(1 << 20), 1, 32,
+                                4, 128, 0.1, None, ctypes.c_void_p(1 << 20), None,
+                                ctypes.c_void_p(1 << 20), 1 << 30, None) == -2
