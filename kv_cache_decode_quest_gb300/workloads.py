@@ -44,15 +44,16 @@ def paged_layout(seqs_k, seqs_v, lengths, block_table, num_pages, num_kv_heads, 
 class QuestRun:
     """Paged KV + Quest selection + split-K decode, one appended token per step.
 
-    mode: "step"     -- se_quest_step: append, select and decode in one kernel;
-          "fused"    -- se_quest_select_append, then se_sparse_decode;
+    mode: "fused"    -- se_quest_select_append, then se_sparse_decode (the
+                        faster path on the bench workloads, the default);
+          "step"     -- se_quest_step: append, select and decode in one kernel;
           "separate" -- se_kv_append, se_quest_select, se_sparse_decode.
     step_tuning: scheduling fields of se_quest_step_opts (mode "step")."""
 
     MODES = ("step", "fused", "separate")
 
     def __init__(self, w: synth.QuestWorkload, inputs: dict, out_dtype: int = 0,
-                 max_splits: int | None = None, device="cuda", mode: str = "step",
+                 max_splits: int | None = None, device="cuda", mode: str = "fused",
                  step_tuning: dict | None = None):
         if mode not in self.MODES:
             raise ValueError(f"mode {mode!r} not in {self.MODES}")
