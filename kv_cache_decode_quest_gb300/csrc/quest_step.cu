@@ -31,7 +31,7 @@
 // page summaries for a score tile, 2-D TMA boxes of K and V chunks for a decode
 // piece.  Warps 0-3 consume: stage s is handled by warp (stage sequence % 4).
 // Score tiles turn summaries into order-preserving keys in global memory; the
-// top-k runs on the four consumer warps (11-bit radix threshold, ballot emit)
+// top-k runs on the four consumer warps (10-bit radix threshold, ballot emit)
 // and writes the view and the new token's row; decode pieces run the mma.sync
 // decode of decode_core.cuh with its last-piece LSE merge.
 //
@@ -189,7 +189,7 @@ __device__ __forceinline__ int scan128(int v, int* tmp, int warp, int lane) {
 
 // Threshold of the top K of m order-preserving keys in shared memory, on the
 // 128 consumer threads: bits above the highest bit in which the largest and
-// smallest key differ are common to all keys, so the 11-bit radix digits start
+// smallest key differ are common to all keys, so the radix digits start
 // there (10-bit digits: the histogram stays small beside the stage ring), and
 // a pass ends the search when the boundary digit is kept whole.  On
 // return: keys above *T (under *mask) are kept, and so are the first *need keys
