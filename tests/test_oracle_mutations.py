@@ -121,3 +121,32 @@ def test_h2o_mutations_are_caught(monkeypatch):
     for bad in (evict_highest, no_update):
         monkeypatch.setattr(T_h2o, "h2o_step", bad)
         assert fails(T_h2o.test_hand_worked_step) or fails(T_h2o.test_mass_conservation_and_rules, 0)
+
+
+def _widen_sign_extended(bits):                # sign-extended to 64 bits, upper half of a double
+    u = np.asarray(bits, dtype=np.uint16).view(np.int16).astype(np.int64) << 48
+    return u.view(np.float64)
+
+
+def _widen_shift_15(bits):                     # one bit short of the upper half
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(15)
+    return u.view(np.float32).astype(np.float64)
+
+
+def _widen_as_float16(bits):                   # the 16 bits viewed as IEEE half
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def _widen_low_half(bits):                     # placed in the low half of binary32
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32)
+    return u.view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("bad", [_widen_sign_extended, _widen_shift_15, _widen_as_float16,
+                                 _widen_low_half])
+def test_widen_mutations_are_caught(monkeypatch, bad):
+    from tests import test_oracle_bf16 as T_bf16
+    monkeypatch.setattr(T_bf16, "widen", bad)
+    caught = any(fails(T_bf16.test_explicit_bit_patterns, b, v) for b, v in T_bf16.CASES) or \
+        fails(T_bf16.test_matches_torch_bfloat16_on_random_patterns)
+    assert caught
