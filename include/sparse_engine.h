@@ -22,7 +22,8 @@
  * Conventions shared by every entry point
  *   - Every pointer in a struct or argument is a DEVICE pointer unless marked
  *     "host".  The caller owns and allocates all memory; the library never
- *     allocates, never frees, and never synchronises the stream.
+ *     allocates, never frees, and never synchronises the stream (except
+ *     se_sync_status, whose purpose is to).
  *   - bf16 = IEEE bfloat16 bit patterns (uint16 in memory).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
  *     Calls are reentrant; the library's only global state is a per-device
@@ -156,27 +157,34 @@ typedef struct se_decode_opts {
                                  external event-record nodes of the graph) */
 } se_decode_opts;
 
-/* Options of se_quest_step (optional; NULL means all defaults).  The four
- * scheduling fields change only the speed, never the results beyond the
- * rounding order of split pieces; 0 picks the library's value. */
+/* Options of se_quest_step (optional; NULL means all defaults). */
 typedef struct se_quest_step_opts {
     int32_t out_dtype;        /* 0 = bf16 output (default), 1 = fp32 output */
     int32_t max_splits;       /* decode pieces per unit at most, 1..64 (0 = 64) */
     void* ev_kernel_begin;    /* NULL or a cudaEvent_t recorded right before / */
     void* ev_kernel_end;      /* right after the step kernel (timing only; captured
                                  as external event-record nodes in a graph) */
-    int32_t tile_pages;       /* candidate pages per score item (0: ~128 KB of summaries) */
-    int32_t piece_chunks;     /* 16-token chunks per decode item (0: 16) */
-    int32_t lag_topk;         /* queue rounds from a sequence's score items to its
-                                 top-k items, <= 64 (0: 8) */
-    int32_t lag_dec;          /* ... to its decode items, <= 2048, raised to lag_topk
-                                 (0: batch - 1, every decode item after every
-                                 score item) */
+    int32_t slice_pages;      /* candidate pages per scoring slice (0: about one
+                                 slice per resident block); speed only */
+    int32_t wait_limit_ns;    /* bound of each wait of one block on another
+                                 (0: 1 s); a wait that runs out sets
+                                 SE_DEV_TIMEOUT and the step's results, its
+                                 append included, are invalid */
 } se_quest_step_opts;
 
 /* ---- library ------------------------------------------------------------ */
 const char* se_status_str(int status);      /* static string, never NULL */
 int se_version(void);                       /* ABI version, currently 1 */
+
+/* Waits for every piece of work enqueued on `stream` and returns the SE_DEV_*
+ * bits of the device status word at byte 0 of workspace `ws` (0 when no
+ * kernel met inconsistent device data): the host-side reading of the status
+ * word that the conventions above describe.  It does not clear the word.
+ * Returns SE_ERR_INVALID_ARG for a NULL ws, SE_ERR_WORKSPACE for a ws that is
+ * not 256-byte aligned (neither launches nor waits), and SE_ERR_CUDA when the
+ * synchronisation or the 4-byte device-to-host copy fails (a failed kernel of
+ * the stream included).  This is the one entry point that synchronises. */
+int se_sync_status(const void* ws, se_stream_t stream);
 
 /* ---- workspace sizes (bytes, multiples of 256) --------------------------- */
 size_t se_small_workspace(void);            /* ops that need only the status word */
@@ -260,7 +268,8 @@ int se_view_from_segments(const se_varlen_kv* kv, int batch, const se_view* view
  * Workspace: se_sparse_decode_workspace(num_units, G, head_dim, max_splits),
  * zero-filled before its first use: it holds the arrival counters of split
  * units, which every call leaves at zero (clear it again after a call that set
- * a device error bit). */
+ * a device error bit).  The counters sit at a fixed offset whatever the shape,
+ * so one workspace serves calls of any shape whose size it covers. */
 int se_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,
                      const se_view* view, const void* q, int batch, int num_q_heads,
                      int num_kv_heads, int head_dim, float scale, const se_decode_opts* opts,
@@ -294,17 +303,23 @@ int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t tot
  *   q, budget_tokens, sel_pages, n_sel, view: as in se_quest_select;
  *   k_new, v_new: as in se_quest_select_append, or both NULL (no append);
  *   scale, out, lse: as in se_sparse_decode (out bf16 or fp32 by opts->out_dtype).
- * The kernel is a queue of work items taken in order by persistent blocks:
- * page-score tiles, per-(sequence, KV head) top-k, decode pieces; an item waits
- * only for items before it, so the waits cannot deadlock; each wait is bounded
- * (a wait that runs out sets SE_DEV_TIMEOUT and the results are invalid).  The
- * page scoring, the selection and the decode overlap across sequences, which the
- * separate calls cannot do.
- * Limits: batch <= 1024 and max_pages_per_seq <= 16384, else SE_ERR_UNSUPPORTED.
+ * The kernel is one cooperative launch (every block resident at once): each
+ * block scores a slice of one sequence's page summaries, then decodes a piece
+ * of one unit, whose top-k it computes itself once every page of that
+ * sequence is scored.  The waits of one block on the others are bounded
+ * (opts->wait_limit_ns): one that runs out sets SE_DEV_TIMEOUT, leaves ctx_len
+ * unchanged and the results invalid.  The last block to finish commits the new
+ * lengths and clears the workspace's control words.
+ * Limits: batch <= 1024, batch * num_kv_heads <= 4096, max_pages_per_seq <=
+ * 16384 (15296 with 16 query heads per KV head at head_dim 128), else
+ * SE_ERR_UNSUPPORTED.  A device that cannot hold the whole grid at once fails
+ * the launch (SE_ERR_CUDA).
  * Workspace: se_quest_step_workspace(batch, num_kv_heads, num_q_heads, head_dim,
- * max_pages_per_seq, max_splits), zero-filled before its first use: it holds the
- * queue counters, which every call leaves at zero (clear it again after a call
- * that set a device error bit). */
+ * max_pages_per_seq, max_splits), zero-filled before its first use: it holds
+ * control words (finished blocks, scored pages per sequence, split arrival
+ * counters), which every call leaves at zero, at fixed offsets whatever the
+ * shape, so one workspace serves calls of any shape whose size it covers.
+ * Clear it again after a call that set a device error bit. */
 int se_quest_step(const se_paged_kv* kv, const void* k_new, const void* v_new, const void* q,
                   int batch, int num_q_heads, const int32_t* budget_tokens, float scale,
                   const se_quest_step_opts* opts, int32_t* sel_pages, int32_t* n_sel,

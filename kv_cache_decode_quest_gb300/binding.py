@@ -57,8 +57,7 @@ class DecodeOptsC(ctypes.Structure):
 class QuestStepOptsC(ctypes.Structure):
     _fields_ = [("out_dtype", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("ev_kernel_begin", ctypes.c_void_p), ("ev_kernel_end", ctypes.c_void_p),
-                ("tile_pages", ctypes.c_int32), ("piece_chunks", ctypes.c_int32),
-                ("lag_topk", ctypes.c_int32), ("lag_dec", ctypes.c_int32)]
+                ("slice_pages", ctypes.c_int32), ("wait_limit_ns", ctypes.c_int32)]
 
 
 # C entry points: name -> (restype, argtypes)
@@ -66,6 +65,7 @@ _VP, _I, _SZ, _F, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.
 SIGNATURES = {
     "se_status_str": (ctypes.c_char_p, [_I]),
     "se_version": (_I, []),
+    "se_sync_status": (_I, [_VP, _VP]),
     "se_small_workspace": (_SZ, []),
     "se_quest_select_workspace": (_SZ, [_I, _I, _I]),
     "se_sparse_decode_workspace": (_SZ, [_I, _I, _I, _I]),
@@ -220,9 +220,18 @@ def workspace(nbytes: int, device="cuda") -> torch.Tensor:
     return torch.zeros(max(256, int(nbytes)), dtype=torch.uint8, device=device)
 
 
+def se_sync_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the SE_DEV_* bits of the workspace's
+    status word (raises on a negative status)."""
+    rc = load().se_sync_status(_p(ws), _stream(stream))
+    if rc < 0:
+        _check(rc, "se_sync_status")
+    return rc
+
+
 def status_word(ws: torch.Tensor) -> int:
-    """The device status word (synchronises through .item())."""
-    return int(ws[:4].view(torch.int32).item())
+    """The device status word of a workspace, read through se_sync_status."""
+    return se_sync_status(ws)
 
 
 # ---------------------------------------------------------------------------
@@ -290,15 +299,15 @@ def se_quest_select_append(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads
 
 def se_quest_step(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads: int, budget_tokens,
                   scale: float, sel_pages, n_sel, view: View, out, lse, ws, out_dtype: int = 0,
-                  max_splits: int = 64, tile_pages: int = 0, piece_chunks: int = 0,
-                  lag_topk: int = 0, lag_dec: int = 0, ev_begin=None, ev_end=None, stream=None):
+                  max_splits: int = 64, slice_pages: int = 0, wait_limit_ns: int = 0,
+                  ev_begin=None, ev_end=None, stream=None):
     """One Quest decode step (append when k_new/v_new are given, select, decode)
     in one kernel."""
     c, vc = kv.c, view.c
     opts = QuestStepOptsC(out_dtype, max_splits,
                           ev_begin.cuda_event if ev_begin is not None else None,
                           ev_end.cuda_event if ev_end is not None else None,
-                          tile_pages, piece_chunks, lag_topk, lag_dec)
+                          slice_pages, wait_limit_ns)
     _check(load().se_quest_step(ctypes.byref(c), _p(k_new), _p(v_new), _p(q), batch, num_q_heads,
                                 _p(budget_tokens), scale, ctypes.byref(opts), _p(sel_pages),
                                 _p(n_sel), ctypes.byref(vc), _p(out), _p(lse), _p(ws), ws.numel(),

@@ -112,6 +112,16 @@ const char* se_status_str(int status) {
 
 int se_version(void) { return 1; }
 
+int se_sync_status(const void* ws, se_stream_t stream) {
+    if (!ws) return SE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return SE_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SE_ERR_CUDA;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SE_ERR_CUDA;
+    return word & (SE_DEV_BAD_INDEX | SE_DEV_CAPACITY | SE_DEV_BAD_LENGTH | SE_DEV_TIMEOUT);
+}
+
 size_t se_small_workspace(void) { return 256; }
 
 size_t se_quest_select_workspace(int batch, int num_kv_heads, int max_pages_per_seq) {
@@ -224,32 +234,35 @@ int se_quest_step(const se_paged_kv* kv, const void* k_new, const void* v_new, c
     if (!aligned(q, 16) || !aligned(out, 16)) return SE_ERR_INVALID_ARG;
     if (view && view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
     if (view && view->max_chunks < kv->max_pages_per_seq) return SE_ERR_CAPACITY;
-    if (batch > 1024 || kv->max_pages_per_seq > 16384) return SE_ERR_UNSUPPORTED;
-    se_quest_step_opts o = {0, SE_MAX_SPLITS, nullptr, nullptr, 0, 0, 0, 0};
+    if (batch > kStepMaxBatch || batch * kv->num_kv_heads > kStepMaxUnits ||
+        kv->max_pages_per_seq > 16384)
+        return SE_ERR_UNSUPPORTED;
+    se_quest_step_opts o = {0, SE_MAX_SPLITS, nullptr, nullptr, 0, 0};
     if (opts) {
         o = *opts;
         if (o.max_splits == 0) o.max_splits = SE_MAX_SPLITS;
     }
     if (o.out_dtype != 0 && o.out_dtype != 1) return SE_ERR_INVALID_ARG;
     if (o.max_splits < 1 || o.max_splits > SE_MAX_SPLITS) return SE_ERR_INVALID_ARG;
-    if (o.tile_pages < 0 || o.piece_chunks < 0 || o.lag_topk < 0 || o.lag_dec < 0)
-        return SE_ERR_INVALID_ARG;
-    if (o.lag_topk > 64 || o.lag_dec > 2048) return SE_ERR_INVALID_ARG;
+    if (o.slice_pages < 0 || o.wait_limit_ns < 0) return SE_ERR_INVALID_ARG;
     const int G = num_q_heads / kv->num_kv_heads;
-    const int lag_dec = std::max(std::max(o.lag_topk, 8), o.lag_dec > 0 ? o.lag_dec : batch - 1);
-    if (quest_step_smem_bytes(batch, kv->num_kv_heads, kv->head_dim, G, kv->max_pages_per_seq,
-                              lag_dec) > 227 * 1024)
+    if (quest_step_smem_bytes(batch, kv->num_kv_heads, kv->head_dim, G) > 227 * 1024)
+        return SE_ERR_UNSUPPORTED;
+    // the top-k stages a unit's keys in the idle stage ring
+    if ((size_t)kv->max_pages_per_seq * 4 + 4352 > quest_step_ring_bytes(kv->head_dim, G))
         return SE_ERR_UNSUPPORTED;
     if ((rc = check_ws(ws, ws_bytes,
                        se_quest_step_workspace(batch, kv->num_kv_heads, num_q_heads, kv->head_dim,
                                                kv->max_pages_per_seq, o.max_splits))))
         return rc;
     if (batch == 0) return SE_OK;
-    const StepTuning tune = {o.tile_pages, o.piece_chunks, o.lag_topk, o.lag_dec};
+    const unsigned long long wait_ns =
+        o.wait_limit_ns > 0 ? (unsigned long long)o.wait_limit_ns : 1000000000ull;
     return cuda_status(launch_quest_step(
         *kv, k_new, v_new, q, batch, num_q_heads, budget_tokens, scale, o.out_dtype, o.max_splits,
-        tune, sel_pages, n_sel, *view, out, lse, ws, static_cast<cudaEvent_t>(o.ev_kernel_begin),
-        static_cast<cudaEvent_t>(o.ev_kernel_end), static_cast<cudaStream_t>(stream)));
+        o.slice_pages, wait_ns, sel_pages, n_sel, *view, out, lse, ws,
+        static_cast<cudaEvent_t>(o.ev_kernel_begin), static_cast<cudaEvent_t>(o.ev_kernel_end),
+        static_cast<cudaStream_t>(stream)));
 }
 
 int se_view_from_segments(const se_varlen_kv* kv, int batch, const se_view* view, void* ws,

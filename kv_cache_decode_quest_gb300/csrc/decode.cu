@@ -498,10 +498,22 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
+// Workspace layout.  The words every call must find at zero -- the split-K
+// arrival counters, one per unit -- come first, right after the 256-byte
+// header, in a block of at least kSelfPlanUnits words.  Their place does not
+// depend on the call's shape, so a workspace that served one call serves any
+// other whose size it covers: up to kSelfPlanUnits units the decode plans
+// for itself and relies on the counters being zero, and those words are
+// never anything but counters (every call leaves them at zero); above that
+// the plan kernel clears the counters it uses at the start of the call.
+size_t decode_ctl_bytes(int num_units) {
+    return 256 + align256((size_t)max(num_units, kSelfPlanUnits) * sizeof(int));
+}
+
 size_t decode_ws_bytes(int num_units, int G, int D, int max_splits) {
     const size_t items = (size_t)num_units * max_splits;
-    return 256 + align256(items * sizeof(int4)) + align256(items * sizeof(int)) +
-           align256((size_t)num_units * sizeof(int2)) + align256((size_t)num_units * sizeof(int)) +
+    return decode_ctl_bytes(num_units) + align256(items * sizeof(int4)) +
+           align256(items * sizeof(int)) + align256((size_t)num_units * sizeof(int2)) +
            align256((kMaxGrid + 1) * sizeof(int)) + align256(items * G * sizeof(float)) +
            align256(items * G * D * sizeof(float));
 }
@@ -512,15 +524,14 @@ DecodeWs decode_ws_carve(void* ws, int num_units, int G, int D, int max_splits) 
     DecodeWs w;
     w.status = reinterpret_cast<int*>(base);
     w.n_items = reinterpret_cast<int*>(base + 16);
-    size_t off = 256;
+    w.counters = reinterpret_cast<int*>(base + 256);
+    size_t off = decode_ctl_bytes(num_units);
     w.items = reinterpret_cast<int4*>(base + off);
     off += align256(items * sizeof(int4));
     w.gstart = reinterpret_cast<int*>(base + off);
     off += align256(items * sizeof(int));
     w.unit_items = reinterpret_cast<int2*>(base + off);
     off += align256((size_t)num_units * sizeof(int2));
-    w.counters = reinterpret_cast<int*>(base + off);
-    off += align256((size_t)num_units * sizeof(int));
     w.cta_first = reinterpret_cast<int*>(base + off);
     off += align256((kMaxGrid + 1) * sizeof(int));
     w.lse_part = reinterpret_cast<float*>(base + off);

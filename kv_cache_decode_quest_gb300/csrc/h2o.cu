@@ -186,15 +186,18 @@ size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
-// Workspace: header | logits [units][stride][G] | lse [B][Hq] | view chunk_row
-// [units][chunks] | view n_tokens [units] | decode workspace.
+// Workspace: the decode workspace first (its header, with the status word at
+// byte 0, and its arrival counters stay at fixed offsets whatever the shape),
+// then logits [units][stride][G] | lse [B][Hq] | view chunk_row [units][chunks]
+// | view n_tokens [units].
 size_t h2o_ws_bytes(int batch, int Hkv, int Hq, int D, int seg_cap) {
     const int units = batch * Hkv, G = Hq / Hkv;
     const int chunks = (seg_cap + kPage - 1) / kPage;
     const size_t stride = (size_t)chunks * kPage;
-    return 256 + al256((size_t)units * stride * G * sizeof(float)) +
+    return decode_ws_bytes(units, G, D, SE_MAX_SPLITS) +
+           al256((size_t)units * stride * G * sizeof(float)) +
            al256((size_t)batch * Hq * sizeof(float)) + al256((size_t)units * chunks * sizeof(int)) +
-           al256((size_t)units * sizeof(int)) + decode_ws_bytes(units, G, D, SE_MAX_SPLITS);
+           al256((size_t)units * sizeof(int));
 }
 
 cudaError_t launch_h2o_step(const se_h2o_state& st, const void* q, const void* k_new,
@@ -207,8 +210,9 @@ cudaError_t launch_h2o_step(const se_h2o_state& st, const void* q, const void* k
     const int chunks = (kv.seg_cap + kPage - 1) / kPage;
     const int stride = chunks * kPage;
     uint8_t* base = static_cast<uint8_t*>(ws);
-    int* status = reinterpret_cast<int*>(base);
-    size_t off = 256;
+    DecodeWs w = decode_ws_carve(base, units, G, D, SE_MAX_SPLITS);
+    int* status = w.status;
+    size_t off = decode_ws_bytes(units, G, D, SE_MAX_SPLITS);
     float* logits = reinterpret_cast<float*>(base + off);
     off += al256((size_t)units * stride * G * sizeof(float));
     float* lse_int = reinterpret_cast<float*>(base + off);
@@ -217,11 +221,8 @@ cudaError_t launch_h2o_step(const se_h2o_state& st, const void* q, const void* k
     view.chunk_row = reinterpret_cast<int32_t*>(base + off);
     off += al256((size_t)units * chunks * sizeof(int));
     view.n_tokens = reinterpret_cast<int32_t*>(base + off);
-    off += al256((size_t)units * sizeof(int));
     view.num_units = units;
     view.max_chunks = chunks;
-    DecodeWs w = decode_ws_carve(base + off, units, G, D, SE_MAX_SPLITS);
-    w.status = status;
 
     cudaError_t e = launch_varlen_append_view(kv, k_new, v_new, batch, view, status, s);
     if (e != cudaSuccess) return e;

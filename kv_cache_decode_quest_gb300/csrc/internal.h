@@ -58,17 +58,19 @@ cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch,
                                 void* ws, int* status, cudaStream_t s);
 
 // ---- quest_step.cu ----
-struct StepTuning {
-    int tile_pages, piece_chunks, lag_topk, lag_dec;   // 0 / negative: defaults
-};
+// se_quest_step's fixed control block holds the counters of at most this many
+// sequences and units.
+constexpr int kStepMaxBatch = 1024;
+constexpr int kStepMaxUnits = 4096;
 size_t quest_step_ws_bytes(int batch, int H, int G, int D, int max_pages, int max_splits);
-size_t quest_step_smem_bytes(int batch, int H, int D, int G, int max_pages, int lag_dec);
+size_t quest_step_smem_bytes(int batch, int H, int D, int G);
+size_t quest_step_ring_bytes(int D, int G);
 cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const void* v_new,
                               const void* q, int batch, int num_q_heads, const int32_t* budget,
-                              float scale, int out_dtype, int max_splits, const StepTuning& tune,
-                              int32_t* sel_pages, int32_t* n_sel, const se_view& view, void* out,
-                              float* lse, void* ws, cudaEvent_t ev_begin, cudaEvent_t ev_end,
-                              cudaStream_t s);
+                              float scale, int out_dtype, int max_splits, int item_pages,
+                              unsigned long long wait_ns, int32_t* sel_pages, int32_t* n_sel,
+                              const se_view& view, void* out, float* lse, void* ws,
+                              cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t s);
 
 // ---- decode.cu ----
 struct DecodeWs {
@@ -78,10 +80,14 @@ struct DecodeWs {
     int* gstart;          // [num_units * max_splits]: global first chunk of each item
     int* cta_first;       // [grid + 1]: first item of each decode CTA
     int2* unit_items;     // [num_units]: (first item, item count)
-    int* counters;        // [num_units]: pieces finished (zeroed by the plan kernel)
+    int* counters;        // [num_units]: pieces finished; at a fixed offset (256), left at
+                          // zero by every call (the plan kernel also clears them)
     float* lse_part;      // [num_units * max_splits][G]   (log2 domain)
     float* o_part;        // [num_units * max_splits][G][D] (normalised)
 };
+// Bytes of the workspace head that must be zero before a call: the status
+// header and the arrival counters (fixed offset, independent of G, D and splits).
+size_t decode_ctl_bytes(int num_units);
 size_t decode_ws_bytes(int num_units, int G, int D, int max_splits);
 DecodeWs decode_ws_carve(void* ws, int num_units, int G, int D, int max_splits);
 cudaError_t launch_sparse_decode(const void* k_rows, const void* v_rows, int64_t total_rows,

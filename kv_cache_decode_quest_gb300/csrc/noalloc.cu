@@ -79,8 +79,11 @@ int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t tot
     int rc = scratch_address(&scratch);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the header (status word, piece count) must start at zero for every call
-    if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return SE_ERR_CUDA;
+    // every word that must start at zero -- the status header and the split-K
+    // arrival counters, which sit at a fixed place right after it -- is
+    // cleared by each call, whatever the previous call's shape or outcome
+    if (cudaMemsetAsync(scratch, 0, se::decode_ctl_bytes(units), s) != cudaSuccess)
+        return SE_ERR_CUDA;
     se::DecodeWs w = se::decode_ws_carve(scratch, units, G, head_dim, max_splits);
     if (status_out) w.status = status_out;
     const cudaError_t e = se::launch_sparse_decode(

@@ -1,4 +1,4 @@
-// One Quest decode step in one persistent kernel: the new token's append, the
+// One Quest decode step in one cooperative kernel: the new token's append, the
 // page scoring, the per-KV-head top-k and the split-K decode over the selected
 // pages.  Same results as se_quest_select_append followed by se_sparse_decode.
 //
@@ -8,36 +8,32 @@
 // rows the view exposes ("SparseEngine：稀疏优先推理引擎", section "方法 / 关键模块").
 //
 // Why one kernel: the step is two HBM streams (the page summaries, then the
-// selected K/V rows) separated by a short, latency-bound top-k per unit.  As
-// separate launches the two streams never overlap and every top-k sits on the
-// critical path.  Here the step is a queue of work items taken in order from
-// one global counter by persistent CTAs:
-//   score tile (sequence b, a range of its candidate pages, all KV heads)
-//   top-k      (unit u = (b, h)): waits until every score tile of b is done
-//   decode     (a piece of unit u): waits until the top-k of u is done
-// The queue is laid out in rounds r = 0, 1, ...: the score tiles of sequence r,
-// then the top-k items of sequence r - lag_topk, then the decode pieces of
-// sequence r - lag_dec (lag_dec >= lag_topk >= 0), so every item depends only on
-// items before it.  A CTA takes items in increasing order and a taken item is
-// held by a running CTA, so the earliest unfinished item always has its inputs
-// and can finish: the waits cannot deadlock, whatever the grid or residency.
-// Every wait is bounded (1 s, or at once when another CTA has given up); a CTA
-// that gives up records SE_DEV_TIMEOUT and raises a global abort word that the
-// others poll.
+// selected K/V rows) joined by a short, latency-bound top-k per unit.  As
+// separate launches every kernel boundary, the top-k kernel and the decode's
+// planning sit on the critical path.  Here every CTA of one resident wave
+// (a cooperative launch, so every CTA is running) follows the same static
+// schedule, computed by each CTA from the sequence lengths and budgets:
+//   1. score: one contiguous slice of one sequence's candidate page summaries
+//      (all KV heads of each page), streamed with 1-D bulk copies through the
+//      stage ring and turned into order-preserving keys in the workspace; the
+//      slice's page count is then added to the sequence's scored counter;
+//   2. decode piece(s): a range of chunks of one unit u = (b, h).  The piece
+//      waits (bounded) until every candidate page of b is scored, runs the
+//      exact top-k of u itself from the keys in L2 (every piece of u computes
+//      the same selection; none waits on another's), writes its ranks of the
+//      selection and of the view, and streams its chunks' K/V with 2-D TMA into
+//      the same ring for the mma.sync decode of decode_core.cuh; split units are
+//      merged by the last piece to finish.
+// The new token's row is written by the piece that holds the unit's last
+// chunk (the forced last page), before its own copy of that chunk.  The last
+// CTA to finish commits ctx_len + 1 of every sequence whose token was
+// appended (every CTA has read the old lengths by then) and clears the
+// control words.  Waits are bounded: a CTA that gives up records
+// SE_DEV_TIMEOUT and raises a global abort word that the other waits poll;
+// every CTA still walks the same barriers to the end.
 //
-// CTA layout (160 threads): warp 4 is the producer; it takes the items, publishes
-// each one to the consumers through a 4-slot descriptor ring (mbarriers), and
-// streams the item's data into one shared-memory stage ring: 1-D bulk copies of
-// page summaries for a score tile, 2-D TMA boxes of K and V chunks for a decode
-// piece.  Warps 0-3 consume: stage s is handled by warp (stage sequence % 4).
-// Score tiles turn summaries into order-preserving keys in global memory; the
-// top-k runs on the four consumer warps (10-bit radix threshold, ballot emit)
-// and writes the view and the new token's row; decode pieces run the mma.sync
-// decode of decode_core.cuh with its last-piece LSE merge.
-//
-// The last CTA to finish resets the queue counters and commits ctx_len + 1 of
-// every sequence whose token was appended, after every CTA has read the old
-// lengths.
+// CTA layout (160 threads): warps 0-3 consume (stage s is handled by warp
+// (stage sequence % 4), in both phases), warp 4 is the producer.
 #include <algorithm>
 
 #include "append.cuh"
@@ -48,22 +44,16 @@
 namespace se {
 namespace {
 
-constexpr int kItemSlots = 4;
-constexpr int kDigit = 10, kStepBins = 1 << kDigit;   // 10-bit radix digits: 8 bins per consumer thread
-constexpr int kCThreads = kConsumerWarps * 32;
-
-enum : int { kItemScore = 0, kItemTopk = 1, kItemDecode = 2, kItemEnd = 3, kItemFold = 4 };
-
-// score: a0..a1 = candidate pages; decode: a0..a1 = chunks, a2 = partial slot
-// (-1: the piece is the whole unit), a3 = the unit's first slot, a4 = its pieces
-struct StepItem {
-    int type, b, h, a0, a1, a2, a3, a4;
-};
+constexpr int kCThreads = kConsumerWarps * 32;         // 128 consumer threads
+constexpr int kDigit = 10, kStepBins = 1 << kDigit;     // 10-bit radix digits: 8 bins per thread
+constexpr int kMaxPieces = 32;                          // decode pieces per CTA at most
+constexpr int kMaxScoreItems = 8;                       // score slices per CTA at most
+constexpr int kMinItemPages = 8;
 
 struct StepParams {
     se_paged_kv kv;
     const uint16_t* q;
-    int Hq, G, batch;
+    int Hq, G, batch, units;
     const int32_t* budget;
     const uint4* k_new;                 // null: no append
     const uint4* v_new;
@@ -75,31 +65,32 @@ struct StepParams {
     int out_f32;
     float* lse_out;
     uint32_t* keys;                     // [units][max_pages_per_seq]
-    float* coef;                        // [batch][H][2][D]: Q- then Q+ per KV head
-    int* sync;                          // [0] item counter, [1] CTAs finished, [2] abort
-    int* seq_folded;                    // [batch] coefficients written
-    int* seq_scored;                    // [batch] score tiles finished
-    int* unit_ready;                    // [units] top-k done
+    int* seq_scored;                    // [batch] candidate pages scored
     int* counters;                      // [units] decode pieces finished
+    int* sync;                          // [0] CTAs finished, [1] abort
     float* o_part;                      // [units * max_splits][G][D]
     float* lse_part;                    // [units * max_splits][G]
-    int tile_pages, piece_chunks, max_splits, lag_topk, lag_dec, rounds;
+    int max_splits, item_pages;         // item_pages 0: about one slice per CTA
+    int off_union;                      // union area offset in dynamic shared memory
+    int ring_bytes;
     int64_t total_rows;
-    // dynamic shared memory offsets (bytes from the 1024-aligned base)
-    int off_coef, off_union, off_sinfo, off_rstart;
+    unsigned long long wait_ns;
     int* status;
 };
 
-template <int D>
+template <int D, int NT>
 struct StepShape {
-    static constexpr int kStageBytes = DecShape<D, 1>::kStageBytes;   // 8 KB at D = 128
-    static constexpr int kStages = D == 64 ? 24 : 12;                  // 96 KB ring
+    using S = DecShape<D, NT>;
+    static constexpr int kStageBytes = S::kStageBytes;                 // 8 KB at D = 128
+    static constexpr int kStages = D == 64 ? 24 : (NT == 1 ? 12 : 8);  // as the decode kernel
     static constexpr int kSumBytes = 2 * D * 2;                        // one (page, head) summary
     static constexpr int kSumsPerStage = kStageBytes / kSumBytes;      // 16
     static_assert(kStages % kConsumerWarps == 0, "stage ownership needs kStages % 4 == 0");
-    // ring, full/empty, item full/empty, stage counts, items, misc ints
-    static constexpr int kFixed = kStages * kStageBytes + kStages * 16 + kItemSlots * 16 +
-                                  kStages * 4 + kItemSlots * (int)sizeof(StepItem) + 64;
+    // small areas after the ring: full/empty barriers, stage token counts,
+    // misc ints, the CTA's pieces (item, unit range, sequence values) and
+    // score slices
+    static constexpr int kFixed = kStages * 16 + kStages * 4 + 64 * 4 + kMaxPieces * 48 +
+                                  kMaxScoreItems * 16;
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -107,67 +98,56 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void st_release(int* p, int v) {
-    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_release_add(int* p, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-
-// Bounded wait for *flag >= target (acquire).  False on timeout, on this CTA's
-// abort, or when another CTA raised the global abort word.
-__device__ bool wait_geq(const int* flagp, int target, volatile int* abort_flag, const int* gabort) {
-    if (ld_acquire(flagp) >= target) return true;
-    const unsigned long long t0 = globaltimer();
-    while (true) {
-        __nanosleep(100);
-        if (ld_acquire(flagp) >= target) return true;
-        if (*abort_flag || *reinterpret_cast<const volatile int*>(gabort)) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
-    }
+__device__ __forceinline__ void producer_bar() {
+    asm volatile("bar.sync 3, %0;" ::"r"(kDecodeThreads) : "memory");
 }
 
-// This CTA gives up: results are invalid, the kernel drains and ends.
+// This CTA gives up: results are invalid; the kernel walks on to its end.
 __device__ __forceinline__ void give_up(const StepParams& p, volatile int* abort_flag) {
     *abort_flag = 1;
     flag(p.status, SE_DEV_TIMEOUT);
-    atomicExch(p.sync + 2, 1);
+    atomicExch(p.sync + 1, 1);
 }
 
-// Per-sequence plan values, the same in every CTA: held = clamped ctx_len,
-// ctx = held + 1 when the new token fits, n pages, k pages of budget.
-struct SeqPlan {
-    int held, ctx, n, k;
-    int tiles, chunks, tokens, pieces;
-};
-__device__ SeqPlan seq_plan(const StepParams& p, int b, bool report) {
-    SeqPlan s;
-    const int cap = p.kv.max_pages_per_seq * kPage;
-    int held = p.kv.ctx_len[b];
-    if (held < 0 || held > cap) {
-        if (report) flag(p.status, SE_DEV_BAD_LENGTH);
-        held = held < 0 ? 0 : cap;
+// Bounded wait (one thread) for *ctr >= target (acquire).  False on timeout,
+// on this CTA's abort, or when another CTA raised the global abort word.
+__device__ bool wait_count(const StepParams& p, const int* ctr, int target,
+                           volatile int* abort_flag) {
+    if (ld_acquire(ctr) >= target) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (ld_acquire(ctr) >= target) return true;
+        if (*abort_flag || *reinterpret_cast<const volatile int*>(p.sync + 1)) return false;
+        if (globaltimer() - t0 > p.wait_ns) return false;
+        __nanosleep(64);
     }
-    const bool pending = p.k_new != nullptr;
-    if (pending && held >= cap && report) flag(p.status, SE_DEV_CAPACITY);
-    s.held = held;
-    s.ctx = (pending && held < cap) ? held + 1 : held;
+}
+
+// A sequence's step values, the same in every CTA: held = clamped ctx_len, the
+// token appended when it fits, n pages, k pages of budget, m candidate pages
+// to score (0 when every page is selected), the unit's chunks and tokens.
+struct SeqVals {
+    int held, ctx, n, k, m, chunks, tokens, room;
+};
+__device__ __forceinline__ SeqVals seq_vals(int held_raw, int bud, int cap, bool pending) {
+    SeqVals s;
+    s.held = held_raw < 0 ? 0 : (held_raw > cap ? cap : held_raw);
+    s.room = pending && s.held < cap;
+    s.ctx = s.room ? s.held + 1 : s.held;
     s.n = (s.ctx + kPage - 1) / kPage;
-    const int bud = p.budget[b];
     s.k = max(1, (bud < 0 ? 0 : bud) / kPage);
-    if (s.n <= s.k) {
-        s.tiles = 0;
-        s.chunks = s.n;
-        s.tokens = s.ctx;
-    } else {
-        s.tiles = (s.n - 1 + p.tile_pages - 1) / p.tile_pages;
+    if (s.n > s.k) {
+        s.m = s.n - 1;
         s.chunks = s.k;
         s.tokens = kPage * (s.k - 1) + (s.ctx - kPage * (s.n - 1));
+    } else {
+        s.m = 0;
+        s.chunks = s.n;
+        s.tokens = s.ctx;
     }
-    s.pieces = max(1, min(p.max_splits, (s.chunks + p.piece_chunks - 1) / p.piece_chunks));
     return s;
 }
 
@@ -189,9 +169,8 @@ __device__ __forceinline__ int scan128(int v, int* tmp, int warp, int lane) {
 
 // Threshold of the top K of m order-preserving keys in shared memory, on the
 // 128 consumer threads: bits above the highest bit in which the largest and
-// smallest key differ are common to all keys, so the radix digits start
-// there (10-bit digits: the histogram stays small beside the stage ring), and
-// a pass ends the search when the boundary digit is kept whole.  On
+// smallest key differ are common to all keys, so the radix digits start there,
+// and a pass ends the search when the boundary digit is kept whole.  On
 // return: keys above *T (under *mask) are kept, and so are the first *need keys
 // equal to *T.
 __device__ void step_threshold(const uint32_t* sk, int m, int K, int* hist, int* tmp,
@@ -268,36 +247,33 @@ __device__ void step_threshold(const uint32_t* sk, int m, int K, int* hist, int*
     *need = remaining;
 }
 
-// Top-k item of unit u = (b, h) on the consumer warps: exact top-(k-1) of the
-// candidate pages 0..n-2 by (score desc, page asc), emitted in page order, plus
-// the last page (always selected, never scored); the view chunk of a selected
-// page is its physical page of this KV head.  With the append, head h's new
-// row goes in first (its loads are issued before the selection, its stores
-// after it).  `area`: the union area of shared memory.
-__device__ void step_topk(const StepParams& p, int b, int h, const SeqPlan& s, uint8_t* area,
-                          int warp, int lane) {
+// The selection of unit u = (b, h) restricted to ranks [c0, c1): exact top-(k-1)
+// of the candidate pages 0..n-2 by (score desc, page asc) in ascending page
+// order, then the last page (always selected, never scored) at rank k-1; all
+// pages when n <= k.  Writes sel_pages[u][rank] for the ranks of the range.
+// The keys were written by the scoring slices of other CTAs (read through
+// L2); `area` is the idle stage ring (hist, small ints, keys).
+__device__ void piece_select(const StepParams& p, int u, const SeqVals& s, int c0, int c1,
+                             uint8_t* area, int warp, int lane) {
     const int ctid = warp * 32 + lane;
-    const se_paged_kv& kv = p.kv;
-    const int H = kv.num_kv_heads, stride = kv.max_pages_per_seq;
-    const int u = b * H + h;
-    int* hist = reinterpret_cast<int*>(area);                    // [2048]
+    const int stride = p.kv.max_pages_per_seq;
+    int32_t* selp = p.sel_pages + (int64_t)u * stride;
+    if (s.m == 0) {
+        for (int c = c0 + ctid; c < c1; c += kCThreads) selp[c] = c;
+        return;
+    }
+    int* hist = reinterpret_cast<int*>(area);                    // [1024]
     int* small = hist + kStepBins;                               // 64 ints
     int* tmp = small;                                            // [4]
     uint32_t* red = reinterpret_cast<uint32_t*>(small + 4);      // [8]
     int* sel = small + 12;                                       // [4]
     int* wgt = small + 16;                                       // [4]
     int* weq = small + 20;                                       // [4]
-    uint32_t* skeys = reinterpret_cast<uint32_t*>(small + 64);   // [stride]
-    const bool room = p.k_new != nullptr && s.ctx == s.held + 1;
-    const int segs = kv.head_dim / 8;
-    AppendRegs ar;
-    if (room && ctid < segs) append_load(kv, b, h, s.held, p.k_new, p.v_new, ctid, ar);
-    const int32_t* btr = kv.block_table + (int64_t)b * stride;
-    int phys_new = -1;
-    if (room) phys_new = btr[s.held / kPage];
-    const int n = s.n, k = s.k, m = n - 1;
-    if (n > k) {
-        // stage the candidate keys (written by other CTAs: read through L2)
+    uint32_t* skeys = reinterpret_cast<uint32_t*>(small + 64);   // [m]
+    const int m = s.m, K = s.k - 1;
+    if (c1 == s.k && ctid == 0) selp[K] = s.n - 1;
+    if (K == 0 || c0 >= K) return;                                // only the last page here
+    {
         const uint32_t* keys = p.keys + (int64_t)u * stride;
         constexpr int kU = 8;
         for (int base = ctid; base < m; base += kCThreads * kU) {
@@ -315,179 +291,262 @@ __device__ void step_topk(const StepParams& p, int b, int h, const SeqPlan& s, u
         }
         consumer_bar();
     }
-    int32_t* selp = p.sel_pages + (int64_t)u * stride;
-    int32_t* crow = p.view.chunk_row + (int64_t)u * p.view.max_chunks;
-    // the view chunk of selected page `page`: its physical page of head h
-    auto chunk_of = [&](int page) {
-        const int phys = btr[page];
-        if (phys >= 0 && phys < kv.num_pages) return (phys * H + h) * kPage;
-        flag(p.status, SE_DEV_BAD_INDEX);
-        return -1;
-    };
-    if (n <= k) {
-        for (int c = ctid; c < n; c += kCThreads) {
-            selp[c] = c;
-            crow[c] = chunk_of(c);
-        }
-        if (ctid == 0) {
-            p.n_sel[u] = n;
-            p.view.n_tokens[u] = s.tokens;
-        }
-    } else {
-        const int K = k - 1;
-        if (K > 0) {
-            int need_eq = 0;
-            uint32_t T = 0, msk = 0;
-            step_threshold(skeys, m, K, hist, tmp, red, sel, &T, &msk, &need_eq, warp, lane);
-            // pages in ascending order: warp w owns a contiguous range read with
-            // a lane stride; ballots rank the kept pages inside the warp and a
-            // scan over the four warps places each warp's run
-            const int chunk = ((m + kConsumerWarps - 1) / kConsumerWarps + 31) & ~31;
-            const int c0 = min(m, warp * chunk), c1 = min(m, c0 + chunk);
-            int gt = 0, eq = 0;
-            for (int i = c0 + lane; i < c1; i += 32) {
-                const uint32_t kk = skeys[i] & msk;
-                gt += kk > T;
-                eq += kk == T;
-            }
-            gt = __reduce_add_sync(0xffffffffu, gt);
-            eq = __reduce_add_sync(0xffffffffu, eq);
-            if (lane == 0) {
-                wgt[warp] = gt;
-                weq[warp] = eq;
-            }
-            consumer_bar();
-            int eq_seen = 0, out = 0;
-            for (int w = 0; w < warp; ++w) {
-                const int take_w = max(0, min(weq[w], need_eq - eq_seen));
-                out += wgt[w] + take_w;
-                eq_seen += weq[w];
-            }
-            const uint32_t lt = (1u << lane) - 1u;
-            for (int i0 = c0; i0 < c1; i0 += 32) {
-                const int i = i0 + lane;
-                const uint32_t kk = i < c1 ? skeys[i] & msk : 0u;
-                const bool is_eq = i < c1 && kk == T;
-                const uint32_t meq = __ballot_sync(0xffffffffu, is_eq);
-                const bool take =
-                    (i < c1 && kk > T) || (is_eq && eq_seen + __popc(meq & lt) < need_eq);
-                const uint32_t mt = __ballot_sync(0xffffffffu, take);
-                if (take) selp[out + __popc(mt & lt)] = i;
-                out += __popc(mt);
-                eq_seen += __popc(meq);
-            }
-        }
-        if (ctid == 0) {
-            selp[K] = n - 1;
-            p.n_sel[u] = k;
-            p.view.n_tokens[u] = s.tokens;
-        }
-        // then the view rows, every block-table lookup in flight together (a
-        // lookup inside the ranking loop above would serialise them)
-        consumer_bar();
-        for (int c = ctid; c < k; c += kCThreads) crow[c] = chunk_of(__ldcg(selp + c));
+    int need_eq = 0;
+    uint32_t T = 0, msk = 0;
+    step_threshold(skeys, m, K, hist, tmp, red, sel, &T, &msk, &need_eq, warp, lane);
+    // pages in ascending order: warp w owns a contiguous range read with a lane
+    // stride; ballots rank the kept pages inside the warp and the counts of the
+    // warps before it place its run
+    const int chunk = ((m + kConsumerWarps - 1) / kConsumerWarps + 31) & ~31;
+    const int r0 = min(m, warp * chunk), r1 = min(m, r0 + chunk);
+    int gt = 0, eq = 0;
+    for (int i = r0 + lane; i < r1; i += 32) {
+        const uint32_t kk = skeys[i] & msk;
+        gt += kk > T;
+        eq += kk == T;
     }
-    if (room && ctid < segs) {
-        if (phys_new >= 0 && phys_new < kv.num_pages) {
-            append_store(kv, b, h, s.held, phys_new, ctid, ar);
-            fence_proxy_async_global();     // the row is read next by TMA (async proxy)
-        } else if (ctid == 0) {
-            flag(p.status, SE_DEV_BAD_INDEX);
-        }
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
+    if (lane == 0) {
+        wgt[warp] = gt;
+        weq[warp] = eq;
+    }
+    consumer_bar();
+    int eq_seen = 0, out = 0;
+    for (int w = 0; w < warp; ++w) {
+        const int take_w = max(0, min(weq[w], need_eq - eq_seen));
+        out += wgt[w] + take_w;
+        eq_seen += weq[w];
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int i0 = r0; i0 < r1 && out < c1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t kk = i < r1 ? skeys[i] & msk : 0u;
+        const bool is_eq = i < r1 && kk == T;
+        const uint32_t meq = __ballot_sync(0xffffffffu, is_eq);
+        const bool take = (i < r1 && kk > T) || (is_eq && eq_seen + __popc(meq & lt) < need_eq);
+        const uint32_t mt = __ballot_sync(0xffffffffu, take);
+        const int rank = out + __popc(mt & lt);
+        if (take && rank >= c0 && rank < c1) selp[rank] = i;
+        out += __popc(mt);
+        eq_seen += __popc(meq);
     }
 }
 
-// Q- / Q+ of sequence b per (KV head, d) for the page bound, on the consumer
-// warps, into coef (global memory): U[p] = sum_d Q-[d] kmin[p,d] + Q+[d] kmax[p,d] with Q+ = sum_g max(q_g, 0)
-// and Q- = sum_g min(q_g, 0) (kmin <= kmax picks the larger product per sign).
-// coef[h][0][d] = Q-, coef[h][1][d] = Q+.  Group sums are xor-shuffles across
-// the lanes of one d-block (G is a power of two).
+// Q- / Q+ of sequence b per (KV head, d) for the page bound, into coef (shared
+// memory): U[p] = sum_d Q-[d] kmin[p,d] + Q+[d] kmax[p,d] with Q+ = sum_g
+// max(q_g, 0) and Q- = sum_g min(q_g, 0) (kmin <= kmax picks the larger
+// product per sign).  coef[h][0][d] = Q-, coef[h][1][d] = Q+.  One (head,
+// 8-channel block) per consumer thread, its group's loads in flight together.
 template <int D>
-__device__ __forceinline__ void step_fold(const StepParams& p, int b, float* coef, int warp,
-                                          int lane) {
+__device__ __forceinline__ void step_fold(const StepParams& p, int b, float* coef, int ctid) {
     const int H = p.kv.num_kv_heads, G = p.G;
-    const int kNdv = 32 / G;                              // d-blocks of 8 per warp task
-    const int tph = (D / 8 + kNdv - 1) / kNdv;            // warp tasks per head
-    const int g = lane / kNdv, dv = lane % kNdv;
-    constexpr int kPre = 4;
-    uint4 qv[kPre];
-#pragma unroll
-    for (int i = 0; i < kPre; ++i) {
-        const int task = warp + i * kConsumerWarps;
-        const int hh = task / tph, d8 = (task % tph) * kNdv + dv;
-        qv[i] = (task < H * tph && d8 < D / 8)
-                    ? *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.Hq + hh * G + g) * D + d8 * 8)
-                    : make_uint4(0, 0, 0, 0);
-    }
-    int i = 0;
-    for (int task = warp; task < H * tph; task += kConsumerWarps, ++i) {
-        const int hh = task / tph, d8 = (task % tph) * kNdv + dv;
-        uint4 v = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int j = 0; j < kPre; ++j)
-            if (i == j) v = qv[j];
-        if (i >= kPre && d8 < D / 8)
-            v = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.Hq + hh * G + g) * D + d8 * 8);
-        const uint32_t a4[4] = {v.x, v.y, v.z, v.w};
+    for (int task = ctid; task < H * (D / 8); task += kCThreads) {
+        const int h = task / (D / 8), d8 = task % (D / 8);
+        const uint16_t* qb = p.q + ((int64_t)b * p.Hq + h * G) * D + d8 * 8;
         float lo[8], hi[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float f0 = bf_lo(a4[e]), f1 = bf_hi(a4[e]);
-            lo[2 * e] = fminf(f0, 0.f);
-            lo[2 * e + 1] = fminf(f1, 0.f);
-            hi[2 * e] = fmaxf(f0, 0.f);
-            hi[2 * e + 1] = fmaxf(f1, 0.f);
-        }
-        for (int o = kNdv; o < 32; o <<= 1) {
+        for (int e = 0; e < 8; ++e) lo[e] = hi[e] = 0.f;
+#pragma unroll 4
+        for (int g = 0; g < G; ++g) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qb + (int64_t)g * D);
+            const uint32_t a4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                lo[e] += __shfl_xor_sync(0xffffffffu, lo[e], o);
-                hi[e] += __shfl_xor_sync(0xffffffffu, hi[e], o);
+            for (int e = 0; e < 4; ++e) {
+                const float f0 = bf_lo(a4[e]), f1 = bf_hi(a4[e]);
+                lo[2 * e] += fminf(f0, 0.f);
+                lo[2 * e + 1] += fminf(f1, 0.f);
+                hi[2 * e] += fmaxf(f0, 0.f);
+                hi[2 * e + 1] += fmaxf(f1, 0.f);
             }
         }
-        if (g == 0 && d8 < D / 8) {
-            float4* cl = reinterpret_cast<float4*>(coef + (hh * 2) * D + d8 * 8);
-            float4* ch = reinterpret_cast<float4*>(coef + (hh * 2 + 1) * D + d8 * 8);
-            cl[0] = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            cl[1] = make_float4(lo[4], lo[5], lo[6], lo[7]);
-            ch[0] = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            ch[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
+        float4* cl = reinterpret_cast<float4*>(coef + (h * 2) * D + d8 * 8);
+        float4* ch = reinterpret_cast<float4*>(coef + (h * 2 + 1) * D + d8 * 8);
+        cl[0] = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        cl[1] = make_float4(lo[4], lo[5], lo[6], lo[7]);
+        ch[0] = make_float4(hi[0], hi[1], hi[2], hi[3]);
+        ch[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
+    }
+}
+
+// One consumer warp scores one stage of `nsum` summaries (all KV heads of a
+// page together; summary t of the slice is page p0 + t / H, head t % H): each
+// summary is read by kLps lanes, 4 16-byte vectors each (vector j of lane
+// `sub` is vector j*kLps + sub of the summary: conflict-free shared-memory
+// reads), and becomes the key of its (unit, page).
+template <int D>
+__device__ __forceinline__ void score_stage(const StepParams& p, const uint8_t* st, int nsum,
+                                            int t0, int b, int p0, const float* coef, int lane) {
+    constexpr int kU4 = D / 4;                            // 16-byte vectors per summary
+    constexpr int kLps = kU4 / 4;                         // lanes per summary
+    constexpr int kR = 32 / kLps;                         // summaries per warp-wide read
+    constexpr int kSum = 2 * D * 2;
+    const int H = p.kv.num_kv_heads, stride = p.kv.max_pages_per_seq;
+    const int sub = lane % kLps, slot = lane / kLps;
+    for (int r = 0; r < nsum; r += kR) {
+        const int tl = r + slot;
+        const int t = t0 + tl;
+        const int h = t % H, pl = t / H;
+        float acc = 0.f;
+        if (tl < nsum) {
+            const uint4* sv = reinterpret_cast<const uint4*>(st + tl * kSum);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 w = sv[j * kLps + sub];
+                const float4* cf =
+                    reinterpret_cast<const float4*>(coef + h * 2 * D + (j * kLps + sub) * 8);
+                const float4 c0 = cf[0], c1 = cf[1];
+                acc = fmaf(c0.x, bf_lo(w.x), acc);
+                acc = fmaf(c0.y, bf_hi(w.x), acc);
+                acc = fmaf(c0.z, bf_lo(w.y), acc);
+                acc = fmaf(c0.w, bf_hi(w.y), acc);
+                acc = fmaf(c1.x, bf_lo(w.z), acc);
+                acc = fmaf(c1.y, bf_hi(w.z), acc);
+                acc = fmaf(c1.z, bf_lo(w.w), acc);
+                acc = fmaf(c1.w, bf_hi(w.w), acc);
+            }
         }
+#pragma unroll
+        for (int o = kLps / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (sub == 0 && tl < nsum)
+            p.keys[((int64_t)b * H + h) * stride + p0 + pl] = float_key(acc);
     }
 }
 
-// The consumers' wait for the next item descriptor is longer than any producer
-// wait, so that a producer which gives up always publishes the end item first:
-// every consumer warp then reads the same descriptors and reaches the same
-// named barriers.
-constexpr unsigned long long kItemWaitLimitNs = 4ull * kWaitLimitNs;
-
-__device__ bool item_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kItemWaitLimitNs) return false;
+// Plans, the same in every CTA, computed by one consumer warp each.
+//
+// Score slices: every sequence's candidate pages are cut into slices of P
+// pages (the last one shorter), P = the option, else about the candidates over
+// the grid, raised until the slices fit kMaxScoreItems rounds of the grid;
+// slice t (in sequence order) is run by CTA t % grid.  Writes this CTA's
+// slices (b, first page, end page) and returns their count.
+__device__ int plan_score(const StepParams& p, const int2* sseq, int lane, int4* items) {
+    const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int cap = p.kv.max_pages_per_seq * kPage;
+    const bool pending = p.k_new != nullptr;
+    auto m_of = [&](int b) {
+        const int2 x = sseq[b];
+        return seq_vals(x.x, x.y, cap, pending).m;
+    };
+    long long M = 0;
+#pragma unroll 1
+    for (int base = 0; base < p.batch; base += 32)
+        M += __reduce_add_sync(0xffffffffu, base + lane < p.batch ? m_of(base + lane) : 0);
+    if (M == 0) return 0;
+    int P = p.item_pages > 0 ? p.item_pages
+                             : max(kMinItemPages, (int)((M + grid - 1) / grid));
+    int total = 0;
+#pragma unroll 1
+    for (int iter = 0; iter < 16; ++iter) {
+        total = 0;
+#pragma unroll 1
+        for (int base = 0; base < p.batch; base += 32) {
+            const int b = base + lane;
+            const int m = b < p.batch ? m_of(b) : 0;
+            total += __reduce_add_sync(0xffffffffu, (m + P - 1) / P);
+        }
+        if (total <= grid * kMaxScoreItems) break;
+        P *= 2;
     }
+    int cnt = 0, run = 0;
+#pragma unroll 1
+    for (int base = 0; base < p.batch; base += 32) {
+        const int b = base + lane;
+        const int m = b < p.batch ? m_of(b) : 0;
+        const int ni = (m + P - 1) / P;
+        int x = ni;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        const int off = run + x - ni;
+        // this CTA's slices c, c + grid, ... that fall in sequence b
+        for (int t = c; t < off + ni; t += grid) {
+            if (t >= off) {
+                const int j = (t - c) / grid;            // slot in this CTA's list
+                const int k = t - off;
+                if (j < kMaxScoreItems)
+                    items[j] = make_int4(b, k * P, min(m, (k + 1) * P), 0);
+            }
+        }
+        run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    cnt = run > c ? (run - c + grid - 1) / grid : 0;
+    return min(cnt, kMaxScoreItems);
 }
 
-// A consumer warp's bounded wait on a full stage.  Every lane polls; the
-// outcome is lane 0's, so that the whole warp takes one branch before the
-// warp-synchronous code that reads the stage.
-__device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           const StepParams& p, int lane) {
-    bool ok = !*abort_flag && mbar_wait(bar, parity, abort_flag);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (!ok && lane == 0 && !*abort_flag) give_up(p, abort_flag);
-    return ok;
+// Decode pieces: unit u gets pieces_u = max(1, min(max_splits, nc_u,
+// floor(nc_u * share / total))) pieces of nc_u * k / pieces_u chunks, share
+// lowered from slots = grid * ceil(units / grid) until the pieces fit the
+// slots; piece t (in unit order) is run by CTA t % grid.  Writes this CTA's
+// pieces (unit, first chunk, end chunk, partial slot or -1), their units'
+// (first piece, pieces) and returns their count.
+__device__ int plan_decode(const StepParams& p, const int2* sseq, int lane, int4* items,
+                           int2* uitems) {
+    const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int H = p.kv.num_kv_heads, units = p.units;
+    const int cap = p.kv.max_pages_per_seq * kPage;
+    const bool pending = p.k_new != nullptr;
+    auto nc_of = [&](int u) {
+        const int2 x = sseq[u / H];
+        return seq_vals(x.x, x.y, cap, pending).chunks;
+    };
+    int total = 0;
+#pragma unroll 1
+    for (int base = 0; base < units; base += 32)
+        total += __reduce_add_sync(0xffffffffu, base + lane < units ? nc_of(base + lane) : 0);
+    const int tot = max(1, total);
+    const int slots = grid * ((units + grid - 1) / grid);
+    auto pieces_of = [&](int nc, int share) {
+        return nc == 0 ? 1
+                       : max(1, min(p.max_splits, min(nc, (int)((long long)nc * share / tot))));
+    };
+    int share = slots, run = 0;
+#pragma unroll 1
+    for (int iter = 0; iter < 6; ++iter) {
+        run = 0;
+#pragma unroll 1
+        for (int base = 0; base < units; base += 32) {
+            const int u = base + lane;
+            const int pc = u < units ? pieces_of(nc_of(u), share) : 0;
+            int x = pc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int off = run + x - pc;
+            if (u < units) {
+                for (int t = c; t < off + pc; t += grid) {
+                    if (t >= off) {
+                        const int j = (t - c) / grid;
+                        const int k = t - off, nc = nc_of(u);
+                        if (j < kMaxPieces) {
+                            items[j] = make_int4(u, (int)((long long)nc * k / pc),
+                                                 (int)((long long)nc * (k + 1) / pc),
+                                                 pc == 1 ? -1 : t);
+                            uitems[j] = make_int2(off, pc);
+                        }
+                    }
+                }
+            }
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        __syncwarp();
+        if (run <= slots || share == 0) break;            // share 0: one piece per unit
+        share = iter == 4 ? 0 : max(0, share - (run - slots));
+    }
+    const int cnt = run > c ? (run - c + grid - 1) / grid : 0;
+    return min(cnt, kMaxPieces);
 }
 
-template <int D, int NT, bool TWO_TERM, int VPL, bool REG>
+template <int D, int NT, bool TWO_TERM>
 __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
     quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                       const StepParams p) {
     using S = DecShape<D, NT>;
-    using SS = StepShape<D>;
+    using SS = StepShape<D, NT>;
     constexpr int NS = SS::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -495,79 +554,57 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
     uint8_t* ring = base;
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + NS * SS::kStageBytes);
     uint64_t* empty = full + NS;
-    uint64_t* ifull = empty + NS;
-    uint64_t* iempty = ifull + kItemSlots;
-    int* stage_ntok = reinterpret_cast<int*>(iempty + kItemSlots);
-    StepItem* items = reinterpret_cast<StepItem*>(stage_ntok + NS);
-    int* misc = reinterpret_cast<int*>(items + kItemSlots);   // 16 ints
-    volatile int* abort_flag = misc;                          // [0]
-    // [1] last-piece flag of the decode merge, [2] top-k go, [3] last CTA,
-    // [4..7] scan scratch, [8] block total
-    float* coef = reinterpret_cast<float*>(base + p.off_coef);
-    uint8_t* area = base + p.off_union;
-    int4* sinfo = reinterpret_cast<int4*>(base + p.off_sinfo);   // [2 * batch]
-    int* rstart = reinterpret_cast<int*>(base + p.off_rstart);   // [rounds + 1]
-    const int* gabort = p.sync + 2;
+    int* stage_ntok = reinterpret_cast<int*>(empty + NS);
+    int* misc = stage_ntok + NS;                               // 64 ints
+    volatile int* abort_flag = misc;                           // [0]
+    // [1] last-piece flag of the merge, [3] last CTA, [4] score slices,
+    // [5] pieces
+    int4* pitem = reinterpret_cast<int4*>(misc + 64);          // [kMaxPieces]
+    int4* pseq = pitem + kMaxPieces;                           // [kMaxPieces] held, ctx, n, k
+    int2* puit = reinterpret_cast<int2*>(pseq + kMaxPieces);   // [kMaxPieces]
+    int4* sitem = reinterpret_cast<int4*>(puit + kMaxPieces);  // [kMaxScoreItems]
+    uint8_t* uni = base + p.off_union;                         // staging, then coef, then merge
+    int2* sseq = reinterpret_cast<int2*>(uni);                 // [batch] (ctx_len, budget)
+    float* coef = reinterpret_cast<float*>(uni);               // [H][2][D]
+    float* merge = reinterpret_cast<float*>(uni);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.kv.num_kv_heads, stride = p.kv.max_pages_per_seq;
+    const int cap = stride * kPage;
+    const bool pending = p.k_new != nullptr;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int s = 0; s < kItemSlots; ++s) {
-            mbar_init(&ifull[s], 1);
-            mbar_init(&iempty[s], kConsumerWarps);
-        }
         *abort_flag = 0;
         fence_barrier_init();
     }
-    int grab = 0;
-    if (warp == kConsumerWarps && lane == 0) grab = atomicAdd(p.sync, 1);
-    if (warp < kConsumerWarps) {
-        // ---- per-sequence plans and the round table (consumer warps) ----
-        const int ctid = threadIdx.x;
-        int carry = 0;
-        for (int b0 = 0; b0 < p.batch; b0 += kCThreads) {
-            const int b = b0 + ctid;
-            SeqPlan s = {};
-            int dec = 0;
-            if (b < p.batch) {
-                s = seq_plan(p, b, true);
-                dec = H * s.pieces;
-            }
-            const int incl = scan128(dec, misc + 4, warp, lane);
-            if (b < p.batch) {
-                sinfo[2 * b] = make_int4(s.tiles, s.pieces, s.chunks, carry + incl - dec);
-                sinfo[2 * b + 1] = make_int4(s.held, s.ctx, s.n, s.k);
-            }
-            if (ctid == kCThreads - 1) misc[8] = incl;
-            consumer_bar();
-            carry += misc[8];
-            consumer_bar();
-        }
-        carry = 0;
-        for (int r0 = 0; r0 <= p.rounds; r0 += kCThreads) {
-            const int r = r0 + ctid;
-            int cnt = 0;
-            if (r < p.rounds) {
-                if (r < p.batch) cnt += sinfo[2 * r].x;
-                const int bt = r - p.lag_topk;
-                if (bt >= 0 && bt < p.batch) cnt += H;
-                const int bd = r - p.lag_dec;
-                if (bd >= 0 && bd < p.batch) cnt += H * sinfo[2 * bd].y;
-            }
-            const int incl = scan128(cnt, misc + 4, warp, lane);
-            if (r <= p.rounds) rstart[r] = carry + incl - cnt;
-            if (ctid == kCThreads - 1) misc[8] = incl;
-            consumer_bar();
-            carry += misc[8];
-            consumer_bar();
+    // every sequence's (ctx_len, budget), one load each, all in flight
+    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
+        const int held = p.kv.ctx_len[b], bud = p.budget[b];
+        sseq[b] = make_int2(held, bud);
+        if (blockIdx.x == 0) {
+            if (held < 0 || held > cap) flag(p.status, SE_DEV_BAD_LENGTH);
+            else if (pending && held >= cap) flag(p.status, SE_DEV_CAPACITY);
         }
     }
     __syncthreads();
-    const int total = rstart[p.rounds];
+    if (warp == 0) {
+        const int n = plan_score(p, sseq, lane, sitem);
+        if (lane == 0) misc[4] = n;
+    } else if (warp == 1) {
+        const int n = plan_decode(p, sseq, lane, pitem, puit);
+        __syncwarp();
+        for (int j = lane; j < n; j += 32) {
+            const int2 x = sseq[pitem[j].x / H];
+            const SeqVals s = seq_vals(x.x, x.y, cap, pending);
+            pseq[j] = make_int4(s.held, x.y, 0, 0);
+        }
+        if (lane == 0) misc[5] = n;
+    }
+    __syncthreads();
+    const int nscore = misc[4], npieces = misc[5];
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
@@ -575,171 +612,87 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
         }
-        auto make_item = [&](int gidx) {
-            StepItem it = {kItemEnd, 0, 0, 0, 0, 0, 0, 0};
-            if (gidx >= p.batch + total || *abort_flag ||
-                *reinterpret_cast<const volatile int*>(gabort))
-                return it;
-            if (gidx < p.batch) {                         // the query folds come first
-                it.type = kItemFold;
-                it.b = gidx;
-                return it;
-            }
-            const int idx = gidx - p.batch;
-            int lo = 0, hi = p.rounds - 1;                // last round starting at or before idx
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (rstart[mid] <= idx) lo = mid; else hi = mid - 1;
-            }
-            const int r = lo;
-            int off = idx - rstart[r];
-            if (r < p.batch) {
-                const int tiles = sinfo[2 * r].x;
-                if (off < tiles) {
-                    const int m = sinfo[2 * r + 1].z - 1;
-                    it.type = kItemScore;
-                    it.b = r;
-                    it.a0 = off * p.tile_pages;
-                    it.a1 = min(m, it.a0 + p.tile_pages);
-                    return it;
-                }
-                off -= tiles;
-            }
-            const int bt = r - p.lag_topk;
-            if (bt >= 0 && bt < p.batch) {
-                if (off < H) {
-                    it.type = kItemTopk;
-                    it.b = bt;
-                    it.h = off;
-                    return it;
-                }
-                off -= H;
-            }
-            const int bd = r - p.lag_dec;
-            const int4 a = sinfo[2 * bd];
-            const int pieces = a.y, chunks = a.z;
-            const int h = off / pieces, kp = off % pieces;
-            it.type = kItemDecode;
-            it.b = bd;
-            it.h = h;
-            it.a0 = (int)((int64_t)chunks * kp / pieces);
-            it.a1 = (int)((int64_t)chunks * (kp + 1) / pieces);
-            it.a3 = a.w + h * pieces;
-            it.a2 = pieces == 1 ? -1 : it.a3 + kp;
-            it.a4 = pieces;
-            return it;
-        };
-        uint32_t seq = 0, iseq = 0;
-        int cur = grab;                                    // lane 0's
-        while (true) {
-            StepItem it = {kItemEnd, 0, 0, 0, 0, 0, 0, 0};
-            int nxt = 0;
+        uint32_t seq = 0;
+        // 1. the score slices: each one contiguous block of summaries, 1-D bulk copies
+        for (int i = 0; i < nscore; ++i) {
+            const int4 it = sitem[i];
+            const int64_t bytes = (int64_t)(it.z - it.y) * H * SS::kSumBytes;
+            const uint8_t* src = static_cast<const uint8_t*>(p.kv.meta) +
+                                 ((int64_t)it.x * stride + it.y) * H * SS::kSumBytes;
+            const int nst = static_cast<int>((bytes + SS::kStageBytes - 1) / SS::kStageBytes);
             if (lane == 0) {
-                it = make_item(cur);
-                if (it.type != kItemEnd) nxt = atomicAdd(p.sync, 1);   // the next item, early
-                const int is = iseq % kItemSlots;
-                // not cut short by the abort word: after an abort the consumers
-                // skip their work, free the slot at once and need the end item
-                volatile int never = 0;
-                if (!mbar_wait(&iempty[is], ((iseq / kItemSlots) & 1) ^ 1, &never)) {
-                    // the consumers stopped reading: publish nothing more
-                    if (!*abort_flag) give_up(p, abort_flag);
-                    it.type = kItemEnd;
-                } else {
-                    items[is] = it;
-                    mbar_arrive(&ifull[is]);
+                for (int j = 0; j < nst; ++j) {
+                    const uint32_t sq = seq + j;
+                    const int s = sq % NS;
+                    if (!*abort_flag && !mbar_wait(&empty[s], ((sq / NS) & 1) ^ 1, abort_flag))
+                        give_up(p, abort_flag);
+                    const uint32_t sz = static_cast<uint32_t>(
+                        min(static_cast<int64_t>(SS::kStageBytes), bytes - (int64_t)j * SS::kStageBytes));
+                    if (!*abort_flag) {
+                        mbar_arrive_expect_tx(&full[s], sz);
+                        bulk_g2s(ring + s * SS::kStageBytes, src + (int64_t)j * SS::kStageBytes, sz,
+                                 &full[s]);
+                    } else {
+                        mbar_arrive(&full[s]);
+                    }
                 }
             }
-            ++iseq;
-            const int type = __shfl_sync(0xffffffffu, it.type, 0);
-            if (type == kItemEnd) break;
-            const int b = __shfl_sync(0xffffffffu, it.b, 0);
-            const int a0 = __shfl_sync(0xffffffffu, it.a0, 0);
-            const int a1 = __shfl_sync(0xffffffffu, it.a1, 0);
-            if (type == kItemScore) {
-                // the tile's summaries are one contiguous block: 1-D bulk copies
-                const int64_t bytes = (int64_t)(a1 - a0) * H * SS::kSumBytes;
-                const uint8_t* src = static_cast<const uint8_t*>(p.kv.meta) +
-                                     ((int64_t)b * stride + a0) * H * SS::kSumBytes;
-                const int nst = static_cast<int>((bytes + SS::kStageBytes - 1) / SS::kStageBytes);
-                if (lane == 0) {
-                    for (int j = 0; j < nst; ++j) {
-                        const uint32_t sq = seq + j;
-                        const int s = sq % NS;
+            seq += nst;
+        }
+        // 2. the decode pieces: the consumers first select and write the
+        // piece's view rows (and the new row), then release the producer
+        const uint64_t kv_policy = l2_evict_first();
+        for (int j = 0; j < npieces; ++j) {
+            producer_bar();
+            const int4 it = pitem[j];
+            const int u = it.x, c0 = it.y, c1 = it.z;
+            const SeqVals sv = seq_vals(pseq[j].x, pseq[j].y, cap, pending);
+            const int ntok = sv.tokens;
+            const int32_t* crow = p.view.chunk_row + (int64_t)u * p.view.max_chunks;
+            int row_next = c0 + lane < c1 ? __ldcg(crow + c0 + lane) : -1;
+            for (int cb = c0; cb < c1; cb += 32) {
+                const int row_l = row_next;
+                row_next = cb + 32 + lane < c1 ? __ldcg(crow + cb + 32 + lane) : -1;
+                const int nb = min(32, c1 - cb);
+                // four chunks per iteration: chunk t = lane / 4 of the group is
+                // led by lane 4t (waits for its stage, arms its barrier); then
+                // lanes 4t..4t+3 issue that chunk's K and V boxes together
+                for (int j0 = 0; j0 < nb; j0 += 4) {
+                    const int t = lane >> 2, qq = lane & 3;
+                    const int jj = j0 + t;
+                    const bool mine = t < 4 && jj < nb;
+                    const int row = __shfl_sync(0xffffffffu, row_l, min(jj, 31));
+                    const uint32_t sq = seq + t;
+                    const int s = sq % NS;
+                    int go = 0;
+                    if (mine && qq == 0) {
+                        const int c = cb + jj;
                         if (!*abort_flag && !mbar_wait(&empty[s], ((sq / NS) & 1) ^ 1, abort_flag))
                             give_up(p, abort_flag);
-                        const uint32_t sz = static_cast<uint32_t>(
-                            min(static_cast<int64_t>(SS::kStageBytes), bytes - (int64_t)j * SS::kStageBytes));
-                        if (!*abort_flag) {
-                            mbar_arrive_expect_tx(&full[s], sz);
-                            bulk_g2s(ring + s * SS::kStageBytes, src + (int64_t)j * SS::kStageBytes, sz,
-                                     &full[s]);
-                        } else {
+                        int cnt = min(kPage, ntok - c * kPage);
+                        if (row < 0 || (int64_t)row >= p.total_rows) {
+                            flag(p.status, SE_DEV_BAD_INDEX);
+                            cnt = 0;
+                        }
+                        stage_ntok[s] = cnt;
+                        go = cnt > 0 && !*abort_flag;
+                        if (go)
+                            mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+                        else
                             mbar_arrive(&full[s]);
-                        }
                     }
-                }
-                seq += nst;
-            } else if (type == kItemDecode) {
-                const int h = __shfl_sync(0xffffffffu, it.h, 0);
-                const int u = b * H + h;
-                const int4 si = sinfo[2 * b + 1];          // held, ctx, n, k
-                const int tokens = si.z <= si.w ? si.y : kPage * (si.w - 1) + (si.y - kPage * (si.z - 1));
-                if (a1 > a0) {
-                    if (lane == 0 && !*abort_flag &&
-                        !wait_geq(p.unit_ready + u, 1, abort_flag, gabort))
-                        give_up(p, abort_flag);
-                    __syncwarp();
-                    // the view rows and the appended row were written by the CTA
-                    // that ran the top-k; the row is read here by TMA
-                    fence_proxy_async_global();
-                }
-                const int32_t* crow = p.view.chunk_row + (int64_t)u * p.view.max_chunks;
-                for (int cb = a0; cb < a1; cb += 32) {
-                    const int row_l = cb + lane < a1 ? __ldcg(crow + cb + lane) : -1;
-                    const int nb = min(32, a1 - cb);
-                    // four chunks per iteration: chunk t = lane / 4 of the group is
-                    // led by lane 4t (waits for its stage, arms its barrier); then
-                    // lanes 4t..4t+3 issue that chunk's K and V boxes together
-                    for (int j0 = 0; j0 < nb; j0 += 4) {
-                        const int t = lane >> 2, q = lane & 3;
-                        const int j = j0 + t;
-                        const bool mine = t < 4 && j < nb;
-                        const int row = __shfl_sync(0xffffffffu, row_l, min(j, 31));
-                        const uint32_t sq = seq + t;
-                        const int s = sq % NS;
-                        int go = 0;
-                        if (mine && q == 0) {
-                            const int c = cb + j;
-                            if (!*abort_flag && !mbar_wait(&empty[s], ((sq / NS) & 1) ^ 1, abort_flag))
-                                give_up(p, abort_flag);
-                            int cnt = min(kPage, tokens - c * kPage);
-                            if (*abort_flag) {
-                                cnt = 0;
-                            } else if (row < 0 || (int64_t)row >= p.total_rows) {
-                                flag(p.status, SE_DEV_BAD_INDEX);
-                                cnt = 0;
-                            }
-                            stage_ntok[s] = cnt;
-                            go = cnt > 0;
-                            if (go)
-                                mbar_arrive_expect_tx(&full[s], S::kStageBytes);
-                            else
-                                mbar_arrive(&full[s]);
-                        }
-                        go = __shfl_sync(0xffffffffu, go, lane & ~3);
-                        if (mine && go && q < 2 * S::kBoxes) {
-                            uint8_t* dst = ring + s * SS::kStageBytes + (q & 1) * S::kChunkBytes +
-                                           (q >> 1) * 2048;
-                            tma_load_2d(dst, (q & 1) ? &tv : &tk, &full[s], 64 * (q >> 1), row);
-                        }
-                        seq += min(4, nb - j0);
+                    go = __shfl_sync(0xffffffffu, go, lane & ~3);
+                    if (mine && go && qq < 2 * S::kBoxes) {
+                        uint8_t* dst = ring + s * S::kStageBytes + (qq & 1) * S::kChunkBytes +
+                                       (qq >> 1) * 2048;
+                        tma_load_2d_hint(dst, (qq & 1) ? &tv : &tk, &full[s], 64 * (qq >> 1), row,
+                                         kv_policy);
                     }
+                    seq += min(4, nb - j0);
                 }
             }
-            cur = __shfl_sync(0xffffffffu, nxt, 0);
         }
-        // every copy issued by this CTA lands before the CTA may exit
+        // Drain: every copy issued by this CTA lands before the CTA may exit.
         if (lane == 0) {
             const uint32_t first = seq > (uint32_t)NS ? seq - NS : 0;
             volatile int never = 0;
@@ -747,8 +700,41 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
                 mbar_wait(&full[q2 % NS], (q2 / NS) & 1, &never);
         }
     } else {
-        // ------------------------------ consumers ------------------------------
+        // -------------------------------- consumers --------------------------------
         const int ctid = threadIdx.x;
+        uint32_t seq = 0;
+        int folded = -1;
+        for (int i = 0; i < nscore; ++i) {
+            const int4 it = sitem[i];
+            const int b = it.x;
+            if (b != folded) {
+                consumer_bar();                          // the previous slice's reads of coef
+                step_fold<D>(p, b, coef, ctid);
+                consumer_bar();
+                folded = b;
+            }
+            const int nsum_all = (it.z - it.y) * H;
+            const int nst = (nsum_all + SS::kSumsPerStage - 1) / SS::kSumsPerStage;
+            for (int j = 0; j < nst; ++j, ++seq) {
+                if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
+                const int s = seq % NS;
+                if (lane == 0 && !*abort_flag && !mbar_wait(&full[s], (seq / NS) & 1, abort_flag))
+                    give_up(p, abort_flag);
+                __syncwarp();
+                if (!*abort_flag)
+                    score_stage<D>(p, ring + s * SS::kStageBytes,
+                                   min(SS::kSumsPerStage, nsum_all - j * SS::kSumsPerStage),
+                                   j * SS::kSumsPerStage, b, it.y, coef, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            // every key of the slice is written: publish the slice's pages
+            consumer_bar();
+            if (ctid == 0) {
+                __threadfence();
+                atomicAdd(p.seq_scored + b, it.z - it.y);
+            }
+        }
         DecOut dout;
         dout.out = p.out;
         dout.out_f32 = p.out_f32;
@@ -758,180 +744,102 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
         dout.counters = p.counters;
         dout.Hq = p.Hq;
         dout.G = p.G;
-        uint32_t seq = 0, iseq = 0;
-        int coef_b = -1;
-        while (true) {
-            const int is = iseq % kItemSlots;
-            if (!item_wait(&ifull[is], (iseq / kItemSlots) & 1)) {
-                // the producer is gone (it always publishes the end item when it
-                // gives up, well inside this limit): stop
-                if (lane == 0) give_up(p, abort_flag);
-                break;
+        const int segs = D / 8;
+        for (int j = 0; j < npieces; ++j) {
+            const int4 it = pitem[j];
+            const int u = it.x, c0 = it.y, c1 = it.z;
+            const int b = u / H, h = u % H;
+            const SeqVals sv = seq_vals(pseq[j].x, pseq[j].y, cap, pending);
+            const bool last_piece = c1 == sv.chunks;
+            const bool app = sv.room && last_piece;
+            AppendRegs ar;
+            if (app && ctid < segs) append_load(p.kv, b, h, sv.held, p.k_new, p.v_new, ctid, ar);
+            const int32_t* btr = p.kv.block_table + (int64_t)b * stride;
+            const int phys_new = app ? btr[sv.held / kPage] : -1;
+            // 1. wait until every candidate page of b is scored (bounded)
+            consumer_bar();                              // the ring is idle
+            if (ctid == 0 && sv.m > 0 && !*abort_flag &&
+                !wait_count(p, p.seq_scored + b, sv.m, abort_flag))
+                give_up(p, abort_flag);
+            consumer_bar();
+            // 2. this piece's ranks of the selection (garbage after an abort,
+            // through the same barriers)
+            piece_select(p, u, sv, c0, c1, ring, warp, lane);
+            consumer_bar();
+            // 3. its view rows: the physical chunk of each selected page
+            const int32_t* selp = p.sel_pages + (int64_t)u * stride;
+            int32_t* crow = p.view.chunk_row + (int64_t)u * p.view.max_chunks;
+            for (int c = c0 + ctid; c < c1; c += kCThreads) {
+                const int page = __ldcg(selp + c);
+                const int phys = (page >= 0 && page < stride) ? btr[page] : -1;
+                if (phys >= 0 && phys < p.kv.num_pages) {
+                    crow[c] = (phys * H + h) * kPage;
+                } else {
+                    crow[c] = -1;
+                    flag(p.status, SE_DEV_BAD_INDEX);
+                }
             }
-            const StepItem it = items[is];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&iempty[is]);
-            ++iseq;
-            if (it.type == kItemEnd) break;
-            const int b = it.b;
-            if (it.type == kItemFold) {
-                step_fold<D>(p, b, p.coef + (int64_t)b * H * 2 * D, warp, lane);
-                consumer_bar();
-                if (ctid == 0) st_release(p.seq_folded + b, 1);
-            } else if (it.type == kItemScore) {
-                constexpr int kU4 = D / 4;                    // 16-byte vectors per summary
-                constexpr int kLps = kU4 / VPL;               // lanes per summary
-                constexpr int kR = 32 / kLps;                 // summaries per warp-wide read
-                const int sub = lane % kLps, slot = lane / kLps;
-                const float* cg = p.coef + (int64_t)b * H * 2 * D;
-                if (b != coef_b) {
-                    // the sequence's coefficients, folded by its fold item
-                    if (ctid == 0 && !*abort_flag &&
-                        !wait_geq(p.seq_folded + b, 1, abort_flag, gabort))
-                        give_up(p, abort_flag);
-                    consumer_bar();
-                    if (!REG) {
-                        for (int i = ctid; i < H * 2 * D / 4; i += kCThreads)
-                            reinterpret_cast<float4*>(coef)[i] = __ldcg(reinterpret_cast<const float4*>(cg) + i);
-                        consumer_bar();
-                    }
-                    coef_b = b;
-                }
-                float cr[REG ? VPL * 8 : 1];
-                if (REG) {
-                    const int h = slot % H;                   // fixed: kR is a multiple of H
-#pragma unroll
-                    for (int j = 0; j < VPL; ++j) {
-                        const float4* c4 = reinterpret_cast<const float4*>(cg + h * 2 * D + (j * kLps + sub) * 8);
-                        const float4 x0 = __ldcg(c4), x1 = __ldcg(c4 + 1);
-                        cr[REG ? j * 8 + 0 : 0] = x0.x;
-                        cr[REG ? j * 8 + 1 : 0] = x0.y;
-                        cr[REG ? j * 8 + 2 : 0] = x0.z;
-                        cr[REG ? j * 8 + 3 : 0] = x0.w;
-                        cr[REG ? j * 8 + 4 : 0] = x1.x;
-                        cr[REG ? j * 8 + 5 : 0] = x1.y;
-                        cr[REG ? j * 8 + 6 : 0] = x1.z;
-                        cr[REG ? j * 8 + 7 : 0] = x1.w;
-                    }
-                }
-                const int nsum_all = (it.a1 - it.a0) * H;
-                const int nst = (nsum_all + SS::kSumsPerStage - 1) / SS::kSumsPerStage;
-                uint32_t* keys = p.keys + (int64_t)b * H * stride + it.a0;
-                for (int j = 0; j < nst; ++j, ++seq) {
-                    if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
-                    const int s = seq % NS;
-                    const bool ok = stage_wait(&full[s], (seq / NS) & 1, abort_flag, p, lane);
-                    const int nsum = min(SS::kSumsPerStage, nsum_all - j * SS::kSumsPerStage);
-                    if (ok) {
-                        const uint8_t* st = ring + s * SS::kStageBytes;
-                        for (int t0 = 0; t0 < nsum; t0 += kR) {
-                            const int tl = t0 + slot;
-                            const int t = j * SS::kSumsPerStage + tl;   // summary within the tile
-                            const int h = t % H, pl = t / H;
-                            float acc = 0.f;
-                            if (tl < nsum) {
-                                const uint4* sv = reinterpret_cast<const uint4*>(st + tl * SS::kSumBytes);
-#pragma unroll
-                                for (int jj = 0; jj < VPL; ++jj) {
-                                    const uint4 w = sv[jj * kLps + sub];
-                                    const uint32_t a4[4] = {w.x, w.y, w.z, w.w};
-                                    const float* cf = coef + h * 2 * D + (jj * kLps + sub) * 8;
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const float c0 = REG ? cr[REG ? jj * 8 + 2 * e : 0] : cf[2 * e];
-                                        const float c1 = REG ? cr[REG ? jj * 8 + 2 * e + 1 : 0] : cf[2 * e + 1];
-                                        acc = fmaf(c0, bf_lo(a4[e]), acc);
-                                        acc = fmaf(c1, bf_hi(a4[e]), acc);
-                                    }
-                                }
-                            }
-#pragma unroll
-                            for (int o = kLps / 2; o >= 1; o >>= 1)
-                                acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                            if (sub == 0 && tl < nsum) keys[(int64_t)h * stride + pl] = float_key(acc);
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[s]);
-                }
-                // the tile's keys are stored: count it for sequence b
-                consumer_bar();
-                if (ctid == 0) red_release_add(p.seq_scored + b, 1);
-            } else if (it.type == kItemTopk) {
-                const int4 a = sinfo[2 * b], c = sinfo[2 * b + 1];
-                SeqPlan s;
-                s.tiles = a.x;
-                s.held = c.x;
-                s.ctx = c.y;
-                s.n = c.z;
-                s.k = c.w;
-                s.tokens = s.n <= s.k ? s.ctx : kPage * (s.k - 1) + (s.ctx - kPage * (s.n - 1));
-                if (ctid == 0) {
-                    int go = !*abort_flag;
-                    if (go && s.tiles > 0 && !wait_geq(p.seq_scored + b, s.tiles, abort_flag, gabort)) {
-                        give_up(p, abort_flag);
-                        go = 0;
-                    }
-                    misc[2] = go;
-                }
-                consumer_bar();
-                const int go = misc[2];
-                if (go) step_topk(p, b, it.h, s, area, warp, lane);
-                consumer_bar();
-                if (ctid == 0 && go) st_release(p.unit_ready + b * H + it.h, 1);
-            } else {
-                const int h = it.h, u = b * H + h;
-                DecState<D, NT> st;
-                dec_begin<D, NT>(st, p.q, (int64_t)b * p.Hq + h * p.G, p.G, lane);
-                for (int c = it.a0; c < it.a1; ++c, ++seq) {
-                    if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
-                    const int s = seq % NS;
-                    const bool ok = stage_wait(&full[s], (seq / NS) & 1, abort_flag, p, lane);
-                    const int cnt = ok ? stage_ntok[s] : 0;
-                    if (cnt > 0)
-                        dec_chunk<D, NT, TWO_TERM>(st, ring + s * SS::kStageBytes, cnt, lane, p.scale,
-                                                   p.scale_log2, p.G, nullptr, 0ull);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[s]);
-                }
-                dec_finish<D, NT>(st, reinterpret_cast<float*>(area), misc + 1, dout, b, h, u, it.a2,
-                                  make_int2(it.a3, it.a4), warp, lane);
+            if (c0 == 0 && ctid == 0) {
+                p.n_sel[u] = sv.chunks;
+                p.view.n_tokens[u] = sv.tokens;
             }
+            // 4. the new token's row, read next by this CTA's TMA (async proxy)
+            if (app && ctid < segs) {
+                if (phys_new >= 0 && phys_new < p.kv.num_pages) {
+                    append_store(p.kv, b, h, sv.held, phys_new, ctid, ar);
+                    fence_proxy_async_global();
+                } else if (ctid == 0) {
+                    flag(p.status, SE_DEV_BAD_INDEX);
+                }
+            }
+            producer_bar();                              // the producer may stream the piece
+            // 5. the decode of the piece's chunks
+            DecState<D, NT> st;
+            dec_begin<D, NT>(st, p.q, (int64_t)b * p.Hq + h * p.G, p.G, lane);
+            for (int c = c0; c < c1; ++c, ++seq) {
+                if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
+                const int s = seq % NS;
+                const uint32_t ph = (seq / NS) & 1;
+                if (!*abort_flag && !mbar_wait(&full[s], ph, abort_flag)) give_up(p, abort_flag);
+                const int cnt = *abort_flag ? 0 : stage_ntok[s];
+                if (cnt > 0)
+                    dec_chunk<D, NT, TWO_TERM>(st, ring + s * S::kStageBytes, cnt, lane, p.scale,
+                                               p.scale_log2, p.G, nullptr, 0);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            consumer_bar();                              // the union area: coef -> merge
+            dec_finish<D, NT>(st, merge, misc + 1, dout, b, h, u, it.w, puit[j], warp, lane);
         }
     }
-
-    // ---- the last CTA to finish resets the queue and commits the lengths ----
+    // ---- end: the last CTA commits the lengths and clears the control words ----
     __syncthreads();
     if (threadIdx.x == 0) {
         int old;
         asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
                      : "=r"(old)
-                     : "l"(p.sync + 1)
+                     : "l"(p.sync)
                      : "memory");
         misc[3] = old == static_cast<int>(gridDim.x) - 1;
     }
     __syncthreads();
     if (misc[3]) {
-        // after an abort the appended rows are not known to be written: the
-        // lengths stay as they were
-        const bool commit = *reinterpret_cast<const volatile int*>(gabort) == 0;
+        const bool aborted = *reinterpret_cast<const volatile int*>(p.sync + 1) != 0;
         for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
-            p.seq_scored[b] = 0;
-            p.seq_folded[b] = 0;
-            const int4 c = sinfo[2 * b + 1];
-            if (commit && p.k_new != nullptr && c.y == c.x + 1) {
-                const int phys = p.kv.block_table[(int64_t)b * stride + c.x / kPage];
-                if (phys >= 0 && phys < p.kv.num_pages) p.kv.ctx_len[b] = c.y;
+            if (pending && !aborted) {
+                const int held = __ldcg(p.kv.ctx_len + b);
+                if (held >= 0 && held < cap) {
+                    const int phys = p.kv.block_table[(int64_t)b * stride + held / kPage];
+                    if (phys >= 0 && phys < p.kv.num_pages) p.kv.ctx_len[b] = held + 1;
+                }
             }
+            p.seq_scored[b] = 0;
         }
-        for (int u = threadIdx.x; u < p.batch * H; u += blockDim.x) {
-            p.unit_ready[u] = 0;
-            p.counters[u] = 0;
-        }
+        for (int u = threadIdx.x; u < p.units; u += blockDim.x) p.counters[u] = 0;
+        __syncthreads();
         if (threadIdx.x == 0) {
-            p.sync[0] = 0;
             p.sync[1] = 0;
-            p.sync[2] = 0;
+            p.sync[0] = 0;
         }
     }
 }
@@ -940,120 +848,117 @@ size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct StepWs {
     int* status;
-    uint32_t* keys;
-    float* coef;
     int* sync;
-    int* seq_folded;
     int* seq_scored;
-    int* unit_ready;
     int* counters;
+    uint32_t* keys;
     float* lse_part;
     float* o_part;
 };
 
-StepWs step_ws_carve(void* ws, int batch, int H, int G, int D, int max_pages, int max_splits) {
+// Workspace layout.  Every word the kernel needs at zero when it starts -- the
+// finished-CTA count and the abort word, the per-sequence scored counters and
+// the per-unit arrival counters -- sits in one control block right after the
+// 256-byte header, each array at an offset fixed by the largest supported
+// shape (kStepMaxBatch sequences, kStepMaxUnits units), so that no call's
+// zero words ever land on another call's data; every call leaves them at zero.
+size_t step_ctl_bytes() {
+    return 256 + 256 + a256((size_t)kStepMaxBatch * sizeof(int)) +
+           a256((size_t)kStepMaxUnits * sizeof(int));
+}
+
+StepWs step_ws_carve(void* ws, int batch, int H, int G, int max_pages, int max_splits) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     const size_t units = (size_t)batch * H, slots = units * max_splits;
     StepWs w;
     w.status = reinterpret_cast<int*>(base);
     size_t off = 256;
-    w.keys = reinterpret_cast<uint32_t*>(base + off);
-    off += a256(units * max_pages * sizeof(uint32_t));
     w.sync = reinterpret_cast<int*>(base + off);
     off += 256;
     w.seq_scored = reinterpret_cast<int*>(base + off);
-    off += a256((size_t)batch * sizeof(int));
-    w.seq_folded = reinterpret_cast<int*>(base + off);
-    off += a256((size_t)batch * sizeof(int));
-    w.coef = reinterpret_cast<float*>(base + off);
-    off += a256(units * 2 * D * sizeof(float));
-    w.unit_ready = reinterpret_cast<int*>(base + off);
-    off += a256(units * sizeof(int));
+    off += a256((size_t)kStepMaxBatch * sizeof(int));
     w.counters = reinterpret_cast<int*>(base + off);
-    off += a256(units * sizeof(int));
+    off += a256((size_t)kStepMaxUnits * sizeof(int));
+    w.keys = reinterpret_cast<uint32_t*>(base + off);
+    off += a256(units * max_pages * sizeof(uint32_t));
     w.lse_part = reinterpret_cast<float*>(base + off);
     off += a256(slots * G * sizeof(float));
     w.o_part = reinterpret_cast<float*>(base + off);
     return w;
 }
 
-template <int D, int NT, bool TWO, int VPL, bool REG>
-cudaError_t run_step(const CUtensorMap& tk, const CUtensorMap& tv, const StepParams& p, size_t smem,
-                     cudaStream_t s) {
-    auto kern = quest_step_kernel<D, NT, TWO, VPL, REG>;
+// Dynamic shared memory: the stage ring, the small areas, then the union area
+// (the sequences' staged lengths and budgets, then the query coefficients,
+// then the decode merge area).
+template <int D, int NT>
+size_t step_smem(int batch, int H, int* off_union, int* ring_bytes) {
+    using SS = StepShape<D, NT>;
+    const size_t ring = (size_t)SS::kStages * SS::kStageBytes;
+    const size_t uni_off = ring + SS::kFixed;
+    const size_t uni = std::max({(size_t)DecShape<D, NT>::kMergeFloats * 4, (size_t)H * 2 * D * 4,
+                                 (size_t)batch * 8});
+    if (off_union) *off_union = static_cast<int>((uni_off + 15) & ~static_cast<size_t>(15));
+    if (ring_bytes) *ring_bytes = static_cast<int>(ring);
+    return 1024 + ((uni_off + 15) & ~static_cast<size_t>(15)) + uni;
+}
+
+template <int D, int NT, bool TWO>
+cudaError_t run_step(const CUtensorMap& tk, const CUtensorMap& tv, StepParams p, cudaStream_t s) {
+    auto kern = quest_step_kernel<D, NT, TWO>;
+    const size_t smem = step_smem<D, NT>(p.batch, p.kv.num_kv_heads, &p.off_union, &p.ring_bytes);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem);
     if (e != cudaSuccess) return e;
-    const int grid = num_sms() * max(1, per_sm);
-    kern<<<grid, kDecodeThreads, smem, s>>>(tk, tv, p);
-    return cudaGetLastError();
-}
-
-template <int D, int NT, bool TWO>
-cudaError_t run_step_vpl(const CUtensorMap& tk, const CUtensorMap& tv, const StepParams& p,
-                         size_t smem, cudaStream_t s) {
-    // register coefficients when a warp-wide read (4 summaries at D = 128 with
-    // 4 vectors per lane, 8 at D = 64) is a multiple of the KV head count
-    constexpr int kR = 32 / (D / 4 / 4);
-    if (kR % p.kv.num_kv_heads == 0) return run_step<D, NT, TWO, 4, true>(tk, tv, p, smem, s);
-    return run_step<D, NT, TWO, 1, false>(tk, tv, p, smem, s);
-}
-
-// Dynamic shared memory of the step kernel: the fixed part, the coefficients,
-// the union (decode merge / top-k keys and histogram), the sequence plans and
-// the round table.  Writes the offsets into p when given.
-size_t step_smem(int batch, int H, int D, int G, int max_pages, int lag_dec, StepParams* p) {
-    // register coefficients (no shared copy) when a warp-wide read covers a
-    // multiple of the KV heads: 4 summaries at D = 128, 8 at D = 64
-    const bool reg = (D == 128 ? 4 : 8) % H == 0;
-    const int NT = G > 8 ? 2 : 1;
-    const size_t fixed = D == 64 ? StepShape<64>::kFixed : StepShape<128>::kFixed;
-    const size_t merge = (size_t)(kConsumerWarps * NT * 8 * 2 + 2 * NT * 8 * D +
-                                  (kConsumerWarps + 1) * NT * 8) * 4;
-    const size_t topk = (size_t)(kStepBins + 64) * 4 + (size_t)max_pages * 4;
-    size_t off = (fixed + 15) & ~size_t(15);
-    const size_t coef = off;
-    off += reg ? 0 : (size_t)H * 2 * D * 4;
-    off = (off + 15) & ~size_t(15);
-    const size_t uni = off;
-    off += std::max(merge, topk);
-    off = (off + 15) & ~size_t(15);
-    const size_t sinfo = off;
-    off += (size_t)batch * 32;
-    const size_t rstart = off;
-    off += (size_t)(batch + lag_dec + 1) * 4;
-    if (p) {
-        p->off_coef = static_cast<int>(coef);
-        p->off_union = static_cast<int>(uni);
-        p->off_sinfo = static_cast<int>(sinfo);
-        p->off_rstart = static_cast<int>(rstart);
-    }
-    return off + 1024;                                              // alignment slack
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int grid = std::min(2048, num_sms() * per_sm);
+    // the pieces of a CTA must fit its list: ceil(units / grid) <= kMaxPieces
+    if ((p.units + grid - 1) / grid > kMaxPieces) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;     // every CTA resident: the waits end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace
 
 size_t quest_step_ws_bytes(int batch, int H, int G, int D, int max_pages, int max_splits) {
+    (void)D;
     const size_t units = (size_t)batch * H, slots = units * max_splits;
-    return 256 + a256(units * max_pages * sizeof(uint32_t)) + 256 +
-           2 * a256((size_t)batch * sizeof(int)) + a256(units * 2 * D * sizeof(float)) +
-           2 * a256(units * sizeof(int)) + a256(slots * G * sizeof(float)) +
-           a256(slots * G * D * sizeof(float));
+    return step_ctl_bytes() + a256(units * max_pages * sizeof(uint32_t)) +
+           a256(slots * G * sizeof(float)) + a256(slots * G * (size_t)D * sizeof(float));
 }
 
-size_t quest_step_smem_bytes(int batch, int H, int D, int G, int max_pages, int lag_dec) {
-    return step_smem(batch, H, D, G, max_pages, lag_dec, nullptr);
+size_t quest_step_smem_bytes(int batch, int H, int D, int G) {
+    const int NT = G > 8 ? 2 : 1;
+    if (D == 64) return NT == 1 ? step_smem<64, 1>(batch, H, nullptr, nullptr)
+                                : step_smem<64, 2>(batch, H, nullptr, nullptr);
+    return NT == 1 ? step_smem<128, 1>(batch, H, nullptr, nullptr)
+                   : step_smem<128, 2>(batch, H, nullptr, nullptr);
+}
+
+size_t quest_step_ring_bytes(int D, int G) {
+    const int NT = G > 8 ? 2 : 1;
+    if (D == 64) return (size_t)StepShape<64, 1>::kStages * StepShape<64, 1>::kStageBytes;
+    return NT == 1 ? (size_t)StepShape<128, 1>::kStages * StepShape<128, 1>::kStageBytes
+                   : (size_t)StepShape<128, 2>::kStages * StepShape<128, 2>::kStageBytes;
 }
 
 cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const void* v_new,
                               const void* q, int batch, int num_q_heads, const int32_t* budget,
-                              float scale, int out_dtype, int max_splits, const StepTuning& tune,
-                              int32_t* sel_pages, int32_t* n_sel, const se_view& view, void* out,
-                              float* lse, void* ws, cudaEvent_t ev_begin, cudaEvent_t ev_end,
-                              cudaStream_t s) {
+                              float scale, int out_dtype, int max_splits, int item_pages,
+                              unsigned long long wait_ns, int32_t* sel_pages, int32_t* n_sel,
+                              const se_view& view, void* out, float* lse, void* ws,
+                              cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t s) {
     const int H = kv.num_kv_heads, D = kv.head_dim, G = num_q_heads / H;
     const int units = batch * H;
     if (units == 0) return cudaSuccess;
@@ -1061,7 +966,7 @@ cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const vo
     CUtensorMap tk, tv;
     if (!encode_rows_map(&tk, kv.k, total_rows, D) || !encode_rows_map(&tv, kv.v, total_rows, D))
         return cudaErrorInvalidValue;
-    const StepWs w = step_ws_carve(ws, batch, H, G, D, kv.max_pages_per_seq, max_splits);
+    const StepWs w = step_ws_carve(ws, batch, H, G, kv.max_pages_per_seq, max_splits);
 
     StepParams p;
     p.kv = kv;
@@ -1069,6 +974,7 @@ cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const vo
     p.Hq = num_q_heads;
     p.G = G;
     p.batch = batch;
+    p.units = units;
     p.budget = budget;
     p.k_new = static_cast<const uint4*>(k_new);
     p.v_new = static_cast<const uint4*>(v_new);
@@ -1081,31 +987,19 @@ cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const vo
     p.out_f32 = out_dtype == 1;
     p.lse_out = lse;
     p.keys = w.keys;
-    p.coef = w.coef;
-    p.sync = w.sync;
-    p.seq_folded = w.seq_folded;
     p.seq_scored = w.seq_scored;
-    p.unit_ready = w.unit_ready;
     p.counters = w.counters;
+    p.sync = w.sync;
     p.o_part = w.o_part;
     p.lse_part = w.lse_part;
-    // defaults: ~128 KB score tiles; decode pieces of 16 chunks (128 KB of K/V
-    // at D = 128); the top-k of a sequence 8 rounds after its score tiles, so
-    // that it mostly finds them done; every decode piece after the last score
-    // tile, so that no scoring block waits behind a decode piece whose top-k
-    // has not run
-    const int page_bytes = H * 2 * D * 2;
-    p.tile_pages = tune.tile_pages > 0 ? tune.tile_pages : std::max(1, 131072 / page_bytes);
-    p.piece_chunks = tune.piece_chunks > 0 ? tune.piece_chunks : 16;
     p.max_splits = max_splits;
-    p.lag_topk = tune.lag_topk > 0 ? tune.lag_topk : 8;
-    p.lag_dec = std::max(p.lag_topk, tune.lag_dec > 0 ? tune.lag_dec : batch - 1);
-    p.rounds = batch + p.lag_dec;
+    p.item_pages = item_pages;
+    p.off_union = 0;
+    p.ring_bytes = 0;
     p.total_rows = total_rows;
+    p.wait_ns = wait_ns;
     p.status = w.status;
     const int NT = G > 8 ? 2 : 1;
-    const size_t smem = step_smem(batch, H, D, G, kv.max_pages_per_seq, p.lag_dec, &p);
-    if (smem > 227 * 1024) return cudaErrorInvalidValue;
 
     auto record = [&](cudaEvent_t ev) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -1119,15 +1013,11 @@ cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const vo
     if (ev_begin && (e = record(ev_begin)) != cudaSuccess) return e;
     const bool two = out_dtype == 1;
     if (D == 64) {
-        e = NT == 1 ? (two ? run_step_vpl<64, 1, true>(tk, tv, p, smem, s)
-                           : run_step_vpl<64, 1, false>(tk, tv, p, smem, s))
-                    : (two ? run_step_vpl<64, 2, true>(tk, tv, p, smem, s)
-                           : run_step_vpl<64, 2, false>(tk, tv, p, smem, s));
+        e = NT == 1 ? (two ? run_step<64, 1, true>(tk, tv, p, s) : run_step<64, 1, false>(tk, tv, p, s))
+                    : (two ? run_step<64, 2, true>(tk, tv, p, s) : run_step<64, 2, false>(tk, tv, p, s));
     } else {
-        e = NT == 1 ? (two ? run_step_vpl<128, 1, true>(tk, tv, p, smem, s)
-                           : run_step_vpl<128, 1, false>(tk, tv, p, smem, s))
-                    : (two ? run_step_vpl<128, 2, true>(tk, tv, p, smem, s)
-                           : run_step_vpl<128, 2, false>(tk, tv, p, smem, s));
+        e = NT == 1 ? (two ? run_step<128, 1, true>(tk, tv, p, s) : run_step<128, 1, false>(tk, tv, p, s))
+                    : (two ? run_step<128, 2, true>(tk, tv, p, s) : run_step<128, 2, false>(tk, tv, p, s));
     }
     if (e != cudaSuccess) return e;
     if (ev_end && (e = record(ev_end)) != cudaSuccess) return e;

@@ -45,6 +45,13 @@ def test_status_strings_and_version(lib):
         assert isinstance(lib.se_status_str(rc), bytes)
 
 
+def test_sync_status_validates_before_touching_the_device(lib):
+    lib.se_sync_status.restype = ctypes.c_int
+    assert lib.se_sync_status(None, None) == -1             # SE_ERR_INVALID_ARG
+    assert lib.se_sync_status(ctypes.c_void_p((1 << 20) + 4), None) == -3   # not 256-aligned
+    assert lib.se_sync_status(ctypes.c_void_p((1 << 20) + 128), None) == -3
+
+
 def test_workspace_sizes(lib):
     assert lib.se_small_workspace() == 256
     assert lib.se_quest_select_workspace(16, 4, 2052) >= 16 * 4 * 2052 * 4
@@ -130,10 +137,13 @@ def test_quest_step_workspace_and_host_validation(lib):
     big = binding.ViewC(1 << 20, 1 << 20, 1025 * 4, 8)
     assert call(batch=1025, view_=big) == -2        # batch limit
     O = binding.QuestStepOptsC
-    assert call(opts=O(0, 65, None, None, 0, 0, 0, 0)) == -1         # max_splits
-    assert call(opts=O(2, 0, None, None, 0, 0, 0, 0)) == -1          # out_dtype
-    assert call(opts=O(0, 0, None, None, -1, 0, 0, 0)) == -1         # tile_pages
-    assert call(opts=O(0, 0, None, None, 0, 0, 65, 0)) == -1         # lag_topk
+    assert call(opts=O(0, 65, None, None, 0, 0)) == -1               # max_splits
+    assert call(opts=O(2, 0, None, None, 0, 0)) == -1                # out_dtype
+    assert call(opts=O(0, 0, None, None, -1, 0)) == -1               # slice_pages
+    assert call(opts=O(0, 0, None, None, 0, -5)) == -1               # wait_limit_ns
+    many = binding.ViewC(1 << 20, 1 << 20, 1024 * 8, 8)
+    kv8 = binding.PagedKVC(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 10, 4, 8, 128, 16)
+    assert call(batch=1024, hq=64, view_=many, kv_=kv8) == -2        # more than 4096 units
     assert call(ws_bytes=1024) == -3                # workspace too small
     # no append (k_new and v_new both NULL) is accepted up to the workspace check
     assert call(k_new=None, v_new=None, ws_bytes=1024) == -3

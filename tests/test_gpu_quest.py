@@ -16,6 +16,9 @@ from tests.parity import TOL_BF16, TOL_F32, bf16_tensor_to_f64, check_topk, max_
 
 pytestmark = pytest.mark.gpu
 U32 = synth.UNBOUNDED_BUDGET
+# int32 words of the one-kernel step's workspace head: status header, sync
+# words, 1024 per-sequence and 4096 per-unit counters
+CTL_WORDS = (256 + 256 + 1024 * 4 + 4096 * 4) // 4
 
 
 def oracle_unit(w, inputs, b, h, s, gpu_pages=None):
@@ -138,19 +141,18 @@ def test_ragged_multi_step_outliers(out_dtype, mode):
 def test_one_kernel_step_matches_two_calls():
     """se_quest_step == se_quest_select_append + se_sparse_decode: selections,
     view, lengths, cache rows and page summaries bit for bit, outputs within
-    the bf16 rounding of their different split pieces; steps open new pages
+    the rounding of their different split pieces; steps open new pages
     (contexts 15, 16, 31, 1000 and 2047 tokens at the start, one sequence with
-    every page selected), and the scheduling knobs (tile, piece, lags) are
-    varied from step to step."""
+    every page selected), and the scoring slice size is varied from step to
+    step."""
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name="quest_step_eq", batch=5, ctx=(15, 16, 31, 1000, 2047),
                      budget=(64, 64, 256, 128, U32), steps=12)
     inputs = synth.quest_inputs(w)
     a = QuestRun(w, inputs, mode="step", out_dtype=1)
     b = QuestRun(w, inputs, mode="fused", out_dtype=1)
-    knobs = [{}, {"tile_pages": 1}, {"tile_pages": 3, "piece_chunks": 1},
-             {"lag_topk": 1, "lag_dec": 1}, {"lag_topk": 7, "lag_dec": 30},
-             {"piece_chunks": 2, "lag_topk": 2, "lag_dec": 3}]
+    knobs = [{}, {"slice_pages": 1}, {"slice_pages": 3}, {"slice_pages": 40},
+             {"slice_pages": 7}, {"slice_pages": 2}]
     for s in range(w.steps):
         a.step_tuning = knobs[s % len(knobs)]
         a.step(s)
@@ -170,11 +172,10 @@ def test_one_kernel_step_matches_two_calls():
     assert torch.equal(a.kv.v.cpu(), b.kv.v.cpu())
     assert torch.equal(a.kv.meta.cpu(), b.kv.meta.cpu())
     assert a.status() == 0 and b.status() == 0
-    # the queue words (item counter, finished CTAs, abort) follow the status
-    # header and the keys, and every call leaves them at zero
-    keys_bytes = a.B * a.Hkv * a.sel.shape[1] * 4
-    sync = (256 + (keys_bytes + 255) // 256 * 256) // 4
-    assert int(a.ws_step.view(torch.int32)[sync:sync + 3].abs().sum().item()) == 0, "queue not reset"
+    # the control words (finished blocks, abort word, scored pages per
+    # sequence, split arrival counters) sit right after the status header,
+    # and every call leaves them at zero
+    assert int(a.ws_step.view(torch.int32)[64:CTL_WORDS].abs().sum().item()) == 0, "not reset"
 
 
 # (hkv 8 at d 128 and hkv 3 at d 64 take the scoring path with coefficients in
@@ -205,7 +206,7 @@ def test_split_count_does_not_change_results(max_splits, mode):
     w = synth.scaled(base, name="quest_splits", batch=2, ctx=(3000, 1234), budget=(U32, 1024),
                      steps=1)
     run_and_check(w, out_dtype=1, max_splits=max_splits, mode=mode,
-                  step_tuning={"piece_chunks": 4} if mode == "step" else None)
+                  step_tuning={"slice_pages": 5} if mode == "step" else None)
 
 
 def test_many_units_block_plan():
@@ -255,3 +256,32 @@ def test_full_size_ragged_128k_sampled():
     w = synth.workloads()["ragged_quest_128k"]
     run_and_check(w, steps={0, 31}, units=list(range(0, 32, 3)), mode="fused")
     run_and_check(w, steps={0, 31}, units=list(range(0, 32, 3)), mode="step")
+
+
+def test_step_wait_that_runs_out_reports_timeout_and_resets():
+    """A bounded wait that runs out (a limit of 1 ns: a block whose sequence is
+    still being scored by other blocks gives up at once) sets SE_DEV_TIMEOUT,
+    leaves ctx_len unchanged and the control words at zero; the next call,
+    with the default limit and the status word cleared, matches the oracle."""
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name="quest_timeout", batch=4, ctx=(20000, 15000, 9000, 30000),
+                     budget=(512, 1024, 256, 2048), steps=2)
+    inputs = synth.quest_inputs(w)
+    run = QuestRun(w, inputs, mode="step", step_tuning={"wait_limit_ns": 1})
+    ctx0 = run.kv.ctx_len.clone()
+    run.step(0)
+    st = se_status(run.ws_step)
+    assert st & 8, f"status {st}: expected SE_DEV_TIMEOUT"
+    assert torch.equal(run.kv.ctx_len, ctx0), "lengths committed after an abort"
+    assert int(run.ws_step.view(torch.int32)[64:CTL_WORDS].abs().sum().item()) == 0
+    run.ws_step.zero_()
+    run.step_tuning = {}
+    run.step(0)
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    check_step(run, inputs, 0)
+
+
+def se_status(ws):
+    from kv_cache_decode_quest_gb300 import binding
+    return binding.se_sync_status(ws)
