@@ -121,15 +121,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same test, but a thread whose phase is not complete is suspended in
+// hardware until it completes or about `hint_ns` pass, instead of returning at
+// once: a waiting warp then takes no issue slots from the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// Suspension bound of one try of a bounded wait: the abort flag and the time
+// limit are looked at least this often.
+constexpr uint32_t kWaitSliceNs = 20000;
+
 // Bounded wait: true when the phase of `parity` completed; false when the
 // CTA-wide abort flag is raised or the time limit passed (the caller then
-// raises the abort flag and records SE_DEV_TIMEOUT).
+// raises the abort flag and records SE_DEV_TIMEOUT).  Between tries the
+// thread sleeps in the barrier (see mbar_try_wait_sleep).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitSliceNs)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > kWaitLimitNs) return false;
     }

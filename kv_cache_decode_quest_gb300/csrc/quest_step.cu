@@ -10,30 +10,36 @@
 // Why one kernel: the step is two HBM streams (the page summaries, then the
 // selected K/V rows) joined by a short, latency-bound top-k per unit.  As
 // separate launches every kernel boundary, the top-k kernel and the decode's
-// planning sit on the critical path.  Here every CTA of one resident wave
-// (a cooperative launch, so every CTA is running) follows the same static
-// schedule, computed by each CTA from the sequence lengths and budgets:
-//   1. score: one contiguous slice of one sequence's candidate page summaries
-//      (all KV heads of each page), streamed with 1-D bulk copies through the
-//      stage ring and turned into order-preserving keys in the workspace; the
-//      slice's page count is then added to the sequence's scored counter;
-//   2. decode piece(s): a range of chunks of one unit u = (b, h).  The piece
-//      waits (bounded) until every candidate page of b is scored, runs the
-//      exact top-k of u itself from the keys in L2 (every piece of u computes
-//      the same selection; none waits on another's), writes its ranks of the
-//      selection and of the view, and streams its chunks' K/V with 2-D TMA into
-//      the same ring for the mma.sync decode of decode_core.cuh; split units are
-//      merged by the last piece to finish.
-// The new token's row is written by the piece that holds the unit's last
-// chunk (the forced last page), before its own copy of that chunk.  The last
-// CTA to finish commits ctx_len + 1 of every sequence whose token was
-// appended (every CTA has read the old lengths by then) and clears the
-// control words.  Waits are bounded: a CTA that gives up records
-// SE_DEV_TIMEOUT and raises a global abort word that the other waits poll;
-// every CTA still walks the same barriers to the end.
+// planning sit on the critical path.  Here every CTA of one resident wave (a
+// cooperative launch, so every CTA is running) follows the same static
+// schedule, computed by each CTA from the sequence lengths and budgets.  The
+// sequences are cut into groups; for each group in turn:
+//   score: one contiguous slice of one sequence's candidate page summaries
+//     (all KV heads of each page), streamed with 1-D bulk copies through the
+//     stage ring and turned into order-preserving keys in the workspace; the
+//     slice's page count is then added to the sequence's scored counter;
+// and then, for each group in turn:
+//   decode piece: a range of chunks of one unit u = (b, h), streamed with 2-D
+//     TMA into the same ring for the mma.sync decode of decode_core.cuh; split
+//     units are merged by the last piece to finish.
+// A piece waits (bounded) until every candidate page of b is scored, computes
+// the exact top-k of u itself from the keys in L2 (every piece of u computes
+// the same selection; none waits on another's), writes its ranks of the
+// selection and of the view, and releases the producer.  When no unit has more
+// than 2048 candidate pages, the CTA's selector warp does this while the other
+// warps stream, so one group's top-k runs while the next group is scored (and
+// the last group's while the first decodes); otherwise the four consumer warps
+// do it between the phases, with one group.  The new token's row is written by
+// the piece that holds the unit's last chunk (the forced last page), before
+// that chunk's copy.  The last CTA to finish commits ctx_len + 1 of every
+// sequence whose token was appended (every CTA has read the old lengths by
+// then) and clears the control words.  Waits are bounded: a CTA that gives up
+// records SE_DEV_TIMEOUT and raises a global abort word that the other waits
+// poll; every CTA still walks the same barriers to the end.
 //
-// CTA layout (160 threads): warps 0-3 consume (stage s is handled by warp
-// (stage sequence % 4), in both phases), warp 4 is the producer.
+// CTA layout (192 threads): warps 0-3 consume (stage s is handled by warp
+// (stage sequence % 4), in both phases), warp 4 is the producer, warp 5 the
+// selector.
 #include <algorithm>
 
 #include "append.cuh"
@@ -45,10 +51,17 @@ namespace se {
 namespace {
 
 constexpr int kCThreads = kConsumerWarps * 32;         // 128 consumer threads
-constexpr int kDigit = 10, kStepBins = 1 << kDigit;     // 10-bit radix digits: 8 bins per thread
+constexpr int kProducerWarp = kConsumerWarps;          // warp 4
+constexpr int kStepThreads = (kConsumerWarps + 1) * 32;
+constexpr int kDigit = 10, kStepBins = 1 << kDigit;     // top-k: 10-bit radix digits
 constexpr int kMaxPieces = 32;                          // decode pieces per CTA at most
 constexpr int kMaxScoreItems = 8;                       // score slices per CTA at most
 constexpr int kMinItemPages = 8;
+constexpr int kMaxGroups = 4;
+constexpr int kAreaKeys = 2048;                         // keys a unit's top-k holds outside the ring
+// the top-k's shared memory: histogram, small ints, keys
+constexpr int kSelectBytes = kStepBins * 4 + 64 * 4;
+constexpr int kAreaBytes = kSelectBytes + kAreaKeys * 4;
 
 struct StepParams {
     se_paged_kv kv;
@@ -64,15 +77,16 @@ struct StepParams {
     void* out;
     int out_f32;
     float* lse_out;
-    uint32_t* keys;                     // [units][max_pages_per_seq]
+    uint32_t* keys;                     // [units][kstride]
+    int kstride;                        // max_pages_per_seq rounded up to 4 (16-byte rows)
     int* seq_scored;                    // [batch] candidate pages scored
     int* counters;                      // [units] decode pieces finished
     int* sync;                          // [0] CTAs finished, [1] abort
     float* o_part;                      // [units * max_splits][G][D]
     float* lse_part;                    // [units * max_splits][G]
-    int max_splits, item_pages;         // item_pages 0: about one slice per CTA
+    int max_splits, item_pages;         // item_pages 0: about one slice per CTA and group
+    int groups;                         // sequence groups asked for, 1..kMaxGroups
     int off_union;                      // union area offset in dynamic shared memory
-    int ring_bytes;
     int64_t total_rows;
     unsigned long long wait_ns;
     int* status;
@@ -86,11 +100,11 @@ struct StepShape {
     static constexpr int kSumBytes = 2 * D * 2;                        // one (page, head) summary
     static constexpr int kSumsPerStage = kStageBytes / kSumBytes;      // 16
     static_assert(kStages % kConsumerWarps == 0, "stage ownership needs kStages % 4 == 0");
-    // small areas after the ring: full/empty barriers, stage token counts,
-    // misc ints, the CTA's pieces (item, unit range, sequence values) and
-    // score slices
-    static constexpr int kFixed = kStages * 16 + kStages * 4 + 64 * 4 + kMaxPieces * 48 +
-                                  kMaxScoreItems * 16;
+    // small areas after the ring: full/empty barriers, two plan barriers,
+    // the pieces' ready barriers, stage token counts, misc ints, the CTA's
+    // pieces (item, sequence values, unit range) and score slices
+    static constexpr int kFixed = kStages * 16 + 16 + kMaxPieces * 8 + kStages * 4 + 64 * 4 +
+                                  kMaxPieces * 32 + kMaxScoreItems * 16;
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -100,9 +114,6 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ void producer_bar() {
-    asm volatile("bar.sync 3, %0;" ::"r"(kDecodeThreads) : "memory");
 }
 
 // This CTA gives up: results are invalid; the kernel walks on to its end.
@@ -247,7 +258,8 @@ __device__ void step_threshold(const uint32_t* sk, int m, int K, int* hist, int*
     *need = remaining;
 }
 
-// The selection of unit u = (b, h) restricted to ranks [c0, c1): exact top-(k-1)
+// The selection of unit u = (b, h) restricted to ranks [c0, c1) on the four
+// consumer warps (used when a unit has more than 2048 candidate pages): exact top-(k-1)
 // of the candidate pages 0..n-2 by (score desc, page asc) in ascending page
 // order, then the last page (always selected, never scored) at rank k-1; all
 // pages when n <= k.  Writes sel_pages[u][rank] for the ranks of the range.
@@ -274,7 +286,7 @@ __device__ void piece_select(const StepParams& p, int u, const SeqVals& s, int c
     if (c1 == s.k && ctid == 0) selp[K] = s.n - 1;
     if (K == 0 || c0 >= K) return;                                // only the last page here
     {
-        const uint32_t* keys = p.keys + (int64_t)u * stride;
+        const uint32_t* keys = p.keys + (int64_t)u * p.kstride;
         constexpr int kU = 8;
         for (int base = ctid; base < m; base += kCThreads * kU) {
             uint32_t kv2[kU];
@@ -333,6 +345,49 @@ __device__ void piece_select(const StepParams& p, int u, const SeqVals& s, int c
     }
 }
 
+__device__ __forceinline__ int warp_excl_scan(int v, int lane) {
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x - v;
+}
+
+// The view rows of ranks [c0, c1) of unit u: the physical chunk of each
+// selected page (from sel_pages, written by the calling threads), `nt`
+// threads t = 0..nt-1, eight block-table lookups of a thread in flight together.
+__device__ void view_rows(const StepParams& p, int u, int c0, int c1, int t, int nt) {
+    const int H = p.kv.num_kv_heads, h = u % H, b = u / H;
+    const int stride = p.kv.max_pages_per_seq;
+    const int32_t* selp = p.sel_pages + (int64_t)u * stride;
+    int32_t* crow = p.view.chunk_row + (int64_t)u * p.view.max_chunks;
+    const int32_t* btr = p.kv.block_table + (int64_t)b * stride;
+    for (int c00 = c0; c00 < c1; c00 += nt * 8) {
+        int page[8], phys[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = c00 + e * nt + t;
+            page[e] = c < c1 ? __ldcg(selp + c) : -1;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) phys[e] = (page[e] >= 0 && page[e] < stride) ? btr[page[e]] : -1;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = c00 + e * nt + t;
+            if (c < c1) {
+                if (phys[e] >= 0 && phys[e] < p.kv.num_pages) {
+                    crow[c] = (phys[e] * H + h) * kPage;
+                } else {
+                    crow[c] = -1;
+                    flag(p.status, SE_DEV_BAD_INDEX);
+                }
+            }
+        }
+    }
+}
+
 // Q- / Q+ of sequence b per (KV head, d) for the page bound, into coef (shared
 // memory): U[p] = sum_d Q-[d] kmin[p,d] + Q+[d] kmax[p,d] with Q+ = sum_g
 // max(q_g, 0) and Q- = sum_g min(q_g, 0) (kmin <= kmax picks the larger
@@ -381,7 +436,7 @@ __device__ __forceinline__ void score_stage(const StepParams& p, const uint8_t* 
     constexpr int kLps = kU4 / 4;                         // lanes per summary
     constexpr int kR = 32 / kLps;                         // summaries per warp-wide read
     constexpr int kSum = 2 * D * 2;
-    const int H = p.kv.num_kv_heads, stride = p.kv.max_pages_per_seq;
+    const int H = p.kv.num_kv_heads;
     const int sub = lane % kLps, slot = lane / kLps;
     for (int r = 0; r < nsum; r += kR) {
         const int tl = r + slot;
@@ -409,140 +464,168 @@ __device__ __forceinline__ void score_stage(const StepParams& p, const uint8_t* 
 #pragma unroll
         for (int o = kLps / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
         if (sub == 0 && tl < nsum)
-            p.keys[((int64_t)b * H + h) * stride + p0 + pl] = float_key(acc);
+            p.keys[((int64_t)b * H + h) * p.kstride + p0 + pl] = float_key(acc);
     }
 }
 
-// Plans, the same in every CTA, computed by one consumer warp each.
-//
-// Score slices: every sequence's candidate pages are cut into slices of P
-// pages (the last one shorter), P = the option, else about the candidates over
-// the grid, raised until the slices fit kMaxScoreItems rounds of the grid;
-// slice t (in sequence order) is run by CTA t % grid.  Writes this CTA's
-// slices (b, first page, end page) and returns their count.
-__device__ int plan_score(const StepParams& p, const int2* sseq, int lane, int4* items) {
+// Plans, the same in every CTA, each computed by one warp.  Group g holds
+// sequences [g*batch/groups, (g+1)*batch/groups).
+__device__ __forceinline__ int group_begin(const StepParams& p, int groups, int g) {
+    return (int)((long long)g * p.batch / groups);
+}
+
+// The schedule's mode: when no unit has more than kAreaKeys candidate pages,
+// the `groups` groups are used and a unit's top-k holds its keys in the union
+// area of shared memory (the stage ring keeps streaming meanwhile); else one
+// group, and the top-k holds them in the idle stage ring.  Returns the groups;
+// *in_area the mode.
+__device__ int step_mode(const StepParams& p, const int2* sseq, int lane, int* in_area) {
+    const int cap = p.kv.max_pages_per_seq * kPage;
+    const bool pending = p.k_new != nullptr;
+    int mx = 0;
+#pragma unroll 1
+    for (int b = lane; b < p.batch; b += 32) {
+        const int2 x = sseq[b];
+        mx = max(mx, seq_vals(x.x, x.y, cap, pending).m);
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    *in_area = mx <= kAreaKeys;
+    return mx <= kAreaKeys ? p.groups : 1;
+}
+
+// Score slices: in each group, every sequence's candidate pages are cut into
+// slices of P pages (the last one shorter), P = the option, else about the
+// group's candidates over the grid, doubled until the slices fit
+// kMaxScoreItems / groups rounds of the grid; slice t of a group (in sequence
+// order) is run by CTA t % grid.  Writes this CTA's slices (b, first page, end
+// page), group by group, and returns their count.
+__device__ int plan_score(const StepParams& p, const int2* sseq, int groups, int lane,
+                          int4* items, int* per_group) {
     const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
     const int cap = p.kv.max_pages_per_seq * kPage;
     const bool pending = p.k_new != nullptr;
+    const int per_cta = kMaxScoreItems / groups;
     auto m_of = [&](int b) {
         const int2 x = sseq[b];
         return seq_vals(x.x, x.y, cap, pending).m;
     };
-    long long M = 0;
+    int cnt = 0;
 #pragma unroll 1
-    for (int base = 0; base < p.batch; base += 32)
-        M += __reduce_add_sync(0xffffffffu, base + lane < p.batch ? m_of(base + lane) : 0);
-    if (M == 0) return 0;
-    int P = p.item_pages > 0 ? p.item_pages
-                             : max(kMinItemPages, (int)((M + grid - 1) / grid));
-    int total = 0;
+    for (int g = 0; g < groups; ++g) {
+        const int b0 = group_begin(p, groups, g), b1 = group_begin(p, groups, g + 1);
+        long long M = 0;
 #pragma unroll 1
-    for (int iter = 0; iter < 16; ++iter) {
-        total = 0;
+        for (int base = b0; base < b1; base += 32)
+            M += __reduce_add_sync(0xffffffffu, base + lane < b1 ? m_of(base + lane) : 0);
+        if (lane == 0) per_group[g] = 0;
+        if (M == 0) continue;
+        int P = p.item_pages > 0 ? p.item_pages : max(kMinItemPages, (int)((M + grid - 1) / grid));
 #pragma unroll 1
-        for (int base = 0; base < p.batch; base += 32) {
-            const int b = base + lane;
-            const int m = b < p.batch ? m_of(b) : 0;
-            total += __reduce_add_sync(0xffffffffu, (m + P - 1) / P);
-        }
-        if (total <= grid * kMaxScoreItems) break;
-        P *= 2;
-    }
-    int cnt = 0, run = 0;
+        for (int iter = 0; iter < 24; ++iter) {
+            int total = 0;
 #pragma unroll 1
-    for (int base = 0; base < p.batch; base += 32) {
-        const int b = base + lane;
-        const int m = b < p.batch ? m_of(b) : 0;
-        const int ni = (m + P - 1) / P;
-        int x = ni;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        const int off = run + x - ni;
-        // this CTA's slices c, c + grid, ... that fall in sequence b
-        for (int t = c; t < off + ni; t += grid) {
-            if (t >= off) {
-                const int j = (t - c) / grid;            // slot in this CTA's list
-                const int k = t - off;
-                if (j < kMaxScoreItems)
-                    items[j] = make_int4(b, k * P, min(m, (k + 1) * P), 0);
+            for (int base = b0; base < b1; base += 32) {
+                const int m = base + lane < b1 ? m_of(base + lane) : 0;
+                total += __reduce_add_sync(0xffffffffu, (m + P - 1) / P);
             }
+            if (total <= grid * per_cta) break;
+            P *= 2;
         }
-        run += __shfl_sync(0xffffffffu, x, 31);
+        int run = 0;
+#pragma unroll 1
+        for (int base = b0; base < b1; base += 32) {
+            const int b = base + lane;
+            const int m = b < b1 ? m_of(b) : 0;
+            const int ni = (m + P - 1) / P;
+            const int off = run + warp_excl_scan(ni, lane);
+            // this CTA's slices c, c + grid, ... that fall in sequence b
+            for (int t = c; t < off + ni; t += grid) {
+                if (t >= off && (t - c) / grid < per_cta) {
+                    const int k = t - off;
+                    items[cnt + (t - c) / grid] = make_int4(b, k * P, min(m, (k + 1) * P), 0);
+                }
+            }
+            run += __reduce_add_sync(0xffffffffu, ni);
+        }
+        const int mine = min(per_cta, run > c ? (run - c + grid - 1) / grid : 0);
+        if (lane == 0) per_group[g] = mine;
+        cnt += mine;
     }
-    cnt = run > c ? (run - c + grid - 1) / grid : 0;
-    return min(cnt, kMaxScoreItems);
+    return cnt;
 }
 
-// Decode pieces: unit u gets pieces_u = max(1, min(max_splits, nc_u,
-// floor(nc_u * share / total))) pieces of nc_u * k / pieces_u chunks, share
-// lowered from slots = grid * ceil(units / grid) until the pieces fit the
-// slots; piece t (in unit order) is run by CTA t % grid.  Writes this CTA's
-// pieces (unit, first chunk, end chunk, partial slot or -1), their units'
-// (first piece, pieces) and returns their count.
-__device__ int plan_decode(const StepParams& p, const int2* sseq, int lane, int4* items,
-                           int2* uitems) {
+// Decode pieces: in each group, unit u gets pieces_u = max(1, min(max_splits,
+// nc_u, floor(nc_u * share / total))) pieces of nc_u * k / pieces_u chunks,
+// share lowered from slots = grid * ceil(units / grid) until the pieces fit the
+// slots; piece t of a group (in unit order) is run by CTA t % grid and owns the
+// partial slot base + t.  Writes this CTA's pieces (unit, first chunk, end
+// chunk, partial slot or -1) and their units' (first slot, pieces), group by
+// group, and returns their count.
+__device__ int plan_decode(const StepParams& p, const int2* sseq, int groups, int lane,
+                           int4* items, int2* uitems, int* per_group) {
     const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    const int H = p.kv.num_kv_heads, units = p.units;
+    const int H = p.kv.num_kv_heads;
     const int cap = p.kv.max_pages_per_seq * kPage;
     const bool pending = p.k_new != nullptr;
+    const int per_cta = kMaxPieces / groups;
     auto nc_of = [&](int u) {
         const int2 x = sseq[u / H];
         return seq_vals(x.x, x.y, cap, pending).chunks;
     };
-    int total = 0;
+    int cnt = 0, base_slot = 0;
 #pragma unroll 1
-    for (int base = 0; base < units; base += 32)
-        total += __reduce_add_sync(0xffffffffu, base + lane < units ? nc_of(base + lane) : 0);
-    const int tot = max(1, total);
-    const int slots = grid * ((units + grid - 1) / grid);
-    auto pieces_of = [&](int nc, int share) {
-        return nc == 0 ? 1
-                       : max(1, min(p.max_splits, min(nc, (int)((long long)nc * share / tot))));
-    };
-    int share = slots, run = 0;
+    for (int g = 0; g < groups; ++g) {
+        const int u0 = group_begin(p, groups, g) * H, u1 = group_begin(p, groups, g + 1) * H;
+        const int units = u1 - u0;
+        if (lane == 0) per_group[g] = 0;
+        if (units == 0) continue;
+        int total = 0;
 #pragma unroll 1
-    for (int iter = 0; iter < 6; ++iter) {
-        run = 0;
+        for (int base = u0; base < u1; base += 32)
+            total += __reduce_add_sync(0xffffffffu, base + lane < u1 ? nc_of(base + lane) : 0);
+        const int tot = max(1, total);
+        const int slots = grid * ((units + grid - 1) / grid);
+        auto pieces_of = [&](int nc, int share) {
+            return nc == 0 ? 1
+                           : max(1, min(p.max_splits, min(nc, (int)((long long)nc * share / tot))));
+        };
+        int share = slots, run = 0;
 #pragma unroll 1
-        for (int base = 0; base < units; base += 32) {
-            const int u = base + lane;
-            const int pc = u < units ? pieces_of(nc_of(u), share) : 0;
-            int x = pc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            const int off = run + x - pc;
-            if (u < units) {
-                for (int t = c; t < off + pc; t += grid) {
-                    if (t >= off) {
-                        const int j = (t - c) / grid;
-                        const int k = t - off, nc = nc_of(u);
-                        if (j < kMaxPieces) {
+        for (int iter = 0; iter < 6; ++iter) {
+            run = 0;
+#pragma unroll 1
+            for (int base = u0; base < u1; base += 32) {
+                const int u = base + lane;
+                const int nc = u < u1 ? nc_of(u) : 0;
+                const int pc = u < u1 ? pieces_of(nc, share) : 0;
+                const int off = run + warp_excl_scan(pc, lane);
+                if (u < u1) {
+                    for (int t = c; t < off + pc; t += grid) {
+                        if (t >= off && (t - c) / grid < per_cta) {
+                            const int j = cnt + (t - c) / grid, k = t - off;
                             items[j] = make_int4(u, (int)((long long)nc * k / pc),
                                                  (int)((long long)nc * (k + 1) / pc),
-                                                 pc == 1 ? -1 : t);
-                            uitems[j] = make_int2(off, pc);
+                                                 pc == 1 ? -1 : base_slot + t);
+                            uitems[j] = make_int2(base_slot + off, pc);
                         }
                     }
                 }
+                run += __reduce_add_sync(0xffffffffu, pc);
             }
-            run += __shfl_sync(0xffffffffu, x, 31);
+            __syncwarp();
+            if (run <= slots || share == 0) break;        // share 0: one piece per unit
+            share = iter == 4 ? 0 : max(0, share - (run - slots));
         }
-        __syncwarp();
-        if (run <= slots || share == 0) break;            // share 0: one piece per unit
-        share = iter == 4 ? 0 : max(0, share - (run - slots));
+        const int mine = min(per_cta, run > c ? (run - c + grid - 1) / grid : 0);
+        if (lane == 0) per_group[g] = mine;
+        cnt += mine;
+        base_slot += run;
     }
-    const int cnt = run > c ? (run - c + grid - 1) / grid : 0;
-    return min(cnt, kMaxPieces);
+    return cnt;
 }
 
 template <int D, int NT, bool TWO_TERM>
-__global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
+__global__ void __launch_bounds__(kStepThreads, 2)
     quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                       const StepParams p) {
     using S = DecShape<D, NT>;
@@ -554,16 +637,21 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
     uint8_t* ring = base;
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + NS * SS::kStageBytes);
     uint64_t* empty = full + NS;
-    int* stage_ntok = reinterpret_cast<int*>(empty + NS);
+    uint64_t* planbar = empty + NS;                            // [0] slices, [1] pieces
+    uint64_t* pready = planbar + 2;                            // [kMaxPieces] view rows written
+    int* stage_ntok = reinterpret_cast<int*>(pready + kMaxPieces);
     int* misc = stage_ntok + NS;                               // 64 ints
     volatile int* abort_flag = misc;                           // [0]
     // [1] last-piece flag of the merge, [3] last CTA, [4] score slices,
-    // [5] pieces
+    // [5] pieces, [6] top-k in the union area, [8..12) slices per group,
+    // [12..16) pieces per group
     int4* pitem = reinterpret_cast<int4*>(misc + 64);          // [kMaxPieces]
-    int4* pseq = pitem + kMaxPieces;                           // [kMaxPieces] held, ctx, n, k
-    int2* puit = reinterpret_cast<int2*>(pseq + kMaxPieces);   // [kMaxPieces]
+    int2* pseq = reinterpret_cast<int2*>(pitem + kMaxPieces);  // [kMaxPieces] held, budget
+    int2* puit = pseq + kMaxPieces;                            // [kMaxPieces]
     int4* sitem = reinterpret_cast<int4*>(puit + kMaxPieces);  // [kMaxScoreItems]
-    uint8_t* uni = base + p.off_union;                         // staging, then coef, then merge
+    // the union area, in turn: the staged lengths, the query coefficients
+    // and the top-k (which never overlap), then the decode merge
+    uint8_t* uni = base + p.off_union;
     int2* sseq = reinterpret_cast<int2*>(uni);                 // [batch] (ctx_len, budget)
     float* coef = reinterpret_cast<float*>(uni);               // [H][2][D]
     float* merge = reinterpret_cast<float*>(uni);
@@ -572,11 +660,15 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
     const int H = p.kv.num_kv_heads, stride = p.kv.max_pages_per_seq;
     const int cap = stride * kPage;
     const bool pending = p.k_new != nullptr;
+    const int segs = D / 8;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(&planbar[0], 1);
+        mbar_init(&planbar[1], 1);
+        for (int j = 0; j < kMaxPieces; ++j) mbar_init(&pready[j], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -590,30 +682,21 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
         }
     }
     __syncthreads();
-    if (warp == 0) {
-        const int n = plan_score(p, sseq, lane, sitem);
-        if (lane == 0) misc[4] = n;
-    } else if (warp == 1) {
-        const int n = plan_decode(p, sseq, lane, pitem, puit);
-        __syncwarp();
-        for (int j = lane; j < n; j += 32) {
-            const int2 x = sseq[pitem[j].x / H];
-            const SeqVals s = seq_vals(x.x, x.y, cap, pending);
-            pseq[j] = make_int4(s.held, x.y, 0, 0);
-        }
-        if (lane == 0) misc[5] = n;
-    }
-    __syncthreads();
-    const int nscore = misc[4], npieces = misc[5];
+    auto plan_wait = [&](int i) {
+        if (!*abort_flag && !mbar_wait(&planbar[i], 0, abort_flag)) give_up(p, abort_flag);
+    };
 
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
+            plan_wait(0);
         }
+        __syncwarp();
+        const int nscore = *abort_flag ? 0 : misc[4];
         uint32_t seq = 0;
-        // 1. the score slices: each one contiguous block of summaries, 1-D bulk copies
+        // the score slices: each one contiguous block of summaries, 1-D bulk copies
         for (int i = 0; i < nscore; ++i) {
             const int4 it = sitem[i];
             const int64_t bytes = (int64_t)(it.z - it.y) * H * SS::kSumBytes;
@@ -639,15 +722,19 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
             }
             seq += nst;
         }
-        // 2. the decode pieces: the consumers first select and write the
-        // piece's view rows (and the new row), then release the producer
+        // the decode pieces, each once the consumers have written its view
+        // rows (and the new token's row)
+        if (lane == 0) plan_wait(1);
+        __syncwarp();
+        const int npieces = misc[5];
         const uint64_t kv_policy = l2_evict_first();
         for (int j = 0; j < npieces; ++j) {
-            producer_bar();
+            if (lane == 0 && !*abort_flag && !mbar_wait(&pready[j], 0, abort_flag))
+                give_up(p, abort_flag);
+            __syncwarp();
             const int4 it = pitem[j];
             const int u = it.x, c0 = it.y, c1 = it.z;
-            const SeqVals sv = seq_vals(pseq[j].x, pseq[j].y, cap, pending);
-            const int ntok = sv.tokens;
+            const int ntok = seq_vals(pseq[j].x, pseq[j].y, cap, pending).tokens;
             const int32_t* crow = p.view.chunk_row + (int64_t)u * p.view.max_chunks;
             int row_next = c0 + lane < c1 ? __ldcg(crow + c0 + lane) : -1;
             for (int cb = c0; cb < c1; cb += 32) {
@@ -670,7 +757,7 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
                         if (!*abort_flag && !mbar_wait(&empty[s], ((sq / NS) & 1) ^ 1, abort_flag))
                             give_up(p, abort_flag);
                         int cnt = min(kPage, ntok - c * kPage);
-                        if (row < 0 || (int64_t)row >= p.total_rows) {
+                        if (!*abort_flag && (row < 0 || (int64_t)row >= p.total_rows)) {
                             flag(p.status, SE_DEV_BAD_INDEX);
                             cnt = 0;
                         }
@@ -702,37 +789,117 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
     } else {
         // -------------------------------- consumers --------------------------------
         const int ctid = threadIdx.x;
+        // the plans: the score slices by warp 0, the pieces by warp 1; each
+        // published through its own mbarrier (release / acquire in the CTA)
+        if (warp == 0) {
+            int in_area = 0;
+            const int groups = step_mode(p, sseq, lane, &in_area);
+            const int n = plan_score(p, sseq, groups, lane, sitem, misc + 8);
+            __syncwarp();
+            if (lane == 0) {
+                misc[4] = n;
+                misc[6] = in_area;
+                mbar_arrive(&planbar[0]);
+            }
+        } else if (warp == 1) {
+            int in_area = 0;
+            const int groups = step_mode(p, sseq, lane, &in_area);
+            const int n = plan_decode(p, sseq, groups, lane, pitem, puit, misc + 12);
+            __syncwarp();
+            for (int j = lane; j < n; j += 32) pseq[j] = sseq[pitem[j].x / H];
+            __syncwarp();
+            if (lane == 0) {
+                misc[5] = n;
+                mbar_arrive(&planbar[1]);
+            }
+        }
+        if (lane == 0) {
+            plan_wait(0);
+            plan_wait(1);
+        }
+        __syncwarp();
+        consumer_bar();                                  // both plans seen before the first fold
+        const int nscore = *abort_flag ? 0 : misc[4];
+        const int npieces = misc[5];
+        const bool in_area = misc[6] != 0;
+        const int groups = in_area ? p.groups : 1;
         uint32_t seq = 0;
-        int folded = -1;
-        for (int i = 0; i < nscore; ++i) {
-            const int4 it = sitem[i];
-            const int b = it.x;
-            if (b != folded) {
-                consumer_bar();                          // the previous slice's reads of coef
-                step_fold<D>(p, b, coef, ctid);
-                consumer_bar();
-                folded = b;
-            }
-            const int nsum_all = (it.z - it.y) * H;
-            const int nst = (nsum_all + SS::kSumsPerStage - 1) / SS::kSumsPerStage;
-            for (int j = 0; j < nst; ++j, ++seq) {
-                if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
-                const int s = seq % NS;
-                if (lane == 0 && !*abort_flag && !mbar_wait(&full[s], (seq / NS) & 1, abort_flag))
-                    give_up(p, abort_flag);
-                __syncwarp();
-                if (!*abort_flag)
-                    score_stage<D>(p, ring + s * SS::kStageBytes,
-                                   min(SS::kSumsPerStage, nsum_all - j * SS::kSumsPerStage),
-                                   j * SS::kSumsPerStage, b, it.y, coef, lane);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-            // every key of the slice is written: publish the slice's pages
+        // the top-k of piece j (its ranks of the selection, its view rows, the
+        // new token's row), then the producer is released for it
+        auto select_piece = [&](int j, uint8_t* area) {
+            const int4 it = pitem[j];
+            const int u = it.x, c0 = it.y, c1 = it.z;
+            const int b = u / H, h = u % H;
+            const SeqVals sv = seq_vals(pseq[j].x, pseq[j].y, cap, pending);
+            const bool app = sv.room && c1 == sv.chunks;     // the piece of the last page
+            AppendRegs ar;
+            if (app && ctid < segs) append_load(p.kv, b, h, sv.held, p.k_new, p.v_new, ctid, ar);
+            const int phys_new = app ? p.kv.block_table[(int64_t)b * stride + sv.held / kPage] : -1;
             consumer_bar();
-            if (ctid == 0) {
-                __threadfence();
-                atomicAdd(p.seq_scored + b, it.z - it.y);
+            if (ctid == 0 && sv.m > 0 && !*abort_flag &&
+                !wait_count(p, p.seq_scored + b, sv.m, abort_flag))
+                give_up(p, abort_flag);
+            consumer_bar();
+            piece_select(p, u, sv, c0, c1, area, warp, lane);
+            consumer_bar();
+            view_rows(p, u, c0, c1, ctid, kCThreads);
+            if (c0 == 0 && ctid == 0) {
+                p.n_sel[u] = sv.chunks;
+                p.view.n_tokens[u] = sv.tokens;
+            }
+            if (app && ctid < segs) {
+                if (phys_new >= 0 && phys_new < p.kv.num_pages) {
+                    append_store(p.kv, b, h, sv.held, phys_new, ctid, ar);
+                    fence_proxy_async_global();              // read next by TMA (async proxy)
+                } else if (ctid == 0) {
+                    flag(p.status, SE_DEV_BAD_INDEX);
+                }
+            }
+            consumer_bar();
+            if (ctid == 0) mbar_arrive(&pready[j]);
+        };
+        int si = 0, pj = 0, folded = -1;
+        for (int g = 0; g < groups; ++g) {
+            const int ns_g = misc[8 + g];
+            for (int k = 0; k < ns_g && si < nscore; ++k, ++si) {
+                const int4 it = sitem[si];
+                const int b = it.x;
+                if (b != folded) {
+                    consumer_bar();                      // the previous reads of the union area
+                    step_fold<D>(p, b, coef, ctid);
+                    consumer_bar();
+                    folded = b;
+                }
+                const int nsum_all = (it.z - it.y) * H;
+                const int nst = (nsum_all + SS::kSumsPerStage - 1) / SS::kSumsPerStage;
+                for (int j = 0; j < nst; ++j, ++seq) {
+                    if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
+                    const int s = seq % NS;
+                    if (lane == 0 && !*abort_flag && !mbar_wait(&full[s], (seq / NS) & 1, abort_flag))
+                        give_up(p, abort_flag);
+                    __syncwarp();
+                    if (!*abort_flag)
+                        score_stage<D>(p, ring + s * SS::kStageBytes,
+                                       min(SS::kSumsPerStage, nsum_all - j * SS::kSumsPerStage),
+                                       j * SS::kSumsPerStage, b, it.y, coef, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                }
+                // every key of the slice is written: publish the slice's pages
+                consumer_bar();
+                if (ctid == 0) {
+                    __threadfence();
+                    atomicAdd(p.seq_scored + b, it.z - it.y);
+                }
+            }
+            if (in_area) {
+                // this group's selections, while the producer streams the next
+                // group's summaries (or the first group's chunks) into the ring
+                const int np_g = misc[12 + g];
+                for (int k = 0; k < np_g && pj < npieces; ++k, ++pj) {
+                    folded = -1;                         // the union area is reused
+                    select_piece(pj, uni);
+                }
             }
         }
         DecOut dout;
@@ -744,56 +911,12 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
         dout.counters = p.counters;
         dout.Hq = p.Hq;
         dout.G = p.G;
-        const int segs = D / 8;
         for (int j = 0; j < npieces; ++j) {
+            // one group: the selection in the idle ring, right before the piece
+            if (!in_area) select_piece(j, ring);
             const int4 it = pitem[j];
             const int u = it.x, c0 = it.y, c1 = it.z;
             const int b = u / H, h = u % H;
-            const SeqVals sv = seq_vals(pseq[j].x, pseq[j].y, cap, pending);
-            const bool last_piece = c1 == sv.chunks;
-            const bool app = sv.room && last_piece;
-            AppendRegs ar;
-            if (app && ctid < segs) append_load(p.kv, b, h, sv.held, p.k_new, p.v_new, ctid, ar);
-            const int32_t* btr = p.kv.block_table + (int64_t)b * stride;
-            const int phys_new = app ? btr[sv.held / kPage] : -1;
-            // 1. wait until every candidate page of b is scored (bounded)
-            consumer_bar();                              // the ring is idle
-            if (ctid == 0 && sv.m > 0 && !*abort_flag &&
-                !wait_count(p, p.seq_scored + b, sv.m, abort_flag))
-                give_up(p, abort_flag);
-            consumer_bar();
-            // 2. this piece's ranks of the selection (garbage after an abort,
-            // through the same barriers)
-            piece_select(p, u, sv, c0, c1, ring, warp, lane);
-            consumer_bar();
-            // 3. its view rows: the physical chunk of each selected page
-            const int32_t* selp = p.sel_pages + (int64_t)u * stride;
-            int32_t* crow = p.view.chunk_row + (int64_t)u * p.view.max_chunks;
-            for (int c = c0 + ctid; c < c1; c += kCThreads) {
-                const int page = __ldcg(selp + c);
-                const int phys = (page >= 0 && page < stride) ? btr[page] : -1;
-                if (phys >= 0 && phys < p.kv.num_pages) {
-                    crow[c] = (phys * H + h) * kPage;
-                } else {
-                    crow[c] = -1;
-                    flag(p.status, SE_DEV_BAD_INDEX);
-                }
-            }
-            if (c0 == 0 && ctid == 0) {
-                p.n_sel[u] = sv.chunks;
-                p.view.n_tokens[u] = sv.tokens;
-            }
-            // 4. the new token's row, read next by this CTA's TMA (async proxy)
-            if (app && ctid < segs) {
-                if (phys_new >= 0 && phys_new < p.kv.num_pages) {
-                    append_store(p.kv, b, h, sv.held, phys_new, ctid, ar);
-                    fence_proxy_async_global();
-                } else if (ctid == 0) {
-                    flag(p.status, SE_DEV_BAD_INDEX);
-                }
-            }
-            producer_bar();                              // the producer may stream the piece
-            // 5. the decode of the piece's chunks
             DecState<D, NT> st;
             dec_begin<D, NT>(st, p.q, (int64_t)b * p.Hq + h * p.G, p.G, lane);
             for (int c = c0; c < c1; ++c, ++seq) {
@@ -808,7 +931,7 @@ __global__ void __launch_bounds__(kDecodeThreads, NT == 2 ? 2 : 0)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
-            consumer_bar();                              // the union area: coef -> merge
+            consumer_bar();                              // the union area -> merge
             dec_finish<D, NT>(st, merge, misc + 1, dout, b, h, u, it.w, puit[j], warp, lane);
         }
     }
@@ -867,6 +990,8 @@ size_t step_ctl_bytes() {
            a256((size_t)kStepMaxUnits * sizeof(int));
 }
 
+int key_stride(int max_pages) { return (max_pages + 3) & ~3; }
+
 StepWs step_ws_carve(void* ws, int batch, int H, int G, int max_pages, int max_splits) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     const size_t units = (size_t)batch * H, slots = units * max_splits;
@@ -880,7 +1005,7 @@ StepWs step_ws_carve(void* ws, int batch, int H, int G, int max_pages, int max_s
     w.counters = reinterpret_cast<int*>(base + off);
     off += a256((size_t)kStepMaxUnits * sizeof(int));
     w.keys = reinterpret_cast<uint32_t*>(base + off);
-    off += a256(units * max_pages * sizeof(uint32_t));
+    off += a256(units * key_stride(max_pages) * sizeof(uint32_t));
     w.lse_part = reinterpret_cast<float*>(base + off);
     off += a256(slots * G * sizeof(float));
     w.o_part = reinterpret_cast<float*>(base + off);
@@ -891,34 +1016,33 @@ StepWs step_ws_carve(void* ws, int batch, int H, int G, int max_pages, int max_s
 // (the sequences' staged lengths and budgets, then the query coefficients,
 // then the decode merge area).
 template <int D, int NT>
-size_t step_smem(int batch, int H, int* off_union, int* ring_bytes) {
+size_t step_smem(int batch, int H, int* off_union) {
     using SS = StepShape<D, NT>;
     const size_t ring = (size_t)SS::kStages * SS::kStageBytes;
-    const size_t uni_off = ring + SS::kFixed;
+    const size_t uni_off = (ring + SS::kFixed + 15) & ~static_cast<size_t>(15);
     const size_t uni = std::max({(size_t)DecShape<D, NT>::kMergeFloats * 4, (size_t)H * 2 * D * 4,
-                                 (size_t)batch * 8});
-    if (off_union) *off_union = static_cast<int>((uni_off + 15) & ~static_cast<size_t>(15));
-    if (ring_bytes) *ring_bytes = static_cast<int>(ring);
-    return 1024 + ((uni_off + 15) & ~static_cast<size_t>(15)) + uni;
+                                 (size_t)batch * 8, (size_t)kAreaBytes});
+    if (off_union) *off_union = static_cast<int>(uni_off);
+    return 1024 + uni_off + uni;
 }
 
 template <int D, int NT, bool TWO>
 cudaError_t run_step(const CUtensorMap& tk, const CUtensorMap& tv, StepParams p, cudaStream_t s) {
     auto kern = quest_step_kernel<D, NT, TWO>;
-    const size_t smem = step_smem<D, NT>(p.batch, p.kv.num_kv_heads, &p.off_union, &p.ring_bytes);
+    const size_t smem = step_smem<D, NT>(p.batch, p.kv.num_kv_heads, &p.off_union);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStepThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int grid = std::min(2048, num_sms() * per_sm);
-    // the pieces of a CTA must fit its list: ceil(units / grid) <= kMaxPieces
-    if ((p.units + grid - 1) / grid > kMaxPieces) return cudaErrorInvalidConfiguration;
+    // the pieces of a CTA must fit its list: groups * ceil(units / grid) <= kMaxPieces
+    if (p.groups * ((p.units + grid - 1) / grid) > kMaxPieces) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.blockDim = dim3(kStepThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -934,29 +1058,28 @@ cudaError_t run_step(const CUtensorMap& tk, const CUtensorMap& tv, StepParams p,
 size_t quest_step_ws_bytes(int batch, int H, int G, int D, int max_pages, int max_splits) {
     (void)D;
     const size_t units = (size_t)batch * H, slots = units * max_splits;
-    return step_ctl_bytes() + a256(units * max_pages * sizeof(uint32_t)) +
+    return step_ctl_bytes() + a256(units * key_stride(max_pages) * sizeof(uint32_t)) +
            a256(slots * G * sizeof(float)) + a256(slots * G * (size_t)D * sizeof(float));
 }
 
 size_t quest_step_smem_bytes(int batch, int H, int D, int G) {
     const int NT = G > 8 ? 2 : 1;
-    if (D == 64) return NT == 1 ? step_smem<64, 1>(batch, H, nullptr, nullptr)
-                                : step_smem<64, 2>(batch, H, nullptr, nullptr);
-    return NT == 1 ? step_smem<128, 1>(batch, H, nullptr, nullptr)
-                   : step_smem<128, 2>(batch, H, nullptr, nullptr);
+    if (D == 64) return NT == 1 ? step_smem<64, 1>(batch, H, nullptr)
+                                : step_smem<64, 2>(batch, H, nullptr);
+    return NT == 1 ? step_smem<128, 1>(batch, H, nullptr) : step_smem<128, 2>(batch, H, nullptr);
 }
 
 size_t quest_step_ring_bytes(int D, int G) {
-    const int NT = G > 8 ? 2 : 1;
     if (D == 64) return (size_t)StepShape<64, 1>::kStages * StepShape<64, 1>::kStageBytes;
-    return NT == 1 ? (size_t)StepShape<128, 1>::kStages * StepShape<128, 1>::kStageBytes
-                   : (size_t)StepShape<128, 2>::kStages * StepShape<128, 2>::kStageBytes;
+    return G > 8 ? (size_t)StepShape<128, 2>::kStages * StepShape<128, 2>::kStageBytes
+                 : (size_t)StepShape<128, 1>::kStages * StepShape<128, 1>::kStageBytes;
 }
 
 cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const void* v_new,
                               const void* q, int batch, int num_q_heads, const int32_t* budget,
                               float scale, int out_dtype, int max_splits, int item_pages,
-                              unsigned long long wait_ns, int32_t* sel_pages, int32_t* n_sel,
+                              int groups, unsigned long long wait_ns, int32_t* sel_pages,
+                              int32_t* n_sel,
                               const se_view& view, void* out, float* lse, void* ws,
                               cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t s) {
     const int H = kv.num_kv_heads, D = kv.head_dim, G = num_q_heads / H;
@@ -987,6 +1110,7 @@ cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const vo
     p.out_f32 = out_dtype == 1;
     p.lse_out = lse;
     p.keys = w.keys;
+    p.kstride = key_stride(kv.max_pages_per_seq);
     p.seq_scored = w.seq_scored;
     p.counters = w.counters;
     p.sync = w.sync;
@@ -994,8 +1118,8 @@ cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const vo
     p.lse_part = w.lse_part;
     p.max_splits = max_splits;
     p.item_pages = item_pages;
+    p.groups = std::max(1, std::min(groups > 0 ? groups : 1, std::min(kMaxGroups, batch)));
     p.off_union = 0;
-    p.ring_bytes = 0;
     p.total_rows = total_rows;
     p.wait_ns = wait_ns;
     p.status = w.status;

@@ -143,16 +143,16 @@ def test_one_kernel_step_matches_two_calls():
     view, lengths, cache rows and page summaries bit for bit, outputs within
     the rounding of their different split pieces; steps open new pages
     (contexts 15, 16, 31, 1000 and 2047 tokens at the start, one sequence with
-    every page selected), and the scoring slice size is varied from step to
-    step."""
+    every page selected), and the scoring slice size and the number of
+    sequence groups are varied from step to step."""
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name="quest_step_eq", batch=5, ctx=(15, 16, 31, 1000, 2047),
                      budget=(64, 64, 256, 128, U32), steps=12)
     inputs = synth.quest_inputs(w)
     a = QuestRun(w, inputs, mode="step", out_dtype=1)
     b = QuestRun(w, inputs, mode="fused", out_dtype=1)
-    knobs = [{}, {"slice_pages": 1}, {"slice_pages": 3}, {"slice_pages": 40},
-             {"slice_pages": 7}, {"slice_pages": 2}]
+    knobs = [{}, {"slice_pages": 1}, {"slice_pages": 3, "groups": 1}, {"slice_pages": 40},
+             {"slice_pages": 7, "groups": 3}, {"slice_pages": 2, "groups": 4}, {"groups": 1}]
     for s in range(w.steps):
         a.step_tuning = knobs[s % len(knobs)]
         a.step(s)
