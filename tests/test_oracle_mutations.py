@@ -150,3 +150,33 @@ def test_widen_mutations_are_caught(monkeypatch, bad):
     caught = any(fails(T_bf16.test_explicit_bit_patterns, b, v) for b, v in T_bf16.CASES) or \
         fails(T_bf16.test_matches_torch_bfloat16_on_random_patterns)
     assert caught
+
+
+def test_omnikv_mutations_are_caught(monkeypatch):
+    import oracle.omnikv as om
+    from tests import test_oracle_omnikv as T_om
+    good = om.omnikv_layers
+
+    def attends_filter_kv(qs, ks, vs, filters, budget, scale):     # the filter layer's K/V reused too
+        res = good(qs, ks, vs, filters, budget, scale)
+        out = []
+        for layer, (pages, _, _) in enumerate(res):
+            f = om.source_layer(layer, filters)
+            tok = om.selected_tokens(pages, len(ks[0]))
+            o, l = om.attend(qs[layer], np.asarray(ks[f])[tok], np.asarray(vs[f])[tok], scale)
+            out.append((pages, o, l))
+        return out
+
+    def own_selection(qs, ks, vs, filters, budget, scale):         # no reuse
+        return good(qs, ks, vs, tuple(range(len(qs))), budget, scale)
+
+    def first_filter(qs, ks, vs, filters, budget, scale):          # always layer 0's decision
+        return good(qs, ks, vs, (0,), budget, scale)
+
+    for bad, pins in ((attends_filter_kv, [(T_om.test_full_budget_is_dense_attention_per_layer, 0)]),
+                      (own_selection, [(T_om.test_reuse_takes_the_filter_layers_pages_not_the_layers_own,)]),
+                      (first_filter, [(T_om.test_every_layer_a_filter_is_per_layer_quest,),
+                                      (T_om.test_reuse_takes_the_filter_layers_pages_not_the_layers_own,)])):
+        monkeypatch.setattr(T_om, "omnikv_layers", bad)
+        assert any(fails(fn, *args) for fn, *args in pins), bad.__name__
+    monkeypatch.setattr(T_om, "omnikv_layers", good)
