@@ -209,7 +209,9 @@ int se_page_meta_build(const se_paged_kv* kv, int batch,
  * at position ctx_len[b], folds the key into its page's min/max (a page's first
  * token sets both), then increments ctx_len[b].  block_table[b][ctx_len[b]/16]
  * must name a page; past max_pages_per_seq: SE_DEV_CAPACITY, token dropped.
- * Workspace: se_small_workspace(). */
+ * kv->meta may be NULL: the rows are written and no summary is kept (a layer
+ * that attends through the pages another layer selects, as in cross-layer
+ * selection reuse; see se_sparse_decode).  Workspace: se_small_workspace(). */
 int se_kv_append(const se_paged_kv* kv, const void* k_new, const void* v_new, int batch,
                  void* ws, size_t ws_bytes, se_stream_t stream);
 
@@ -267,6 +269,13 @@ int se_view_from_segments(const se_varlen_kv* kv, int batch, const se_view* view
  * out bf16 or fp32 [batch][num_q_heads][head_dim]; lse fp32 [batch][num_q_heads] or NULL.
  * A chunk row outside [0, total_rows) sets SE_DEV_BAD_INDEX and counts as empty.
  * view->max_chunks <= 2^20 (16M tokens per unit), else SE_ERR_UNSUPPORTED.
+ * Cross-layer selection reuse ([tokendh] "把边界划在'生命周期'上": OmniKV decides
+ * in some layers which history matters and later layers reuse that decision):
+ * the view holds row numbers of a row-addressed base, and caches that share one
+ * paging (the layers of a model with one block table) share row numbers, so
+ * the view a filter layer's se_quest_select filled may be passed with another
+ * layer's k_rows/v_rows and q: that layer attends over its own keys and values
+ * of the same pages, with no selection of its own.
  * Workspace: se_sparse_decode_workspace(num_units, G, head_dim, max_splits),
  * zero-filled before its first use: it holds the arrival counters of split
  * units, which every call leaves at zero (clear it again after a call that set

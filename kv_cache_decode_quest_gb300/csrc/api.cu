@@ -146,7 +146,7 @@ int se_page_meta_build(const se_paged_kv* kv, int batch, void* ws, size_t ws_byt
 
 int se_kv_append(const se_paged_kv* kv, const void* k_new, const void* v_new, int batch, void* ws,
                  size_t ws_bytes, se_stream_t stream) {
-    int rc = check_paged(kv, true);
+    int rc = check_paged(kv, false);
     if (rc) return rc;
     if (batch < 0 || (batch > 0 && (!k_new || !v_new))) return SE_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SE_ERR_INVALID_ARG;

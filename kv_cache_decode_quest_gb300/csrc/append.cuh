@@ -1,7 +1,8 @@
 // One KV head's share of a decode-step append into the paged cache: the new
 // key/value row at position `pos` of sequence b (physical page `phys`, slot
-// pos % 16) and the key folded into that page's channel-wise min/max summary,
-// the page's first token setting both (Quest's page summary kept beside the
+// pos % 16) and, when the cache keeps page summaries (meta not null), the key
+// folded into that page's channel-wise min/max summary, the page's first
+// token setting both (Quest's page summary kept beside the
 // full history: tokendh.com article on SparseEngine, section
 // "历史太长,会撑爆什么").  Threads t = 0..nt-1 share the head_dim/8 vectors.
 #pragma once
@@ -44,7 +45,7 @@ __device__ __forceinline__ void append_load(const se_paged_kv& kv, int b, int h,
     const int64_t m0 = (((int64_t)b * kv.max_pages_per_seq + p) * H + h) * 2;
     r.k = k_new[((int64_t)b * H + h) * segs + sg];
     r.v = v_new[((int64_t)b * H + h) * segs + sg];
-    if (slot != 0) {
+    if (slot != 0 && M != nullptr) {
         r.mn = M[m0 * segs + sg];
         r.mx = M[(m0 + 1) * segs + sg];
     }
@@ -60,6 +61,7 @@ __device__ __forceinline__ void append_store(const se_paged_kv& kv, int b, int h
     const int64_t m0 = (((int64_t)b * kv.max_pages_per_seq + p) * H + h) * 2;
     K[row * segs + sg] = r.k;
     V[row * segs + sg] = r.v;
+    if (M == nullptr) return;                 // a cache kept without page summaries
     if (slot == 0) {
         M[m0 * segs + sg] = r.k;
         M[(m0 + 1) * segs + sg] = r.k;

@@ -184,6 +184,34 @@ class H2OWorkload:
     seed: int = 0
 
 
+@dataclasses.dataclass(frozen=True)
+class OmniKVWorkload:
+    """Multi-layer Quest decode with cross-layer selection reuse: the filter
+    layers select pages with Quest; every other layer attends through the
+    selection of the latest filter layer before it.  Every layer has its own
+    K, V and queries (drawn like a QuestWorkload of the same shape), and all
+    layers share one paging of the cache."""
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    ctx: tuple
+    budget: tuple
+    steps: int
+    outliers: bool
+    layers: int
+    filters: tuple        # filter layers, sorted, containing 0
+    max_splits: int = 64
+    seed: int = 0
+
+    def layer(self, layer: int) -> QuestWorkload:
+        """Layer ``layer``'s tensors as a QuestWorkload (its own sub-streams)."""
+        return QuestWorkload(f"{self.name}/L{layer}", self.batch, self.num_q_heads,
+                             self.num_kv_heads, self.head_dim, self.ctx, self.budget, self.steps,
+                             self.outliers, self.max_splits, self.seed)
+
+
 UNBOUNDED_BUDGET = 2 ** 31 - 1
 
 
@@ -193,7 +221,8 @@ def _ragged_ctx(seed, batch, lo, hi):
 
 
 def workloads(seed: int = 0) -> dict:
-    """The five synthetic workloads, keyed by name."""
+    """The synthetic workloads, keyed by name: the five of the hot path and the
+    multi-layer cross-layer reuse workload."""
     ragged = _ragged_ctx(seed, 8, 65536, 131072)
     return {
         "tiny_quest": QuestWorkload(
@@ -208,6 +237,10 @@ def workloads(seed: int = 0) -> dict:
         "h2o_16k": H2OWorkload(
             "h2o_16k", batch=64, num_q_heads=32, num_kv_heads=4, head_dim=128,
             ctx=16384, budget=4096, recent=256, window=32, steps=256, seed=seed),
+        "omnikv_32k": OmniKVWorkload(
+            "omnikv_32k", batch=16, num_q_heads=32, num_kv_heads=4, head_dim=128,
+            ctx=(32768,) * 16, budget=(2048,) * 16, steps=16, outliers=True, layers=4,
+            filters=(0,), seed=seed),
         "ragged_quest_128k": QuestWorkload(
             "ragged_quest_128k", batch=8, num_q_heads=32, num_kv_heads=4, head_dim=128,
             ctx=ragged,
@@ -295,3 +328,8 @@ def h2o_inputs(w: H2OWorkload) -> dict:
 def scaled(w, **changes):
     """A copy of workload ``w`` with some fields replaced (smaller test sizes)."""
     return dataclasses.replace(w, **changes)
+
+
+def omnikv_inputs(w: OmniKVWorkload) -> list:
+    """Per layer, the tensors of ``quest_inputs`` for that layer's sub-streams."""
+    return [quest_inputs(w.layer(layer)) for layer in range(w.layers)]

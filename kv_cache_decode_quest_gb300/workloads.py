@@ -155,15 +155,17 @@ class QuestRun:
 
     def algorithmic_bytes(self, ctx_now: np.ndarray) -> dict:
         """Bytes one step must move at least, given each sequence's length after
-        the append: page summaries of every candidate page (2*D*2 bytes per page
-        and KV head), K and V of every selected token (2*D*2 bytes per token and
-        KV head), q, the appended k/v, and the output."""
+        the append: page summaries of every candidate page of a sequence that is
+        not wholly selected (2*D*2 bytes per page and KV head), K and V of every
+        selected token (2*D*2 bytes per token and KV head), q, the appended k/v,
+        and the output."""
         D, Hkv, Hq = self.D, self.Hkv, self.Hq
         meta = sel = 0
         for b, L in enumerate(ctx_now):
             n = -(-int(L) // PAGE)
             k = max(1, min(self.w.budget[b], 2 ** 31 - 1) // PAGE)
-            meta += max(0, n - 1) * Hkv * 2 * D * 2
+            if n > k:                                  # every page selected: nothing scored
+                meta += (n - 1) * Hkv * 2 * D * 2
             if n <= k:
                 toks = int(L)
             else:
@@ -172,6 +174,108 @@ class QuestRun:
         outb = 4 if self.out_dtype == 1 else 2
         small = self.B * (Hq * D * 2 + 2 * Hkv * D * 2 + Hq * D * outb)
         return {"meta": meta, "kv": sel, "small": small, "total": meta + sel + small}
+
+
+class OmniRun:
+    """Cross-layer selection reuse over `layers` attention layers of one model:
+    every layer keeps its own paged K/V (one block table for all), the filter
+    layers keep page summaries and select with se_quest_select_append, the
+    other layers append with se_kv_append (no summaries) and every layer
+    decodes with se_sparse_decode through the view of the latest filter layer
+    at or before it."""
+
+    def __init__(self, w: synth.OmniKVWorkload, inputs: list, device="cuda", out_dtype: int = 0):
+        self.w = w
+        B, Hq, Hkv, D, S, L = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.steps, w.layers
+        self.B, self.Hq, self.Hkv, self.D, self.S, self.L = B, Hq, Hkv, D, S, L
+        self.G = Hq // Hkv
+        self.scale = 1.0 / math.sqrt(D)
+        self.out_dtype = out_dtype
+        self.filters = tuple(sorted(w.filters))
+        if not self.filters or self.filters[0] != 0:
+            raise ValueError("layer 0 must be a filter layer")
+        ctx = np.asarray(w.ctx, dtype=np.int64)
+        pages = -(-(ctx + S) // PAGE)
+        bt, num_pages = synth.block_table(w.seed, w.name + "/block_table", pages)
+        maxp = bt.shape[1]
+        units = B * Hkv
+        block_table = torch.from_numpy(bt).to(device)
+        self.kv, self.q, self.k_new, self.v_new = [], [], [], []
+        self.sel, self.n_sel, self.view, self.ws_sel = {}, {}, {}, {}
+        for layer in range(L):
+            inp = inputs[layer]
+            K, V = paged_layout(inp["k"], inp["v"], ctx, bt, num_pages, Hkv, D)
+            meta = (torch.zeros(B, maxp, Hkv, 2, D, dtype=torch.bfloat16, device=device)
+                    if layer in self.filters else None)
+            self.kv.append(se.PagedKV(k=to_dev_bf16(K, device), v=to_dev_bf16(V, device), meta=meta,
+                                      block_table=block_table,
+                                      ctx_len=torch.from_numpy(ctx.astype(np.int32)).to(device)))
+            del K, V
+            self.q.append(to_dev_bf16(np.asarray(inp["q"]), device))
+            kn = np.stack([np.stack([inp["k"][b][:, ctx[b] + s] for b in range(B)]) for s in range(S)])
+            vn = np.stack([np.stack([inp["v"][b][:, ctx[b] + s] for b in range(B)]) for s in range(S)])
+            self.k_new.append(to_dev_bf16(kn, device))
+            self.v_new.append(to_dev_bf16(vn, device))
+            if layer in self.filters:
+                self.sel[layer] = torch.zeros(units, maxp, dtype=torch.int32, device=device)
+                self.n_sel[layer] = torch.zeros(units, dtype=torch.int32, device=device)
+                self.view[layer] = se.View.empty(units, maxp, device)
+                self.ws_sel[layer] = se.workspace(se.se_quest_select_workspace(B, Hkv, maxp), device)
+        self.budget = torch.tensor([min(b, 2 ** 31 - 1) for b in w.budget], dtype=torch.int32,
+                                   device=device)
+        self.ws_small = se.workspace(se.se_small_workspace(), device)
+        self.ws_dec = se.workspace(se.se_sparse_decode_workspace(units, self.G, D, w.max_splits),
+                                   device)
+        odt = torch.float32 if out_dtype == 1 else torch.bfloat16
+        self.out = [torch.zeros(B, Hq, D, dtype=odt, device=device) for _ in range(L)]
+        self.lse = [torch.zeros(B, Hq, dtype=torch.float32, device=device) for _ in range(L)]
+        for layer in self.filters:
+            se.se_page_meta_build(self.kv[layer], B, self.ws_small)
+
+    def source(self, layer: int) -> int:
+        return max(f for f in self.filters if f <= layer)
+
+    def step(self, s: int, ev_begin=None, ev_end=None):
+        """One decode step through every layer, in layer order."""
+        for layer in range(self.L):
+            kv = self.kv[layer]
+            if layer in self.filters:
+                se.se_quest_select_append(kv, self.k_new[layer][s], self.v_new[layer][s],
+                                          self.q[layer][s], self.B, self.Hq, self.budget,
+                                          self.sel[layer], self.n_sel[layer], self.view[layer],
+                                          self.ws_sel[layer])
+            else:
+                se.se_kv_append(kv, self.k_new[layer][s], self.v_new[layer][s], self.B,
+                                self.ws_small)
+            timed = ev_begin is not None and layer == self.L - 1
+            se.se_sparse_decode(kv.k, kv.v, self.view[self.source(layer)], self.q[layer][s], self.B,
+                                self.Hq, self.Hkv, self.D, self.scale, self.out[layer],
+                                self.lse[layer], self.ws_dec, out_dtype=self.out_dtype,
+                                max_splits=self.w.max_splits, ev_begin=ev_begin if timed else None,
+                                ev_end=ev_end if timed else None)
+
+    def status(self) -> int:
+        st = se.status_word(self.ws_small) | se.status_word(self.ws_dec)
+        for ws in self.ws_sel.values():
+            st |= se.status_word(ws)
+        return st
+
+    def algorithmic_bytes(self, ctx_now: np.ndarray) -> dict:
+        """Bytes one step must move at least: the filter layers' page summaries
+        of every candidate page, every layer's K and V of the selected tokens,
+        and each layer's q, appended k/v and output."""
+        D, Hkv, Hq = self.D, self.Hkv, self.Hq
+        meta = kv = 0
+        for b, L in enumerate(ctx_now):
+            n = -(-int(L) // PAGE)
+            k = max(1, min(self.w.budget[b], 2 ** 31 - 1) // PAGE)
+            meta += max(0, n - 1) * Hkv * 2 * D * 2 if n > k else 0
+            toks = int(L) if n <= k else (k - 1) * PAGE + (int(L) - PAGE * (n - 1))
+            kv += toks * Hkv * 2 * D * 2
+        outb = 4 if self.out_dtype == 1 else 2
+        small = self.B * (Hq * D * 2 + 2 * Hkv * D * 2 + Hq * D * outb)
+        total = len(self.filters) * meta + self.L * (kv + small)
+        return {"meta": len(self.filters) * meta, "kv": self.L * kv, "total": total}
 
 
 class SnapKVRun:
