@@ -38,7 +38,7 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_quest_gb300", "csrc")
 # the Quest step as the bench runs it: "step" = append, select and decode in one
 # kernel (se_quest_step); "fused" = se_quest_select_append + se_sparse_decode
 HEADLINE_MODE = "fused"
-RAGGED_MODE = "fused"
+RAGGED_MODE = "step"
 # per mode: the dominant kernel, its source and its committed ncu traffic record
 KERNEL_OF_MODE = {
     "step": ("quest_step_kernel", os.path.join(CSRC, "quest_step.cu"), "quest_step_kernel_{}.json"),
@@ -171,7 +171,146 @@ def _oracle_worker(args):
     return done, time.perf_counter() - t0
 
 
-def cpu_baseline(name, seconds=12.0, cores=None):
+def cpu_model():
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu), or the machine type."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
+def _timed_calls(fn, seconds):
+    """Calls fn() until `seconds` have passed (at least once); returns calls/s."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            return n / dt, n
+
+
+def _oracle_rates_worker(seconds):
+    """Single-threaded oracle rates of one query of each workload (the oracle as
+    it stands; a bounded sample of each workload's queries)."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import oracle
+    from oracle.quest import selected_tokens
+    from kv_cache_decode_quest_gb300 import synth
+    W = synth.workloads()
+    out = {}
+
+    def quest_query(w, k, v, q, b, s):
+        G = w.num_q_heads // w.num_kv_heads
+        L = w.ctx[b] + s + 1
+        for h in range(w.num_kv_heads):
+            K, V = oracle.widen(k[h, :L]), oracle.widen(v[h, :L])
+            qg = oracle.widen(q[s, b, h * G:(h + 1) * G])
+            U = oracle.quest_bound(qg, *oracle.page_minmax(K))
+            pages = oracle.quest_select(U, oracle.quest_k_pages(min(w.budget[b], 2 ** 31 - 1)))
+            oracle.attend(qg, K[selected_tokens(pages, L)], V[selected_tokens(pages, L)],
+                          1 / math.sqrt(w.head_dim))
+
+    for name in ("tiny_quest", "quest_32k"):
+        w = W[name]
+        k, v = synth.quest_sequence(w, 0)
+        q = synth.quest_queries(w)
+        r, n = _timed_calls(lambda: quest_query(w, k, v, q, 0, 0), seconds)
+        out[name] = {"queries_per_s": round(r, 3), "queries": n}
+    w = W["ragged_quest_128k"]
+    seqs = {b: synth.quest_sequence(w, b) for b in (0, 1)}      # one dense, one sparse request
+    q = synth.quest_queries(w)
+    cyc = [0]
+
+    def ragged_query():
+        b = cyc[0] % 2
+        cyc[0] += 1
+        quest_query(w, *seqs[b], q, b, 0)
+    r, n = _timed_calls(ragged_query, seconds)
+    out["ragged_quest_128k"] = {"queries_per_s": round(r, 4), "queries": n,
+                                "sample": "alternating a full-budget and a 4096-budget request"}
+    # SnapKV: one (request, KV head) compaction, and one decode query
+    w = synth.scaled(W["snapkv_32k"], batch=1)
+    inp = synth.snapkv_inputs(w, 0)
+    G = w.num_q_heads // w.num_kv_heads
+    scale = 1 / math.sqrt(w.head_dim)
+
+    def compact_unit():
+        K, V = oracle.widen(inp["k"][0][0]), oracle.widen(inp["v"][0][0])
+        A = oracle.window_scores(oracle.widen(inp["q_win"][0][:, :G]), K, scale)
+        keep = oracle.keep_positions(A, w.ctx, w.window, w.keep, w.pool_kernel)
+        oracle.compact(K, V, keep)
+    r, n = _timed_calls(compact_unit, seconds)
+    units = W["snapkv_32k"].batch * w.num_kv_heads
+    out["snapkv_32k_compaction"] = {"batches_per_s": round(r / units, 5), "units_timed": n,
+                                    "sample": f"one (request, KV head) of the 8 x 32K batch, "
+                                              f"rate divided by its {units} units"}
+    kept = w.keep + w.window
+    K, V = oracle.widen(inp["k"][0][0][:kept]), oracle.widen(inp["v"][0][0][:kept])
+    qd = oracle.widen(inp["q_win"][0][0, :G])
+
+    def snap_decode():
+        for _ in range(w.num_kv_heads):
+            oracle.attend(qd, K, V, scale)
+    r, n = _timed_calls(snap_decode, seconds)
+    out["snapkv_32k_decode"] = {"queries_per_s": round(r, 3), "queries": n,
+                                "sample": f"{kept}-token attention per KV head"}
+    # H2O: one decode step of one request over its 4 KV heads
+    w = synth.scaled(W["h2o_16k"], batch=1)
+    hi = synth.h2o_inputs(w)
+    G = w.num_q_heads // w.num_kv_heads
+    scale = 1 / math.sqrt(w.head_dim)
+    st = oracle.h2o_init(oracle.widen(hi["q_win"][0][:, :G]), oracle.widen(hi["k"][0][0]),
+                         oracle.widen(hi["v"][0][0]), w.budget, w.recent, scale)
+    qn = oracle.widen(hi["q"][0, 0, :G])
+    kn, vn = oracle.widen(hi["k_new"][0, 0, 0]), oracle.widen(hi["v_new"][0, 0, 0])
+
+    def h2o_query():
+        for _ in range(w.num_kv_heads):
+            oracle.h2o_step(st, qn, kn, vn, w.ctx, w.budget, w.recent, scale)
+    r, n = _timed_calls(h2o_query, seconds)
+    out["h2o_16k"] = {"queries_per_s": round(r, 3), "queries": n}
+    # cross-layer reuse: one request through 4 layers
+    w = W["omnikv_32k"]
+    lay = [synth.quest_sequence(w.layer(x), 0) for x in range(w.layers)]
+    lq = [synth.quest_queries(w.layer(x)) for x in range(w.layers)]
+    G = w.num_q_heads // w.num_kv_heads
+    L = w.ctx[0] + 1
+
+    def omni_query():
+        for h in range(w.num_kv_heads):
+            oracle.omnikv_layers([oracle.widen(lq[x][0, 0, h * G:(h + 1) * G]) for x in range(w.layers)],
+                                 [oracle.widen(lay[x][0][h, :L]) for x in range(w.layers)],
+                                 [oracle.widen(lay[x][1][h, :L]) for x in range(w.layers)],
+                                 w.filters, w.budget[0], 1 / math.sqrt(w.head_dim))
+    r, n = _timed_calls(omni_query, seconds)
+    out["omnikv_32k"] = {"layer_queries_per_s": round(r * w.layers, 3), "queries": n}
+    return out
+
+
+def oracle_rates(seconds=2.0):
+    """Single-threaded oracle rates per workload, in one spawned process."""
+    import multiprocessing as mp
+    with mp.get_context("spawn").Pool(1) as pool:
+        return pool.apply(_oracle_rates_worker, (seconds,))
+
+
+def cpu_baseline(name, seconds=12.0, cores=None, single=None):
     import multiprocessing as mp
     cores = cores or max(1, os.cpu_count() or 1)
     from kv_cache_decode_quest_gb300 import synth
@@ -183,10 +322,14 @@ def cpu_baseline(name, seconds=12.0, cores=None):
     wall = time.perf_counter() - t0
     q = sum(r[0] for r in res)
     per_worker = [r[0] / r[1] for r in res]
-    return {"value": sum(per_worker), "unit": "queries/s", "cores": cores, "kind": "oracle",
+    line = {"value": sum(per_worker), "unit": "queries/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(), "nproc": os.cpu_count(),
             "sample": f"{q} oracle queries ({name}: page summaries, bound, top-k, fp64 "
                       f"attention per KV head), ~{seconds:.0f} s per core on {cores} "
                       f"single-threaded spawned workers, wall {wall:.1f} s"}
+    if single is not None:
+        line["single_core"] = {"value": single, "unit": "queries/s", "cores": 1}
+    return line
 
 
 # ---------------------------------------------------------------------------
@@ -439,8 +582,12 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
 
-    # oracle baseline first (spawned workers), rank 0 only
-    cpu = cpu_baseline(HEADLINE, seconds=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None
+    # oracle baselines first (spawned workers), rank 0 only: every workload's
+    # single-threaded oracle rate, then the headline's on all host cores
+    rates = oracle_rates(args.oracle_seconds) if (rank == 0 and args.oracle_seconds > 0) else {}
+    cpu = (cpu_baseline(HEADLINE, seconds=args.cpu_seconds,
+                        single=rates.get(HEADLINE, {}).get("queries_per_s"))
+           if (rank == 0 and args.cpu_seconds > 0) else None)
 
     peak, peak_kind = peaks()
     qb = QuestBench(HEADLINE, device, mode=HEADLINE_MODE)
@@ -469,6 +616,9 @@ def run_ours(args):
     extra = {}
     if args.extras:
         extra = run_extras(args, device, peak)
+        for key, val in extra.items():
+            if key in rates:
+                val["oracle_single_core"] = rates[key]
 
     if rank != 0:
         return
@@ -541,7 +691,7 @@ def timed_steps(step, K, W, flush, before=None):
     return [a.elapsed_time(b) for a, b, _, _ in evs], [c.elapsed_time(d) for _, _, c, d in evs]
 
 
-EXTRAS = ("ragged_quest_128k", "snapkv_32k", "h2o_16k")
+EXTRAS = ("tiny_quest", "ragged_quest_128k", "omnikv_32k", "snapkv_32k", "h2o_16k")
 
 
 def run_extras(args, device, peak, only=None):
@@ -550,9 +700,13 @@ def run_extras(args, device, peak, only=None):
     out = {}
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     want = set(EXTRAS if only is None else [only])
+    if "tiny_quest" in want:
+        tiny(out, device)
     # ragged 64K-128K Quest decode (half dense-equivalent), split-K up to 64
     if "ragged_quest_128k" in want:
         ragged(out, device, peak)
+    if "omnikv_32k" in want:
+        omnikv(out, device, peak, flush)
     if "snapkv_32k" in want:
         snapkv(out, device, peak, flush)
     if "h2o_16k" in want:
@@ -579,6 +733,68 @@ def ragged(out, device, peak):
         "step_gbs": round(sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9, 1),
         "steps": K, "warmup": 3}
     del qb
+    torch.cuda.empty_cache()
+
+
+def tiny(out, device):
+    """The one-sequence, one-query Quest step (2K context, 8 of 128 pages): a
+    latency figure (no roofline target), one replayed graph per step."""
+    import torch
+    qb = QuestBench("tiny_quest", device, mode=HEADLINE_MODE)
+    qb.capture()
+    step_ms, _, _ = qb.timed(50, 5, graphs=True)
+    out["tiny_quest"] = {
+        "us_per_step": round(sum(step_ms) / len(step_ms) * 1e3, 2),
+        "us_per_step_min": round(min(step_ms) * 1e3, 2),
+        "queries_per_s": round(len(step_ms) / (sum(step_ms) / 1e3), 1),
+        "step": "Quest select with the append fused + split-K decode, one replayed graph",
+        "steps": 50, "warmup": 5}
+    del qb
+    torch.cuda.empty_cache()
+
+
+def omnikv(out, device, peak, flush):
+    """Cross-layer selection reuse: 16 x 32K requests through 4 attention
+    layers, layer 0 selecting with Quest and layers 1-3 decoding through its
+    view; one replayed graph per step index, L2 flushed before each step."""
+    import numpy as np
+    import torch
+    from kv_cache_decode_quest_gb300 import synth, workloads
+    w = synth.workloads()["omnikv_32k"]
+    run = workloads.OmniRun(w, synth.omnikv_inputs(w), device=device)
+    side = torch.cuda.Stream()
+    graphs = []
+    for s in range(w.steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            run.step(s)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    W, K = 3, w.steps - 3
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for s in range(W):
+        flush.zero_()
+        graphs[s].replay()
+    evs = []
+    for s in range(W, W + K):
+        flush.zero_()
+        e = (E(), E())
+        e[0].record()
+        graphs[s].replay()
+        e[1].record()
+        evs.append(e)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    nbytes = sum(run.algorithmic_bytes(np.asarray(w.ctx) + s + 1)["total"] for s in range(W, W + K))
+    gbs = nbytes / (sum(ms) / 1e3) / 1e9
+    out["omnikv_32k"] = {
+        "layer_queries_per_s": round(w.batch * w.layers * K / (sum(ms) / 1e3), 1),
+        "steps_per_s": round(K / (sum(ms) / 1e3), 1),
+        "ms_per_step": round(sum(ms) / K, 5),
+        "step_algorithmic_gbs": round(gbs, 1), "step_frac": round(gbs / peak, 4),
+        "layers": w.layers, "filter_layers": list(w.filters), "batch": w.batch,
+        "status": run.status(), "steps": K, "warmup": W}
+    del run, graphs
     torch.cuda.empty_cache()
 
 
@@ -723,6 +939,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="seconds of oracle work per host core for cpu_baseline (0 = skip)")
+    ap.add_argument("--oracle-seconds", type=float, default=2.0,
+                    help="seconds of single-threaded oracle work per workload (0 = skip)")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--only", choices=EXTRAS, default=None,
                     help="run one of the other workloads alone and print its figures")
