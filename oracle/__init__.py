@@ -38,3 +38,4 @@ from .attention import attend, logits  # noqa: F401
 from .snapkv import window_scores, max_pool, keep_positions, compact  # noqa: F401
 from .h2o import H2OState, h2o_init, h2o_step  # noqa: F401
 from .omnikv import omnikv_layers, source_layer, filter_pages  # noqa: F401
+from .prune import span_keep_positions, sink_recent_pages  # noqa: F401

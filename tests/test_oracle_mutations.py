@@ -180,3 +180,25 @@ def test_omnikv_mutations_are_caught(monkeypatch):
         monkeypatch.setattr(T_om, "omnikv_layers", bad)
         assert any(fails(fn, *args) for fn, *args in pins), bad.__name__
     monkeypatch.setattr(T_om, "omnikv_layers", good)
+
+
+def test_span_prune_mutations_are_caught(monkeypatch):
+    import oracle.prune as pr
+    from tests import test_oracle_prune as T_pr
+
+    def pool_unclipped(A, L, s0, s1, keep, kernel):             # neighbours outside the span used
+        A = np.asarray(A, float)
+        s0 = max(0, min(int(s0), L))
+        s1 = max(s0, min(int(s1), L))
+        full = snap.max_pool(A, kernel)
+        cand = topk.top_k(full[s0:s1], keep) + s0
+        return np.concatenate([np.arange(s0), cand, np.arange(s1, L)]).astype(np.int64)
+
+    def drops_tail(A, L, s0, s1, keep, kernel):                 # tokens after the span lost
+        got = pr.span_keep_positions(A, L, s0, s1, keep, kernel)
+        return got[got < max(0, min(int(s1), L))]
+
+    for bad in (pool_unclipped, drops_tail):
+        monkeypatch.setattr(T_pr, "span_keep_positions", bad)
+        assert fails(T_pr.test_span_selection_matches_brute_force_on_small_cases) or \
+            fails(T_pr.test_outside_positions_untouched_and_ascending), bad.__name__
