@@ -372,6 +372,38 @@ int se_snapkv_compact(const se_paged_kv* prefill, const void* q_win, int batch, 
                       int window, int pool_kernel, int keep, int recent, float scale,
                       const se_varlen_kv* out, void* ws, size_t ws_bytes, se_stream_t stream);
 
+/* ---- prefix-cache pruning over a caller span ([tokendh] "该删哪段历史,让应用自己说了算:
+ * 可控前缀裁剪": the application names a region of the history and how much of it
+ * to keep; a scorer keeps the tokens of the region that matter and the logical
+ * prefix stays whole for prefix matching) ---------------------------------------
+ * For unit (b, h), L = ctx_len[b]: the candidates are the positions
+ * [span[2b], span[2b+1]) clipped to [0, L).  Their scores are the window
+ * column scores A[j] of se_snapkv_compact (window rows L-window .. L-1, the
+ * scorer the pages name, KVzip, being undescribed there), max-pooled over the
+ * span with `pool_kernel` (neighbours outside the span ignored).  The best
+ * keep_tokens[b] candidates under (pooled desc, position asc) are kept, and so
+ * is every position outside the span.  Output as se_snapkv_compact: rows in
+ * ascending position, pos = the logical positions (so a logical prefix still
+ * matches), score = the unpooled A of each kept token, seg_len[u] = rows kept,
+ * seq_len[b] = L; rows past seg_cap: SE_DEV_CAPACITY.
+ * span int32 [batch][2], keep_tokens int32 [batch]: device.
+ * Limits and workspace: those of se_snapkv_compact. */
+int se_span_prune(const se_paged_kv* prefix, const void* q_win, int batch, int num_q_heads,
+                  int window, int pool_kernel, const int32_t* span, const int32_t* keep_tokens,
+                  float scale, const se_varlen_kv* out, void* ws, size_t ws_bytes,
+                  se_stream_t stream);
+
+/* StreamingLLM-style view of a paged cache (the first tokens as attention
+ * sinks plus a recent window; "SparseEngine 统一接入十五种稀疏注意力", section
+ * "哪些情况下加速幅度会缩小"), at page granularity: unit u = (b, h) attends the
+ * pages [0, sink_pages) and the last recent_pages pages of its n =
+ * ceil(ctx_len[b]/16) pages, each page once (all pages when they overlap), in
+ * page order; n_tokens counts their valid tokens.  Needs view->max_chunks >=
+ * min(sink_pages + recent_pages, max_pages_per_seq).  Feed the view to
+ * se_sparse_decode.  Workspace: se_small_workspace(). */
+int se_view_sink_recent(const se_paged_kv* kv, int batch, int sink_pages, int recent_pages,
+                        const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);
+
 /* ---- (d) H2O decode step ([tokendh] H2O: accumulated attention scores updated
  * every decode step, then a physical deletion) -----------------------------------
  * For each unit u = (b, h):

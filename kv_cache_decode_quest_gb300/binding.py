@@ -89,6 +89,8 @@ SIGNATURES = {
     "se_varlen_append_view": (_I, [_VP, _VP, _VP, _I, _VP, _VP, _SZ, _VP]),
     "se_snapkv_compact": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _SZ, _VP]),
     "se_h2o_step": (_I, [_VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "se_span_prune": (_I, [_VP, _VP, _I, _I, _I, _I, _VP, _VP, _F, _VP, _VP, _SZ, _VP]),
+    "se_view_sink_recent": (_I, [_VP, _I, _I, _I, _VP, _VP, _SZ, _VP]),
 }
 
 _lib = None
@@ -376,3 +378,23 @@ def se_h2o_step(st: H2OState, q, k_new, v_new, batch: int, num_q_heads: int, sca
     _check(load().se_h2o_step(ctypes.byref(c), _p(q), _p(k_new), _p(v_new), batch, num_q_heads,
                               scale, out_dtype, _p(out), _p(lse), _p(evicted_pos), _p(ws),
                               ws.numel(), _stream(stream)), "se_h2o_step")
+
+
+def se_span_prune(prefix: PagedKV, q_win, batch: int, num_q_heads: int, window: int,
+                  pool_kernel: int, span, keep_tokens, scale: float, out: VarlenKV, ws,
+                  stream=None):
+    """Prune each sequence's span [span[b,0], span[b,1]) to its best
+    keep_tokens[b] tokens by window score; everything else is kept."""
+    c, oc = prefix.c, out.c
+    _check(load().se_span_prune(ctypes.byref(c), _p(q_win), batch, num_q_heads, window,
+                                pool_kernel, _p(span), _p(keep_tokens), scale, ctypes.byref(oc),
+                                _p(ws), ws.numel(), _stream(stream)), "se_span_prune")
+
+
+def se_view_sink_recent(kv: PagedKV, batch: int, sink_pages: int, recent_pages: int, view: View,
+                        ws, stream=None):
+    """The sink + recent pages view of a paged cache."""
+    c, vc = kv.c, view.c
+    _check(load().se_view_sink_recent(ctypes.byref(c), batch, sink_pages, recent_pages,
+                                      ctypes.byref(vc), _p(ws), ws.numel(), _stream(stream)),
+           "se_view_sink_recent")

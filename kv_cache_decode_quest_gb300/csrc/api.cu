@@ -383,6 +383,55 @@ int se_snapkv_compact(const se_paged_kv* prefill, const void* q_win, int batch, 
                                              (int)max_ctx, static_cast<cudaStream_t>(stream)));
 }
 
+int se_span_prune(const se_paged_kv* prefix, const void* q_win, int batch, int num_q_heads,
+                  int window, int pool_kernel, const int32_t* span, const int32_t* keep_tokens,
+                  float scale, const se_varlen_kv* out, void* ws, size_t ws_bytes,
+                  se_stream_t stream) {
+    int rc = check_paged(prefix, false);
+    if (rc) return rc;
+    if ((rc = check_varlen(out))) return rc;
+    if (batch < 0 || num_q_heads <= 0) return SE_ERR_INVALID_ARG;
+    if (num_q_heads % prefix->num_kv_heads) return SE_ERR_UNSUPPORTED;
+    const int G = num_q_heads / prefix->num_kv_heads;
+    if (!group_ok(G)) return SE_ERR_UNSUPPORTED;
+    if (out->num_kv_heads != prefix->num_kv_heads || out->head_dim != prefix->head_dim)
+        return SE_ERR_INVALID_ARG;
+    if (window < 1 || window > 64 || window * G > 256) return SE_ERR_UNSUPPORTED;
+    if (pool_kernel < 1 || pool_kernel > 63 || pool_kernel % 2 == 0) return SE_ERR_UNSUPPORTED;
+    if (batch == 0) return SE_OK;
+    if (!q_win || !aligned(q_win, 16) || !span || !keep_tokens) return SE_ERR_INVALID_ARG;
+    const size_t base = se_snapkv_workspace(batch, prefix->num_kv_heads, num_q_heads, window, 0);
+    const size_t per_ctx = (size_t)batch * prefix->num_kv_heads * 8;
+    if (!ws || !aligned(ws, 256) || ws_bytes < base) return SE_ERR_WORKSPACE;
+    int64_t max_ctx = (int64_t)((ws_bytes - base) / per_ctx);
+    max_ctx = std::min<int64_t>(max_ctx, (int64_t)prefix->max_pages_per_seq * SE_PAGE_SIZE);
+    while (max_ctx > 0 &&
+           se_snapkv_workspace(batch, prefix->num_kv_heads, num_q_heads, window, (int)max_ctx) >
+               ws_bytes)
+        --max_ctx;
+    if (max_ctx <= 0) return SE_ERR_WORKSPACE;
+    return cuda_status(launch_snapkv_compact(*prefix, q_win, batch, num_q_heads, window,
+                                             pool_kernel, 0, 0, scale, *out, ws, (int)max_ctx,
+                                             static_cast<cudaStream_t>(stream), span,
+                                             keep_tokens));
+}
+
+int se_view_sink_recent(const se_paged_kv* kv, int batch, int sink_pages, int recent_pages,
+                        const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream) {
+    int rc = check_paged(kv, false);
+    if (rc) return rc;
+    if (batch < 0 || sink_pages < 0 || recent_pages < 0) return SE_ERR_INVALID_ARG;
+    if (!view || !view->chunk_row || !view->n_tokens) return SE_ERR_INVALID_ARG;
+    if (view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
+    if (view->max_chunks < std::min<int64_t>((int64_t)sink_pages + recent_pages,
+                                             kv->max_pages_per_seq))
+        return SE_ERR_CAPACITY;
+    if ((rc = check_ws(ws, ws_bytes, se_small_workspace()))) return rc;
+    return cuda_status(launch_view_sink_recent(*kv, batch, sink_pages, recent_pages, *view,
+                                               static_cast<int*>(ws),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 size_t se_h2o_workspace(int batch, int num_kv_heads, int num_q_heads, int head_dim, int seg_cap) {
     if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads ||
         seg_cap < 0 || !head_dim_ok(head_dim))

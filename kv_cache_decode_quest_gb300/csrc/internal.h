@@ -45,6 +45,9 @@ cudaError_t launch_varlen_append(const se_varlen_kv& kv, const void* k_new, cons
 cudaError_t launch_varlen_append_view(const se_varlen_kv& kv, const void* k_new,
                                       const void* v_new, int batch, const se_view& view,
                                       int* status, cudaStream_t s);
+cudaError_t launch_view_sink_recent(const se_paged_kv& kv, int batch, int sink_pages,
+                                    int recent_pages, const se_view& view, int* status,
+                                    cudaStream_t s);
 cudaError_t launch_view_from_segments(const se_varlen_kv& kv, int batch, const se_view& view,
                                       int* status, cudaStream_t s);
 
@@ -109,7 +112,8 @@ cudaError_t launch_snapkv_scores_tc(const se_paged_kv& kv, const void* q_win, in
 size_t snapkv_ws_bytes(int units, int max_ctx);
 cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int batch, int Hq,
                                   int W, int pool_kernel, int keep, int recent, float scale,
-                                  const se_varlen_kv& out, void* ws, int max_ctx, cudaStream_t s);
+                                  const se_varlen_kv& out, void* ws, int max_ctx, cudaStream_t s,
+                                  const int32_t* span = nullptr, const int32_t* keep_seq = nullptr);
 
 // ---- h2o.cu ----
 size_t h2o_ws_bytes(int batch, int Hkv, int Hq, int D, int seg_cap);

@@ -164,7 +164,55 @@ __global__ void view_segments_kernel(se_varlen_kv kv, se_view view, int* status)
     if (threadIdx.x == 0) view.n_tokens[u] = len;
 }
 
+// The sink + recent view of unit u = (b, h) of a paged cache (StreamingLLM:
+// the first tokens and a recent window, here at page granularity): pages
+// [0, sink) and [n - recent, n) of the sequence's n pages, each page once;
+// its chunk is the page's physical rows of head h.  Only the newest page can
+// be partial, and it is the view's last chunk when it is selected.
+__global__ void view_sink_recent_kernel(se_paged_kv kv, int sink, int recent, se_view view,
+                                        int* status) {
+    pdl_wait();
+    pdl_trigger();
+    const int H = kv.num_kv_heads;
+    const int u = blockIdx.x, b = u / H, h = u % H;
+    const int cap = kv.max_pages_per_seq * kPage;
+    int L = kv.ctx_len[b];
+    if (L < 0 || L > cap) {
+        if (threadIdx.x == 0 && h == 0) flag(status, SE_DEV_BAD_LENGTH);
+        L = L < 0 ? 0 : cap;
+    }
+    const int n = (L + kPage - 1) / kPage;
+    const int first = min(sink, n);                       // pages [0, first)
+    const int tail0 = max(first, n - recent);             // then pages [tail0, n)
+    const int np = first + (n - tail0);
+    const int32_t* bt = kv.block_table + (int64_t)b * kv.max_pages_per_seq;
+    for (int c = threadIdx.x; c < np && c < view.max_chunks; c += blockDim.x) {
+        const int page = c < first ? c : tail0 + (c - first);
+        const int phys = bt[page];
+        if (phys >= 0 && phys < kv.num_pages) {
+            view.chunk_row[(int64_t)u * view.max_chunks + c] = (phys * H + h) * kPage;
+        } else {
+            view.chunk_row[(int64_t)u * view.max_chunks + c] = -1;
+            flag(status, SE_DEV_BAD_INDEX);
+        }
+    }
+    if (threadIdx.x == 0) {
+        // tokens: every selected page is full except the newest (page n - 1)
+        const bool last_in = np > 0 && (tail0 < n || first == n);
+        view.n_tokens[u] = last_in ? kPage * (np - 1) + (L - kPage * (n - 1)) : kPage * np;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_view_sink_recent(const se_paged_kv& kv, int batch, int sink_pages,
+                                    int recent_pages, const se_view& view, int* status,
+                                    cudaStream_t s) {
+    const int units = batch * kv.num_kv_heads;
+    if (units == 0) return cudaSuccess;
+    view_sink_recent_kernel<<<units, 128, 0, s>>>(kv, sink_pages, recent_pages, view, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_page_meta_build(const se_paged_kv& kv, int batch, int* status,
                                    cudaStream_t s) {

@@ -341,13 +341,19 @@ struct SkSelParams {
     const float* colsum;     // [units][max_ctx]
     uint32_t* keys;          // [units][max_ctx], used when the keys do not fit shared memory
     int max_ctx, recent, keep, pool_kernel;
+    // span pruning (null: SnapKV, candidates [0, L - recent)): per sequence
+    // the candidate span [span[2b], span[2b+1]) and the candidates to keep
+    const int32_t* span;
+    const int32_t* keep_seq;
     int keys_in_smem;
     int* status;
 };
 constexpr int kGatherRows = 128;                // kept rows per gather CTA
 constexpr int kSelSmemMax = 200 * 1024;         // shared-memory key budget of the select
 
-// One CTA (1024 threads) per unit: max-pooled candidate scores -> keys (in
+// One CTA (1024 threads) per unit (candidates: SnapKV's prefix before the
+// recent window, or a caller's span with every position outside it kept):
+// max-pooled candidate scores -> keys (in
 // shared memory when they fit), exact top-`keep` by (pooled desc, position
 // asc) with four 8-bit radix passes, then the kept positions in ascending
 // order (each thread owns a contiguous run of candidates: two block scans
@@ -367,10 +373,19 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
         if (threadIdx.x == 0 && h == 0) flag(p.status, SE_DEV_BAD_LENGTH);
         L = L < 0 ? 0 : lim;
     }
-    const int R = min(p.recent, L);
-    const int ncand = L - R;
+    // candidates [s0, s1): SnapKV's [0, L - recent), or the caller's span;
+    // the positions before and after them are all kept
+    int s0 = 0, s1 = L - min(p.recent, L), K = 0;
+    if (p.span != nullptr) {
+        s0 = min(max(p.span[2 * b], 0), L);
+        s1 = min(max(p.span[2 * b + 1], s0), L);
+        K = min(max(p.keep_seq[b], 0), s1 - s0);
+    } else {
+        K = min(p.keep, s1);
+    }
+    const int ncand = s1 - s0, R = L - s1;
     const int rad = p.pool_kernel / 2;
-    const float* A = p.colsum + (int64_t)u * p.max_ctx;
+    const float* A = p.colsum + (int64_t)u * p.max_ctx + s0;
     uint32_t* ky = p.keys_in_smem ? skeys : p.keys + (int64_t)u * p.max_ctx;
     const int nw = blockDim.x >> 5, wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // max-pool over [j-rad, j+rad] clipped to the candidates: a warp takes 32
@@ -407,18 +422,19 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
     }
     __syncthreads();
 
-    const int K = min(p.keep, ncand);
     const int off = p.out.seg_off[u];
     const int cap = p.out.seg_cap;
-    const int n_kept = K + R;
+    const int n_kept = s0 + K + R;
     const int n = min(n_kept, cap);
     if (threadIdx.x == 0 && n_kept > cap) flag(p.status, SE_DEV_CAPACITY);
     const bool off_ok = off >= 0 && (int64_t)off + n <= p.out.total_rows;
     if (threadIdx.x == 0 && !off_ok) flag(p.status, SE_DEV_BAD_INDEX);
     int32_t* pos = p.out.pos + off;
     if (off_ok) {
+        for (int j = threadIdx.x; j < s0 && j < cap; j += blockDim.x) pos[j] = j;
+        pos += s0;                                        // the candidates' ranks start here
         if (K == ncand) {
-            for (int j = threadIdx.x; j < ncand && j < cap; j += blockDim.x) pos[j] = j;
+            for (int j = threadIdx.x; j < ncand && j + s0 < cap; j += blockDim.x) pos[j] = s0 + j;
         } else if (K > 0) {
             int need_eq;
             const uint32_t T = block_radix_select([&](int i) { return ky[i]; }, ncand, K, hist, tmp,
@@ -472,14 +488,14 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
                 const uint32_t mt = __ballot_sync(0xffffffffu, take);
                 if (take) {
                     const int at = o + __popc(mt & lt);
-                    if (at < cap) pos[at] = i;
+                    if (at + s0 < cap) pos[at] = s0 + i;
                 }
                 o += __popc(mt);
                 eq_seen += __popc(meq);
             }
         }
         for (int t = threadIdx.x; t < R; t += blockDim.x)
-            if (K + t < cap) pos[K + t] = ncand + t;
+            if (s0 + K + t < cap) pos[K + t] = s1 + t;
     }
     if (threadIdx.x == 0) {
         p.out.seg_len[u] = off_ok ? n : 0;
@@ -550,7 +566,8 @@ size_t snapkv_ws_bytes(int units, int max_ctx) {
 
 cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int batch, int Hq,
                                   int W, int pool_kernel, int keep, int recent, float scale,
-                                  const se_varlen_kv& out, void* ws, int max_ctx, cudaStream_t s) {
+                                  const se_varlen_kv& out, void* ws, int max_ctx, cudaStream_t s,
+                                  const int32_t* span, const int32_t* keep_seq) {
     const int H = kv.num_kv_heads, units = batch * H, G = Hq / H, D = kv.head_dim;
     if (units == 0) return cudaSuccess;
     uint8_t* base = static_cast<uint8_t*>(ws);
@@ -593,6 +610,8 @@ cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int 
     q.recent = recent;
     q.keep = keep;
     q.pool_kernel = pool_kernel;
+    q.span = span;
+    q.keep_seq = keep_seq;
     q.status = p.status;
     const size_t key_bytes = (size_t)max_ctx * sizeof(uint32_t);
     q.keys_in_smem = key_bytes <= kSelSmemMax;
