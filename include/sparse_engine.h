@@ -404,6 +404,62 @@ int se_span_prune(const se_paged_kv* prefix, const void* q_win, int batch, int n
 int se_view_sink_recent(const se_paged_kv* kv, int batch, int sink_pages, int recent_pages,
                         const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);
 
+/* ---- Chain Cache: retained state carried across turns ([tokendh] "聊天记录也能
+ * '续命':Chain Cache": a method that deleted history physically resumes from the
+ * state it kept when a new turn continues the same logical prefix; [netics]
+ * "部署长上下文 Agent 的团队可以从中得到什么": the ChainCacheIndex links a session
+ * to its retained per-layer KV, its method metadata and its logical token
+ * prefix).  The device part copies state; the host part is a prefix index.
+ *
+ * Snapshot: a caller-owned device buffer (256-byte aligned) of
+ * se_chain_snapshot_bytes(num_seqs, num_kv_heads, head_dim, rows, with_score)
+ * bytes: a format header, then one slot per (saved sequence i, KV head h) of
+ * `rows` rows: the unit's seg_len retained rows of K and V, their logical
+ * positions, their scores when the cache keeps scores (with_score = score !=
+ * NULL), and the sequence's seq_len.  A cache's method metadata that is not
+ * per token (H2O's budget and recent window) stays with the caller.
+ *
+ * se_chain_save: slot (i, h) <- unit (seqs[i], h) of kv, rows [0, seg_len) in
+ * their order.  se_chain_restore: unit (seqs[i], h) of kv <- slot (i, h),
+ * written at that unit's seg_off with seg_len and seq_len set; the target
+ * cache may place its segments anywhere (its seg_off), need not be the saved
+ * one, and must have the same num_kv_heads, head_dim and score presence.  A
+ * restored cache decodes exactly as the saved one would have (the rows, their
+ * order, positions and scores are the same bytes).
+ * seqs int32 [num_seqs] device.  A segment longer than `rows`, or a slot
+ * longer than the target's seg_cap: SE_DEV_CAPACITY (truncated).  A snapshot
+ * written for another shape, or seqs[i] < 0: SE_DEV_BAD_INDEX, unit left as is.
+ * Workspace: se_small_workspace(). */
+size_t se_chain_snapshot_bytes(int num_seqs, int num_kv_heads, int head_dim, int rows,
+                               int with_score);
+int se_chain_save(const se_varlen_kv* kv, const int32_t* seqs, int num_seqs, int rows, void* snap,
+                  size_t snap_bytes, void* ws, size_t ws_bytes, se_stream_t stream);
+int se_chain_restore(const void* snap, size_t snap_bytes, int num_seqs, int rows,
+                     const int32_t* seqs, const se_varlen_kv* kv, void* ws, size_t ws_bytes,
+                     se_stream_t stream);
+
+/* The ChainCacheIndex (host): maps the logical token prefix a saved session
+ * stands for -- every token of the conversation so far, the physically
+ * deleted ones included -- to the caller's id for that session (for instance
+ * a snapshot buffer).  A new request whose tokens begin with a stored prefix
+ * matches it; the longest stored prefix wins, compared token by token.
+ * Tokens are host int32 arrays.  The index is the one object the library
+ * allocates (host memory, freed by se_chain_index_destroy); its calls are
+ * thread-safe.
+ *   create: NULL when out of memory.
+ *   put: stores (tokens, id) -- an existing entry with that id is replaced.
+ *   match: the id of the longest stored prefix of tokens (-1 when none), its
+ *          length in *matched_tokens (may be NULL).
+ *   erase: forgets id (no error when absent).  size: entries stored. */
+typedef struct se_chain_index se_chain_index;
+se_chain_index* se_chain_index_create(void);
+void se_chain_index_destroy(se_chain_index* ix);
+int se_chain_index_put(se_chain_index* ix, const int32_t* tokens, int64_t n_tokens, int64_t id);
+int64_t se_chain_index_match(se_chain_index* ix, const int32_t* tokens, int64_t n_tokens,
+                             int64_t* matched_tokens);
+int se_chain_index_erase(se_chain_index* ix, int64_t id);
+int64_t se_chain_index_size(se_chain_index* ix);
+
 /* ---- (d) H2O decode step ([tokendh] H2O: accumulated attention scores updated
  * every decode step, then a physical deletion) -----------------------------------
  * For each unit u = (b, h):

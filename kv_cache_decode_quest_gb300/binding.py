@@ -89,6 +89,15 @@ SIGNATURES = {
     "se_varlen_append_view": (_I, [_VP, _VP, _VP, _I, _VP, _VP, _SZ, _VP]),
     "se_snapkv_compact": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _SZ, _VP]),
     "se_h2o_step": (_I, [_VP, _VP, _VP, _VP, _I, _I, _F, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "se_chain_snapshot_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "se_chain_save": (_I, [_VP, _VP, _I, _I, _VP, _SZ, _VP, _SZ, _VP]),
+    "se_chain_restore": (_I, [_VP, _SZ, _I, _I, _VP, _VP, _VP, _SZ, _VP]),
+    "se_chain_index_create": (_VP, []),
+    "se_chain_index_destroy": (None, [_VP]),
+    "se_chain_index_put": (_I, [_VP, _VP, _I64, _I64]),
+    "se_chain_index_match": (_I64, [_VP, _VP, _I64, _VP]),
+    "se_chain_index_erase": (_I, [_VP, _I64]),
+    "se_chain_index_size": (_I64, [_VP]),
     "se_span_prune": (_I, [_VP, _VP, _I, _I, _I, _I, _VP, _VP, _F, _VP, _VP, _SZ, _VP]),
     "se_view_sink_recent": (_I, [_VP, _I, _I, _I, _VP, _VP, _SZ, _VP]),
 }
@@ -398,3 +407,69 @@ def se_view_sink_recent(kv: PagedKV, batch: int, sink_pages: int, recent_pages: 
     _check(load().se_view_sink_recent(ctypes.byref(c), batch, sink_pages, recent_pages,
                                       ctypes.byref(vc), _p(ws), ws.numel(), _stream(stream)),
            "se_view_sink_recent")
+
+
+def se_chain_snapshot_bytes(num_seqs: int, num_kv_heads: int, head_dim: int, rows: int,
+                            with_score: bool) -> int:
+    return load().se_chain_snapshot_bytes(num_seqs, num_kv_heads, head_dim, rows, int(with_score))
+
+
+def se_chain_save(kv: VarlenKV, seqs, rows: int, snap, ws, stream=None):
+    """Copy the retained segments of sequences `seqs` (int32 device) into `snap`."""
+    c = kv.c
+    _check(load().se_chain_save(ctypes.byref(c), _p(seqs), seqs.numel(), rows, _p(snap),
+                                snap.numel(), _p(ws), ws.numel(), _stream(stream)),
+           "se_chain_save")
+
+
+def se_chain_restore(snap, rows: int, seqs, kv: VarlenKV, ws, stream=None):
+    """Copy a snapshot's slots into the segments of sequences `seqs` of `kv`."""
+    c = kv.c
+    _check(load().se_chain_restore(_p(snap), snap.numel(), seqs.numel(), rows, _p(seqs),
+                                   ctypes.byref(c), _p(ws), ws.numel(), _stream(stream)),
+           "se_chain_restore")
+
+
+class ChainIndex:
+    """The host ChainCacheIndex: logical token prefix -> session id."""
+
+    def __init__(self):
+        self._h = load().se_chain_index_create()
+        if not self._h:
+            raise SparseEngineError("se_chain_index_create failed")
+
+    def close(self):
+        if self._h:
+            load().se_chain_index_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _tok(tokens):
+        import numpy as np
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        return t, t.ctypes.data_as(ctypes.c_void_p), t.size
+
+    def put(self, tokens, sid: int):
+        t, ptr, n = self._tok(tokens)
+        _check(load().se_chain_index_put(self._h, ptr, n, sid), "se_chain_index_put")
+
+    def match(self, tokens):
+        """(id, matched tokens) of the longest stored prefix, (-1, 0) if none."""
+        t, ptr, n = self._tok(tokens)
+        m = ctypes.c_int64(0)
+        sid = load().se_chain_index_match(self._h, ptr, n, ctypes.byref(m))
+        if sid < -1:
+            _check(int(sid), "se_chain_index_match")
+        return int(sid), int(m.value)
+
+    def erase(self, sid: int):
+        _check(load().se_chain_index_erase(self._h, sid), "se_chain_index_erase")
+
+    def __len__(self):
+        return int(load().se_chain_index_size(self._h))

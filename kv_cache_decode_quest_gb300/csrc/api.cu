@@ -432,6 +432,38 @@ int se_view_sink_recent(const se_paged_kv* kv, int batch, int sink_pages, int re
                                                static_cast<cudaStream_t>(stream)));
 }
 
+int se_chain_save(const se_varlen_kv* kv, const int32_t* seqs, int num_seqs, int rows, void* snap,
+                  size_t snap_bytes, void* ws, size_t ws_bytes, se_stream_t stream) {
+    int rc = check_varlen(kv);
+    if (rc) return rc;
+    if (num_seqs < 0 || rows < 0) return SE_ERR_INVALID_ARG;
+    if (num_seqs == 0) return SE_OK;
+    if (!seqs || !snap || !aligned(snap, 256)) return SE_ERR_INVALID_ARG;
+    if (snap_bytes < chain_snapshot_bytes(num_seqs, kv->num_kv_heads, kv->head_dim, rows,
+                                          kv->score != nullptr))
+        return SE_ERR_CAPACITY;
+    if ((rc = check_ws(ws, ws_bytes, se_small_workspace()))) return rc;
+    return cuda_status(launch_chain_copy(true, *kv, seqs, num_seqs, rows, snap,
+                                         static_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+int se_chain_restore(const void* snap, size_t snap_bytes, int num_seqs, int rows,
+                     const int32_t* seqs, const se_varlen_kv* kv, void* ws, size_t ws_bytes,
+                     se_stream_t stream) {
+    int rc = check_varlen(kv);
+    if (rc) return rc;
+    if (num_seqs < 0 || rows < 0) return SE_ERR_INVALID_ARG;
+    if (num_seqs == 0) return SE_OK;
+    if (!seqs || !snap || !aligned(snap, 256)) return SE_ERR_INVALID_ARG;
+    if (snap_bytes < chain_snapshot_bytes(num_seqs, kv->num_kv_heads, kv->head_dim, rows,
+                                          kv->score != nullptr))
+        return SE_ERR_CAPACITY;
+    if ((rc = check_ws(ws, ws_bytes, se_small_workspace()))) return rc;
+    return cuda_status(launch_chain_copy(false, *kv, seqs, num_seqs, rows,
+                                         const_cast<void*>(snap), static_cast<int*>(ws),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 size_t se_h2o_workspace(int batch, int num_kv_heads, int num_q_heads, int head_dim, int seg_cap) {
     if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads ||
         seg_cap < 0 || !head_dim_ok(head_dim))

@@ -76,6 +76,11 @@ cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const vo
                               const se_view& view, void* out, float* lse, void* ws,
                               cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t s);
 
+// ---- chain.cu ----
+size_t chain_snapshot_bytes(int num_seqs, int H, int D, int rows, bool with_score);
+cudaError_t launch_chain_copy(bool save, const se_varlen_kv& kv, const int32_t* seqs, int n,
+                              int rows, void* snap, int* status, cudaStream_t s);
+
 // ---- decode.cu ----
 struct DecodeWs {
     int* status;
