@@ -33,7 +33,7 @@ Parity pins: every function here is pinned by tests under ``tests/`` marked
 
 from .bf16 import widen  # noqa: F401
 from .topk import rank_order, top_k  # noqa: F401
-from .quest import page_minmax, quest_bound, quest_k_pages, quest_select  # noqa: F401
+from .quest import page_minmax, quest_bound, quest_bound_max, quest_k_pages, quest_select  # noqa: F401
 from .attention import attend, logits  # noqa: F401
 from .snapkv import window_scores, max_pool, keep_positions, compact  # noqa: F401
 from .h2o import H2OState, h2o_init, h2o_step  # noqa: F401

@@ -15,7 +15,9 @@ Definitions used here:
   which is >= q.k for every key of the page;
 * GQA reading: the KV head's page score is the SUM of its query heads' bounds
   (an upper bound of the group-summed logit; all query heads of a KV head
-  share one page selection);
+  share one page selection); the alternative reading, the MAX of the query
+  heads' bounds (an upper bound of every head's own logit), is
+  ``quest_bound_max``, selectable as a flag;
 * budget: k = max(1, floor(budget / 16)) pages per KV head; the last page
   (holding the newest token) is always selected and counts against k; the
   other k-1 are the best remaining pages under (score desc, page asc); if the
@@ -51,6 +53,17 @@ def quest_bound(q_group, kmin, kmax):
     lo = q[:, None, :] * np.asarray(kmin, dtype=np.float64)[None, :, :]   # [G][P][D]
     hi = q[:, None, :] * np.asarray(kmax, dtype=np.float64)[None, :, :]
     return np.maximum(lo, hi).sum(axis=(0, 2))
+
+
+def quest_bound_max(q_group, kmin, kmax):
+    """The max-aggregation variant of the bound (the alternative reading of
+    how a KV head's query heads combine): U[p] = max over the group's query
+    heads g of sum_d max(q[g,d]*kmin[p,d], q[g,d]*kmax[p,d]) -- each head's own
+    upper bound, the largest of them.  q_group [G][D]."""
+    q = np.asarray(q_group, dtype=np.float64)
+    lo = q[:, None, :] * np.asarray(kmin, dtype=np.float64)[None, :, :]   # [G][P][D]
+    hi = q[:, None, :] * np.asarray(kmax, dtype=np.float64)[None, :, :]
+    return np.maximum(lo, hi).sum(axis=2).max(axis=0)
 
 
 def quest_k_pages(budget_tokens: int, page_size: int = PAGE) -> int:

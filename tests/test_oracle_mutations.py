@@ -202,3 +202,22 @@ def test_span_prune_mutations_are_caught(monkeypatch):
         monkeypatch.setattr(T_pr, "span_keep_positions", bad)
         assert fails(T_pr.test_span_selection_matches_brute_force_on_small_cases) or \
             fails(T_pr.test_outside_positions_untouched_and_ascending), bad.__name__
+
+
+def _bound_max_by_min(q_group, kmin, kmax):     # min over the group instead of max
+    q = np.asarray(q_group, float)
+    return np.maximum(q[:, None] * kmin[None], q[:, None] * kmax[None]).sum(axis=2).min(axis=0)
+
+
+def _bound_max_of_products(q_group, kmin, kmax):  # max taken before the channel sum
+    q = np.asarray(q_group, float)
+    return np.maximum(q[:, None] * kmin[None], q[:, None] * kmax[None]).max(axis=0).sum(axis=1)
+
+
+@pytest.mark.parametrize("bad", [_bound_max_by_min, _bound_max_of_products, quest.quest_bound])
+def test_quest_bound_max_mutations_are_caught(monkeypatch, bad):
+    monkeypatch.setattr(T_quest, "quest_bound_max", bad)
+    caught = fails(T_quest.test_max_bound_hand_worked) or \
+        fails(T_quest.test_max_bound_page_size_one_is_the_exact_max_logit) or \
+        any(fails(T_quest.test_max_bound_dominates_every_heads_logit, s) for s in range(3))
+    assert caught

@@ -88,3 +88,48 @@ def test_budget_to_pages():
 def test_selected_tokens_partial_last_page():
     assert selected_tokens([0, 2], ctx=37, page_size=16).tolist() == \
         list(range(0, 16)) + list(range(32, 37))
+
+
+# ---- the max-aggregation variant --------------------------------------------
+
+from oracle.quest import quest_bound_max  # noqa: E402
+
+
+def test_max_bound_hand_worked():
+    """Two query heads, one page of two keys, D = 2:
+    head 0 (1, -1): per channel max(1*kmin, 1*kmax) + max(-kmin, -kmax)
+    head 1 (-2, 0.5)."""
+    k = np.array([[1.0, 2.0], [3.0, -1.0]])
+    kmin, kmax = k.min(axis=0)[None], k.max(axis=0)[None]     # (1, -1), (3, 2)
+    q = np.array([[1.0, -1.0], [-2.0, 0.5]])
+    # head 0: 3 + 1 = 4;  head 1: max(-2, -6) + max(-0.5, 1) = -2 + 1 = -1
+    assert np.allclose(quest_bound_max(q, kmin, kmax), [4.0])
+    assert np.allclose(quest_bound(q, kmin, kmax), [3.0])
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_max_bound_dominates_every_heads_logit(seed):
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((200, 32))
+    q = rng.standard_normal((8, 32))
+    U = quest_bound_max(q, *page_minmax(K))
+    logits = q @ K.T                                          # [G][T]
+    for p in range(len(U)):
+        assert U[p] >= logits[:, p * 16:(p + 1) * 16].max() - 1e-9
+
+
+def test_max_bound_page_size_one_is_the_exact_max_logit():
+    rng = np.random.default_rng(4)
+    K = rng.standard_normal((40, 8))
+    q = rng.standard_normal((4, 8))
+    kmin, kmax = page_minmax(K, page_size=1)
+    want = np.array([max(float(q[g] @ K[t]) for g in range(4)) for t in range(40)])
+    assert np.allclose(quest_bound_max(q, kmin, kmax), want)
+
+
+def test_max_bound_single_head_is_the_sum_bound():
+    rng = np.random.default_rng(5)
+    K = rng.standard_normal((100, 16))
+    q = rng.standard_normal((1, 16))
+    mm = page_minmax(K)
+    assert np.array_equal(quest_bound_max(q, *mm), quest_bound(q, *mm))
