@@ -69,6 +69,10 @@ extern "C" {
 #define SE_PAGE_SIZE 16
 #define SE_MAX_SPLITS 64
 
+/* How a KV head's page bound combines its query heads (se_select_opts). */
+#define SE_AGG_SUM 0             /* sum of the query heads' bounds (default) */
+#define SE_AGG_MAX 1             /* largest of the query heads' bounds */
+
 typedef void* se_stream_t;       /* cudaStream_t */
 
 /* Paged KV cache with Quest page summaries ([jetabc] paging; [tokendh] the
@@ -252,6 +256,24 @@ int se_quest_select_append(const se_paged_kv* kv, const void* k_new, const void*
                            const void* q, int batch, int num_q_heads,
                            const int32_t* budget_tokens, int32_t* sel_pages, int32_t* n_sel,
                            const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);
+
+/* Options of se_quest_select_ex (NULL means all defaults). */
+typedef struct se_select_opts {
+    int32_t group_agg;        /* SE_AGG_SUM (0, default) or SE_AGG_MAX */
+} se_select_opts;
+
+/* se_quest_select (k_new, v_new NULL) or se_quest_select_append (both given)
+ * with options.  group_agg = SE_AGG_MAX takes the other reading of how a KV
+ * head's query heads combine in the page bound:
+ *   U[p] = max_g sum_d max(q[b,hG+g,d]*kmin[p,h,d], q[b,hG+g,d]*kmax[p,h,d]),
+ * the largest of the heads' own bounds (an upper bound of every head's logit
+ * over the page) instead of their sum; everything else is the same.  It needs
+ * G <= 8 query heads per KV head and num_kv_heads in {1, 2, 4, 8}, else
+ * SE_ERR_UNSUPPORTED.  Arguments, limits and workspace: se_quest_select's. */
+int se_quest_select_ex(const se_paged_kv* kv, const void* k_new, const void* v_new,
+                       const void* q, int batch, int num_q_heads, const int32_t* budget_tokens,
+                       const se_select_opts* opts, int32_t* sel_pages, int32_t* n_sel,
+                       const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream);
 
 /* View of whole varlen segments: chunk c of unit u starts at row seg_off[u] + 16c;
  * n_tokens[u] = seg_len[u].  Needs view->max_chunks >= ceil(seg_cap / 16).

@@ -54,6 +54,13 @@ class DecodeOptsC(ctypes.Structure):
                 ("ev_kernel_begin", ctypes.c_void_p), ("ev_kernel_end", ctypes.c_void_p)]
 
 
+class SelectOptsC(ctypes.Structure):
+    _fields_ = [("group_agg", ctypes.c_int32)]
+
+
+SE_AGG_SUM, SE_AGG_MAX = 0, 1
+
+
 class QuestStepOptsC(ctypes.Structure):
     _fields_ = [("out_dtype", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("ev_kernel_begin", ctypes.c_void_p), ("ev_kernel_end", ctypes.c_void_p),
@@ -81,6 +88,8 @@ SIGNATURES = {
     "se_quest_step": (_I, [_VP, _VP, _VP, _VP, _I, _I, _VP, _F, _VP, _VP, _VP, _VP, _VP, _VP,
                            _VP, _SZ, _VP]),
     "se_view_from_segments": (_I, [_VP, _I, _VP, _VP, _SZ, _VP]),
+    "se_quest_select_ex": (_I, [_VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                                _VP]),
     "se_sparse_decode": (_I, [_VP, _VP, _I64, _VP, _VP, _I, _I, _I, _I, _F, _VP, _VP, _VP,
                               _VP, _SZ, _VP]),
     "se_sparse_decode_noalloc": (_I, [_VP, _VP, _I64, _VP, _VP, _I, _I, _I, _I, _F, _I, _VP,
@@ -307,6 +316,19 @@ def se_quest_select_append(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads
                                          num_q_heads, _p(budget_tokens), _p(sel_pages),
                                          _p(n_sel), ctypes.byref(vc), _p(ws), ws.numel(),
                                          _stream(stream)), "se_quest_select_append")
+
+
+def se_quest_select_ex(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads: int,
+                       budget_tokens, sel_pages, n_sel, view: View, ws, group_agg: int = 0,
+                       stream=None):
+    """Quest selection (with the append when k_new/v_new are given) with
+    options: group_agg SE_AGG_SUM or SE_AGG_MAX."""
+    c, vc = kv.c, view.c
+    opts = SelectOptsC(group_agg)
+    _check(load().se_quest_select_ex(ctypes.byref(c), _p(k_new), _p(v_new), _p(q), batch,
+                                     num_q_heads, _p(budget_tokens), ctypes.byref(opts),
+                                     _p(sel_pages), _p(n_sel), ctypes.byref(vc), _p(ws),
+                                     ws.numel(), _stream(stream)), "se_quest_select_ex")
 
 
 def se_quest_step(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads: int, budget_tokens,

@@ -207,6 +207,37 @@ int se_quest_select_append(const se_paged_kv* kv, const void* k_new, const void*
                                            static_cast<cudaStream_t>(stream)));
 }
 
+int se_quest_select_ex(const se_paged_kv* kv, const void* k_new, const void* v_new,
+                       const void* q, int batch, int num_q_heads, const int32_t* budget_tokens,
+                       const se_select_opts* opts, int32_t* sel_pages, int32_t* n_sel,
+                       const se_view* view, void* ws, size_t ws_bytes, se_stream_t stream) {
+    if ((k_new == nullptr) != (v_new == nullptr)) return SE_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return SE_ERR_INVALID_ARG;
+    const int agg = opts ? opts->group_agg : SE_AGG_SUM;
+    if (agg != SE_AGG_SUM && agg != SE_AGG_MAX) return SE_ERR_INVALID_ARG;
+    int rc = check_paged(kv, true);
+    if (rc) return rc;
+    if (batch < 0 || num_q_heads <= 0) return SE_ERR_INVALID_ARG;
+    if (num_q_heads % kv->num_kv_heads || !group_ok(num_q_heads / kv->num_kv_heads))
+        return SE_ERR_UNSUPPORTED;
+    if (agg == SE_AGG_MAX &&
+        (num_q_heads / kv->num_kv_heads > 8 || 8 % kv->num_kv_heads != 0))
+        return SE_ERR_UNSUPPORTED;
+    if (batch > 0 && (!q || !budget_tokens || !sel_pages || !n_sel || !view || !view->chunk_row ||
+                      !view->n_tokens))
+        return SE_ERR_INVALID_ARG;
+    if (!aligned(q, 16)) return SE_ERR_INVALID_ARG;
+    if (view && view->num_units != batch * kv->num_kv_heads) return SE_ERR_INVALID_ARG;
+    if (view && view->max_chunks < kv->max_pages_per_seq) return SE_ERR_CAPACITY;
+    if (kv->max_pages_per_seq > 26624) return SE_ERR_UNSUPPORTED;
+    if ((rc = check_ws(ws, ws_bytes,
+                       se_quest_select_workspace(batch, kv->num_kv_heads, kv->max_pages_per_seq))))
+        return rc;
+    return cuda_status(launch_quest_select(*kv, q, batch, num_q_heads, budget_tokens, sel_pages,
+                                           n_sel, *view, k_new, v_new, ws, static_cast<int*>(ws),
+                                           static_cast<cudaStream_t>(stream), agg));
+}
+
 size_t se_quest_step_workspace(int batch, int num_kv_heads, int num_q_heads, int head_dim,
                                int max_pages_per_seq, int max_splits) {
     if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 ||

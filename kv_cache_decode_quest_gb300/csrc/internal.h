@@ -58,7 +58,7 @@ size_t quest_ws_bytes(int units, int max_pages);
 cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch, int num_q_heads,
                                 const int32_t* budget, int32_t* sel_pages, int32_t* n_sel,
                                 const se_view& view, const void* k_new, const void* v_new,
-                                void* ws, int* status, cudaStream_t s);
+                                void* ws, int* status, cudaStream_t s, int group_agg = SE_AGG_SUM);
 
 // ---- quest_step.cu ----
 // se_quest_step's fixed control block holds the counters of at most this many

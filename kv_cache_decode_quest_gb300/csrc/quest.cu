@@ -254,6 +254,112 @@ __global__ void __launch_bounds__(kSelThreads, kSelMinBlocks)
     }
 }
 
+// The max-aggregation variant of the bound (flag SE_AGG_MAX):
+//   U[p] = max_g sum_d max(q_g[d]*kmin[p,d], q_g[d]*kmax[p,d])
+// is G dot products of length 2*D per (page, KV head) instead of one, so it is
+// computed without the shared-memory ring: grid (CTAs per sequence, batch),
+// 8 warps per CTA; every warp of a sequence owns one KV head h (8 % H == 0,
+// G <= 8) and a stride of its candidate pages, and each lane keeps, for the 8
+// channels of its 16-byte vector of a summary, the coefficients of all G query
+// heads in registers (min(q, 0) for the kmin vectors, max(q, 0) for the kmax
+// ones).  A summary is read by kVec = D/4 lanes (one coalesced 16-byte load
+// each, kU summaries in flight per lane); the G partial sums are reduced over
+// those lanes by a halving butterfly (each level keeps half of the values:
+// G - 1 shuffles, then the plain levels), and their maximum over g (the lanes
+// of the G partial results) is the page's key.
+template <int D, int G>
+__global__ void __launch_bounds__(256)
+    quest_score_max_kernel(se_paged_kv kv, const uint16_t* __restrict__ q, int Hq,
+                           const int32_t* __restrict__ budget, uint32_t* __restrict__ keys_ws,
+                           int pending, int32_t* __restrict__ tickets, int* status) {
+    constexpr int kVec = D / 4;                           // 16-byte vectors per summary
+    constexpr int kSpr = 32 / kVec;                       // summaries per warp-wide read
+    constexpr int kU = 8;                                 // reads in flight per lane
+    static_assert(G <= kVec, "the halving reduction needs G <= lanes per summary");
+    const int b = blockIdx.y, x = blockIdx.x;
+    const int H = kv.num_kv_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
+    const int stride = kv.max_pages_per_seq;
+    int ctx = clamp_ctx(kv.ctx_len[b], stride * kPage, status, threadIdx.x == 0 && x == 0);
+    if (pending) {
+        if (ctx < stride * kPage) ++ctx;
+        if (x == 0 && threadIdx.x == 0) tickets[b] = 0;
+    }
+    const int n = (ctx + kPage - 1) / kPage;
+    const int bud = budget[b];
+    const int k = max(1, (bud < 0 ? 0 : bud) / kPage);
+    if (n <= k) return;
+    const int m = n - 1;
+    const int gw = x * 8 + warp, W = gridDim.x * 8;
+    const int h = gw % H, wp = gw / H, WP = W / H;
+    const int v = lane % kVec, sub = lane / kVec;
+    const bool upper_part = v >= D / 8;                   // a kmax vector
+    const int d0 = (v % (D / 8)) * 8;
+    float c[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const uint4 w = *reinterpret_cast<const uint4*>(q + ((int64_t)b * Hq + h * G + g) * D + d0);
+        const uint32_t a4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float f0 = bf_lo(a4[e]), f1 = bf_hi(a4[e]);
+            c[g][2 * e] = upper_part ? fmaxf(f0, 0.f) : fminf(f0, 0.f);
+            c[g][2 * e + 1] = upper_part ? fmaxf(f1, 0.f) : fminf(f1, 0.f);
+        }
+    }
+    const uint4* M = static_cast<const uint4*>(kv.meta) + (int64_t)b * stride * H * kVec;
+    const int slots = (m + kSpr - 1) / kSpr;              // page groups of one warp-wide read
+    uint32_t* keys = keys_ws + ((int64_t)b * H + h) * stride;
+    for (int j0 = wp; j0 < slots; j0 += WP * kU) {
+        uint4 xv[kU];
+#pragma unroll
+        for (int t = 0; t < kU; ++t) {
+            const int page = (j0 + t * WP) * kSpr + sub;
+            xv[t] = page < m ? M[((int64_t)page * H + h) * kVec + v] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int t = 0; t < kU; ++t) {
+            const int page = (j0 + t * WP) * kSpr + sub;
+            const uint32_t a4[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+            float acc[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float s0 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    s0 = fmaf(c[g][2 * e], bf_lo(a4[e]), s0);
+                    s0 = fmaf(c[g][2 * e + 1], bf_hi(a4[e]), s0);
+                }
+                acc[g] = s0;
+            }
+            // halving butterfly over the kVec lanes of the summary
+            int off = kVec / 2;
+#pragma unroll
+            for (int lvl = G; lvl > 1; lvl >>= 1) {
+                const bool up = (lane & off) != 0;
+#pragma unroll
+                for (int i = 0; i < lvl / 2; ++i) {
+                    const float send = up ? acc[i] : acc[i + lvl / 2];
+                    const float keep = up ? acc[i + lvl / 2] : acc[i];
+                    acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+                off >>= 1;
+            }
+#pragma unroll
+            for (int o = off; o >= 1; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+            // acc[0] is one head's bound; the G heads sit on the lanes that
+            // differ in the halving bits
+            float mx = acc[0];
+#pragma unroll
+            for (int o = kVec / 2; o >= kVec / G && o >= 1; o >>= 1)
+                if (G > 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (v == 0 && page < m) keys[page] = float_key(mx);
+        }
+    }
+}
+
 // Threshold of the top K of m order-preserving keys in shared memory (256
 // threads).  Bits above the highest bit in which the largest and smallest key
 // differ are common to all keys, so the 11-bit radix digits start there; a pass
@@ -519,7 +625,7 @@ size_t quest_ws_bytes(int units, int max_pages) {
 cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch, int num_q_heads,
                                 const int32_t* budget, int32_t* sel_pages, int32_t* n_sel,
                                 const se_view& view, const void* k_new, const void* v_new,
-                                void* ws, int* status, cudaStream_t s) {
+                                void* ws, int* status, cudaStream_t s, int group_agg) {
     const int units = batch * kv.num_kv_heads;
     if (units == 0) return cudaSuccess;
     uint32_t* keys = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256);
@@ -541,11 +647,35 @@ cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch,
                                              budget, keys, pending, tickets, status);
         return cudaSuccess;
     };
-    cudaError_t e;
-    if (kv.head_dim == 128)
+    cudaError_t e = cudaSuccess;
+    if (group_agg == SE_AGG_MAX) {
+        // the max of the group: 8 warps per CTA, a few CTAs per SM
+        const int per = max(1, min((num_sms() * 4) / batch, kv.max_pages_per_seq));
+        const int G = num_q_heads / H;
+        auto gm = [&](auto kern) {
+            kern<<<dim3(per, batch), 256, 0, s>>>(kv, static_cast<const uint16_t*>(q), num_q_heads,
+                                                 budget, keys, pending, tickets, status);
+        };
+        if (kv.head_dim == 128) {
+            switch (G) {
+                case 1: gm(quest_score_max_kernel<128, 1>); break;
+                case 2: gm(quest_score_max_kernel<128, 2>); break;
+                case 4: gm(quest_score_max_kernel<128, 4>); break;
+                default: gm(quest_score_max_kernel<128, 8>); break;
+            }
+        } else {
+            switch (G) {
+                case 1: gm(quest_score_max_kernel<64, 1>); break;
+                case 2: gm(quest_score_max_kernel<64, 2>); break;
+                case 4: gm(quest_score_max_kernel<64, 4>); break;
+                default: gm(quest_score_max_kernel<64, 8>); break;
+            }
+        }
+    } else if (kv.head_dim == 128) {
         e = (4 % H == 0) ? go(quest_score_kernel<128, 4, true>) : go(quest_score_kernel<128, 1, false>);
-    else
+    } else {
         e = (8 % H == 0) ? go(quest_score_kernel<64, 4, true>) : go(quest_score_kernel<64, 1, false>);
+    }
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -116,8 +116,15 @@ class QuestRun:
         se.se_quest_select(self.kv, self.q[s], self.B, self.Hq, self.budget, self.sel, self.n_sel,
                            self.view, self.ws_sel)
 
+    group_agg = se.SE_AGG_SUM
+
     def append_select(self, s: int):
         """The step's append fused into the selection (one kernel fewer)."""
+        if self.group_agg != se.SE_AGG_SUM:
+            se.se_quest_select_ex(self.kv, self.k_new[s], self.v_new[s], self.q[s], self.B,
+                                  self.Hq, self.budget, self.sel, self.n_sel, self.view,
+                                  self.ws_sel, group_agg=self.group_agg)
+            return
         se.se_quest_select_append(self.kv, self.k_new[s], self.v_new[s], self.q[s], self.B,
                                   self.Hq, self.budget, self.sel, self.n_sel, self.view,
                                   self.ws_sel)

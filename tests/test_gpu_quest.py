@@ -21,17 +21,18 @@ U32 = synth.UNBOUNDED_BUDGET
 CTL_WORDS = (256 + 256 + 1024 * 4 + 4096 * 4) // 4
 
 
-def oracle_unit(w, inputs, b, h, s, gpu_pages=None):
+def oracle_unit(w, inputs, b, h, s, gpu_pages=None, agg=0):
     """Oracle for unit (b, h) at step s (after that step's append).  Returns
     (U, oracle pages, k, out [G][D], lse [G]) where the attention uses the
-    GPU's page set when given (after it passed the selection check)."""
+    GPU's page set when given (after it passed the selection check); agg 1
+    takes the max-aggregation bound."""
     G = w.num_q_heads // w.num_kv_heads
     L = w.ctx[b] + s + 1
     K = oracle.widen(inputs["k"][b][h, :L])
     V = oracle.widen(inputs["v"][b][h, :L])
     q = oracle.widen(inputs["q"][s, b, h * G:(h + 1) * G])
     kmin, kmax = oracle.page_minmax(K)
-    U = oracle.quest_bound(q, kmin, kmax)
+    U = (oracle.quest_bound_max if agg else oracle.quest_bound)(q, kmin, kmax)
     k = oracle.quest_k_pages(min(w.budget[b], U32))
     pages = oracle.quest_select(U, k)
     use = pages if gpu_pages is None else np.asarray(gpu_pages)
@@ -54,7 +55,7 @@ def check_step(run, inputs, s, units=None):
         b, h = divmod(u, Hkv)
         gpu_pages = sel[u, :n_sel[u]]
         assert np.all(np.diff(gpu_pages) > 0), "pages not ascending"
-        U, pages, k, _, _ = oracle_unit(w, inputs, b, h, s)
+        U, pages, k, _, _ = oracle_unit(w, inputs, b, h, s, agg=run.group_agg)
         n = len(U)
         if n > k:
             cand = U[:n - 1]
@@ -67,7 +68,7 @@ def check_step(run, inputs, s, units=None):
                 assert len(gpu_pages) == 1
         else:
             assert np.array_equal(gpu_pages, pages)
-        _, _, _, o_ref, l_ref = oracle_unit(w, inputs, b, h, s, gpu_pages)
+        _, _, _, o_ref, l_ref = oracle_unit(w, inputs, b, h, s, gpu_pages, agg=run.group_agg)
         err = max_abs(out[b, h * G:(h + 1) * G], o_ref)
         worst = max(worst, err)
         assert err <= tol, f"step {s} unit {u}: max-abs {err} > {tol}"
@@ -76,10 +77,11 @@ def check_step(run, inputs, s, units=None):
 
 
 def run_and_check(w, out_dtype=0, max_splits=None, steps=None, units=None, mode="step",
-                  step_tuning=None):
+                  step_tuning=None, group_agg=0):
     inputs = synth.quest_inputs(w)
     run = QuestRun(w, inputs, out_dtype=out_dtype, max_splits=max_splits, mode=mode,
                    step_tuning=step_tuning)
+    run.group_agg = group_agg
     worst = 0.0
     for s in range(w.steps):
         run.step(s)
@@ -285,3 +287,22 @@ def test_step_wait_that_runs_out_reports_timeout_and_resets():
 def se_status(ws):
     from kv_cache_decode_quest_gb300 import binding
     return binding.se_sync_status(ws)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 4, 128), (16, 2, 64), (8, 8, 128), (4, 1, 64),
+                                       (16, 8, 128), (2, 2, 64)])
+def test_max_aggregation_bound(hq, hkv, d):
+    """se_quest_select_ex with SE_AGG_MAX (the largest of the query heads'
+    bounds): selections against the oracle's max bound, outputs against the
+    oracle attention, with the append fused, over ragged contexts."""
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name=f"quest_max_g{hq // hkv}_d{d}", batch=3, num_q_heads=hq,
+                     num_kv_heads=hkv, head_dim=d, ctx=(777, 3000, 40), budget=(128, 512, 64),
+                     steps=3)
+    run_and_check(w, mode="fused", group_agg=1)
+
+
+def test_max_aggregation_full_size_sampled():
+    """The 16 x 32K workload with the max bound, steps 0 and 3."""
+    w = synth.scaled(synth.workloads()["quest_32k"], steps=4)
+    run_and_check(w, mode="fused", group_agg=1, steps={0, 3}, units=list(range(0, 64, 5)))
