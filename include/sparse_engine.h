@@ -168,14 +168,10 @@ typedef struct se_quest_step_opts {
     void* ev_kernel_begin;    /* NULL or a cudaEvent_t recorded right before / */
     void* ev_kernel_end;      /* right after the step kernel (timing only; captured
                                  as external event-record nodes in a graph) */
-    int32_t slice_pages;      /* candidate pages per scoring slice (0: about one
-                                 slice per resident block); speed only */
     int32_t wait_limit_ns;    /* bound of each wait of one block on another
                                  (0: 1 s); a wait that runs out sets
                                  SE_DEV_TIMEOUT and the step's results, its
                                  append included, are invalid */
-    int32_t groups;           /* sequence groups scored and decoded in turn,
-                                 0..4 (0: 1); speed only */
 } se_quest_step_opts;
 
 /* ---- library ------------------------------------------------------------ */
@@ -336,11 +332,12 @@ int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t tot
  *   q, budget_tokens, sel_pages, n_sel, view: as in se_quest_select;
  *   k_new, v_new: as in se_quest_select_append, or both NULL (no append);
  *   scale, out, lse: as in se_sparse_decode (out bf16 or fp32 by opts->out_dtype).
- * The kernel is one cooperative launch (every block resident at once).  The
- * sequences are taken in groups: each block scores a slice of one sequence's
- * page summaries per group, then decodes a piece of one unit per group; a
- * piece's top-k is computed by the block itself, once every page of that
- * sequence is scored, while its copy engine keeps streaming the next data.  The waits of one block on the others are bounded
+ * The kernel is one cooperative launch (every block resident at once).  Each
+ * block scores a slice of one sequence's page summaries (up to 32 sequences
+ * share the blocks in proportion to their candidate pages), then decodes
+ * pieces of units; a piece's top-k is computed by the block itself, once
+ * every page of that sequence is scored, while its copy engine keeps
+ * streaming the next data.  The waits of one block on the others are bounded
  * (opts->wait_limit_ns): one that runs out sets SE_DEV_TIMEOUT, leaves ctx_len
  * unchanged and the results invalid.  The last block to finish commits the new
  * lengths and clears the workspace's control words.

@@ -64,8 +64,7 @@ SE_AGG_SUM, SE_AGG_MAX = 0, 1
 class QuestStepOptsC(ctypes.Structure):
     _fields_ = [("out_dtype", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("ev_kernel_begin", ctypes.c_void_p), ("ev_kernel_end", ctypes.c_void_p),
-                ("slice_pages", ctypes.c_int32), ("wait_limit_ns", ctypes.c_int32),
-                ("groups", ctypes.c_int32)]
+                ("wait_limit_ns", ctypes.c_int32)]
 
 
 # C entry points: name -> (restype, argtypes)
@@ -333,15 +332,15 @@ def se_quest_select_ex(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads: in
 
 def se_quest_step(kv: PagedKV, k_new, v_new, q, batch: int, num_q_heads: int, budget_tokens,
                   scale: float, sel_pages, n_sel, view: View, out, lse, ws, out_dtype: int = 0,
-                  max_splits: int = 64, slice_pages: int = 0, wait_limit_ns: int = 0,
-                  groups: int = 0, ev_begin=None, ev_end=None, stream=None):
+                  max_splits: int = 64, wait_limit_ns: int = 0, ev_begin=None, ev_end=None,
+                  stream=None):
     """One Quest decode step (append when k_new/v_new are given, select, decode)
     in one kernel."""
     c, vc = kv.c, view.c
     opts = QuestStepOptsC(out_dtype, max_splits,
                           ev_begin.cuda_event if ev_begin is not None else None,
                           ev_end.cuda_event if ev_end is not None else None,
-                          slice_pages, wait_limit_ns, groups)
+                          wait_limit_ns)
     _check(load().se_quest_step(ctypes.byref(c), _p(k_new), _p(v_new), _p(q), batch, num_q_heads,
                                 _p(budget_tokens), scale, ctypes.byref(opts), _p(sel_pages),
                                 _p(n_sel), ctypes.byref(vc), _p(out), _p(lse), _p(ws), ws.numel(),

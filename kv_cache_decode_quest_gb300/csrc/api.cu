@@ -268,17 +268,16 @@ int se_quest_step(const se_paged_kv* kv, const void* k_new, const void* v_new, c
     if (batch > kStepMaxBatch || batch * kv->num_kv_heads > kStepMaxUnits ||
         kv->max_pages_per_seq > 16384)
         return SE_ERR_UNSUPPORTED;
-    se_quest_step_opts o = {0, SE_MAX_SPLITS, nullptr, nullptr, 0, 0, 0};
+    se_quest_step_opts o = {0, SE_MAX_SPLITS, nullptr, nullptr, 0};
     if (opts) {
         o = *opts;
         if (o.max_splits == 0) o.max_splits = SE_MAX_SPLITS;
     }
     if (o.out_dtype != 0 && o.out_dtype != 1) return SE_ERR_INVALID_ARG;
     if (o.max_splits < 1 || o.max_splits > SE_MAX_SPLITS) return SE_ERR_INVALID_ARG;
-    if (o.slice_pages < 0 || o.wait_limit_ns < 0 || o.groups < 0 || o.groups > 4)
-        return SE_ERR_INVALID_ARG;
+    if (o.wait_limit_ns < 0) return SE_ERR_INVALID_ARG;
     const int G = num_q_heads / kv->num_kv_heads;
-    if (quest_step_smem_bytes(batch, kv->num_kv_heads, kv->head_dim, G) > 227 * 1024)
+    if (quest_step_smem_bytes(kv->num_kv_heads, kv->head_dim, G) > 227 * 1024)
         return SE_ERR_UNSUPPORTED;
     // a unit with more than 2048 candidate pages is selected by the consumer
     // warps, which stage its keys in the idle stage ring
@@ -293,7 +292,7 @@ int se_quest_step(const se_paged_kv* kv, const void* k_new, const void* v_new, c
         o.wait_limit_ns > 0 ? (unsigned long long)o.wait_limit_ns : 1000000000ull;
     return cuda_status(launch_quest_step(
         *kv, k_new, v_new, q, batch, num_q_heads, budget_tokens, scale, o.out_dtype, o.max_splits,
-        o.slice_pages, o.groups, wait_ns, sel_pages, n_sel, *view, out, lse, ws,
+        wait_ns, sel_pages, n_sel, *view, out, lse, ws,
         static_cast<cudaEvent_t>(o.ev_kernel_begin), static_cast<cudaEvent_t>(o.ev_kernel_end),
         static_cast<cudaStream_t>(stream)));
 }

@@ -66,12 +66,12 @@ cudaError_t launch_quest_select(const se_paged_kv& kv, const void* q, int batch,
 constexpr int kStepMaxBatch = 1024;
 constexpr int kStepMaxUnits = 4096;
 size_t quest_step_ws_bytes(int batch, int H, int G, int D, int max_pages, int max_splits);
-size_t quest_step_smem_bytes(int batch, int H, int D, int G);
+size_t quest_step_smem_bytes(int H, int D, int G);
 size_t quest_step_ring_bytes(int D, int G);
 cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const void* v_new,
                               const void* q, int batch, int num_q_heads, const int32_t* budget,
-                              float scale, int out_dtype, int max_splits, int item_pages,
-                              int groups, unsigned long long wait_ns, int32_t* sel_pages,
+                              float scale, int out_dtype, int max_splits,
+                              unsigned long long wait_ns, int32_t* sel_pages,
                               int32_t* n_sel,
                               const se_view& view, void* out, float* lse, void* ws,
                               cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t s);

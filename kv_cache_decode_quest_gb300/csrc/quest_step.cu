@@ -11,14 +11,16 @@
 // selected K/V rows) joined by a short, latency-bound top-k per unit.  As
 // separate launches every kernel boundary, the top-k kernel and the decode's
 // planning sit on the critical path.  Here every CTA of one resident wave (a
-// cooperative launch, so every CTA is running) follows the same static
-// schedule, computed by each CTA from the sequence lengths and budgets.  The
-// sequences are cut into groups; for each group in turn:
+// cooperative launch, so every CTA is running) follows a static schedule that
+// it computes itself:
 //   score: one contiguous slice of one sequence's candidate page summaries
-//     (all KV heads of each page), streamed with 1-D bulk copies through the
-//     stage ring and turned into order-preserving keys in the workspace; the
-//     slice's page count is then added to the sequence's scored counter;
-// and then, for each group in turn:
+//     (all KV heads of each page), derived from the lengths and budgets alone
+//     so that the first copy leaves at once; streamed with 1-D bulk copies
+//     through the stage ring and turned into order-preserving keys in the
+//     workspace; the slice's page count is then added to the sequence's
+//     scored counter;
+//   plan: once its own slices are scored (while the other CTAs finish
+//     theirs), the decode pieces, the same split plan in every CTA;
 //   decode piece: a range of chunks of one unit u = (b, h), streamed with 2-D
 //     TMA into the same ring for the mma.sync decode of decode_core.cuh; split
 //     units are merged by the last piece to finish.
@@ -26,20 +28,19 @@
 // the exact top-k of u itself from the keys in L2 (every piece of u computes
 // the same selection; none waits on another's), writes its ranks of the
 // selection and of the view, and releases the producer.  When no unit has more
-// than 2048 candidate pages, the CTA's selector warp does this while the other
-// warps stream, so one group's top-k runs while the next group is scored (and
-// the last group's while the first decodes); otherwise the four consumer warps
-// do it between the phases, with one group.  The new token's row is written by
-// the piece that holds the unit's last chunk (the forced last page), before
-// that chunk's copy.  The last CTA to finish commits ctx_len + 1 of every
-// sequence whose token was appended (every CTA has read the old lengths by
-// then) and clears the control words.  Waits are bounded: a CTA that gives up
-// records SE_DEV_TIMEOUT and raises a global abort word that the other waits
-// poll; every CTA still walks the same barriers to the end.
+// than 2048 candidate pages, the consumers select all the CTA's pieces first,
+// in shared memory, while the producer already streams the first pieces'
+// chunks; otherwise each selection runs in the idle stage ring right before
+// its piece.  The new token's row is written by the piece that holds the
+// unit's last chunk (the forced last page), before that chunk's copy.  The
+// last CTA to finish commits ctx_len + 1 of every sequence whose token was
+// appended (every CTA has read the old lengths by then) and clears the
+// control words.  Waits are bounded: a CTA that gives up records
+// SE_DEV_TIMEOUT and raises a global abort word that the other waits poll;
+// every CTA still walks the same barriers to the end.
 //
-// CTA layout (192 threads): warps 0-3 consume (stage s is handled by warp
-// (stage sequence % 4), in both phases), warp 4 is the producer, warp 5 the
-// selector.
+// CTA layout (160 threads): warps 0-3 consume (stage s is handled by warp
+// (stage sequence % 4), in both phases), warp 4 is the producer.
 #include <algorithm>
 
 #include "append.cuh"
@@ -56,8 +57,6 @@ constexpr int kStepThreads = (kConsumerWarps + 1) * 32;
 constexpr int kDigit = 10, kStepBins = 1 << kDigit;     // top-k: 10-bit radix digits
 constexpr int kMaxPieces = 32;                          // decode pieces per CTA at most
 constexpr int kMaxScoreItems = 8;                       // score slices per CTA at most
-constexpr int kMinItemPages = 8;
-constexpr int kMaxGroups = 4;
 constexpr int kAreaKeys = 2048;                         // keys a unit's top-k holds outside the ring
 // the top-k's shared memory: histogram, small ints, keys
 constexpr int kSelectBytes = kStepBins * 4 + 64 * 4;
@@ -84,8 +83,7 @@ struct StepParams {
     int* sync;                          // [0] CTAs finished, [1] abort
     float* o_part;                      // [units * max_splits][G][D]
     float* lse_part;                    // [units * max_splits][G]
-    int max_splits, item_pages;         // item_pages 0: about one slice per CTA and group
-    int groups;                         // sequence groups asked for, 1..kMaxGroups
+    int max_splits;
     int off_union;                      // union area offset in dynamic shared memory
     int64_t total_rows;
     unsigned long long wait_ns;
@@ -100,11 +98,12 @@ struct StepShape {
     static constexpr int kSumBytes = 2 * D * 2;                        // one (page, head) summary
     static constexpr int kSumsPerStage = kStageBytes / kSumBytes;      // 16
     static_assert(kStages % kConsumerWarps == 0, "stage ownership needs kStages % 4 == 0");
-    // small areas after the ring: full/empty barriers, two plan barriers,
-    // the pieces' ready barriers, stage token counts, misc ints, the CTA's
-    // pieces (item, sequence values, unit range) and score slices
+    // small areas after the ring: full/empty barriers, the plan barrier (and
+    // 8 bytes of padding), the pieces' ready barriers, stage token counts,
+    // misc ints, the CTA's pieces (item, sequence values, unit range) and its
+    // score slices (the consumers' and the producer's copies)
     static constexpr int kFixed = kStages * 16 + 16 + kMaxPieces * 8 + kStages * 4 + 64 * 4 +
-                                  kMaxPieces * 32 + kMaxScoreItems * 16;
+                                  kMaxPieces * 32 + 2 * kMaxScoreItems * 16;
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -468,160 +467,196 @@ __device__ __forceinline__ void score_stage(const StepParams& p, const uint8_t* 
     }
 }
 
-// Plans, the same in every CTA, each computed by one warp.  Group g holds
-// sequences [g*batch/groups, (g+1)*batch/groups).
-__device__ __forceinline__ int group_begin(const StepParams& p, int groups, int g) {
-    return (int)((long long)g * p.batch / groups);
+// score_stage with the lane's coefficients in registers (kPerStage summaries
+// per full stage).  When H (a power of two) divides the summaries of one
+// warp-wide read, lane (slot, sub) always reads head slot % H and the same
+// channel vectors j*kLps + sub, so its 32 coefficients are loaded once per
+// slice (coef_regs) and a stage costs shared memory nothing but the
+// summaries' own bytes.  The stage's kPerStage / kR reads are independent
+// chains, computed together with no branch between them (a partial last stage
+// reads stale bytes past nsum and stores no key for them); each chain sums in
+// the order of score_stage.  krow: the lane's key row at the stage's first
+// page, (b*H + slot%H)*kstride + p0 + t0/H + slot/H.
+template <int D>
+__device__ __forceinline__ bool coef_in_regs(int H) {
+    return (H & (H - 1)) == 0 && (32 / (D / 16)) % H == 0;
+}
+template <int D>
+__device__ __forceinline__ void coef_regs(const float* coef, int H, int lane, float (&cr)[32]) {
+    constexpr int kLps = D / 16;
+    const int sub = lane % kLps, h = (lane / kLps) % H;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float4* cf = reinterpret_cast<const float4*>(coef + h * 2 * D + (j * kLps + sub) * 8);
+        const float4 c0 = cf[0], c1 = cf[1];
+        cr[j * 8 + 0] = c0.x;
+        cr[j * 8 + 1] = c0.y;
+        cr[j * 8 + 2] = c0.z;
+        cr[j * 8 + 3] = c0.w;
+        cr[j * 8 + 4] = c1.x;
+        cr[j * 8 + 5] = c1.y;
+        cr[j * 8 + 6] = c1.z;
+        cr[j * 8 + 7] = c1.w;
+    }
+}
+template <int D, int kPerStage>
+__device__ __forceinline__ void score_stage_regs(const uint8_t* st, int nsum, uint32_t* krow,
+                                                 int lgH, const float (&cr)[32], int lane) {
+    constexpr int kLps = D / 16;
+    constexpr int kR = 32 / kLps;
+    constexpr int kSum = 2 * D * 2;
+    constexpr int kIt = kPerStage / kR;
+    const int sub = lane % kLps, slot = lane / kLps;
+    float acc[kIt];
+#pragma unroll
+    for (int r = 0; r < kIt; ++r) acc[r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 w[kIt];
+#pragma unroll
+        for (int r = 0; r < kIt; ++r)
+            w[r] = reinterpret_cast<const uint4*>(st + (r * kR + slot) * kSum)[j * kLps + sub];
+#pragma unroll
+        for (int r = 0; r < kIt; ++r) {
+            acc[r] = fmaf(cr[j * 8 + 0], bf_lo(w[r].x), acc[r]);
+            acc[r] = fmaf(cr[j * 8 + 1], bf_hi(w[r].x), acc[r]);
+            acc[r] = fmaf(cr[j * 8 + 2], bf_lo(w[r].y), acc[r]);
+            acc[r] = fmaf(cr[j * 8 + 3], bf_hi(w[r].y), acc[r]);
+            acc[r] = fmaf(cr[j * 8 + 4], bf_lo(w[r].z), acc[r]);
+            acc[r] = fmaf(cr[j * 8 + 5], bf_hi(w[r].z), acc[r]);
+            acc[r] = fmaf(cr[j * 8 + 6], bf_lo(w[r].w), acc[r]);
+            acc[r] = fmaf(cr[j * 8 + 7], bf_hi(w[r].w), acc[r]);
+        }
+    }
+#pragma unroll
+    for (int o = kLps / 2; o >= 1; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < kIt; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+    if (sub == 0) {
+#pragma unroll
+        for (int r = 0; r < kIt; ++r)
+            if (r * kR + slot < nsum) krow[(r * kR) >> lgH] = float_key(acc[r]);
+    }
 }
 
-// The schedule's mode: when no unit has more than kAreaKeys candidate pages,
-// the `groups` groups are used and a unit's top-k holds its keys in the union
-// area of shared memory (the stage ring keeps streaming meanwhile); else one
-// group, and the top-k holds them in the idle stage ring.  Returns the groups;
-// *in_area the mode.
-__device__ int step_mode(const StepParams& p, const int2* sseq, int lane, int* in_area) {
+// This CTA's scoring slices, from the lengths and budgets alone (no plan
+// step, so the first copy goes out at once); one warp, v = (ctx_len, budget)
+// of sequence `lane` when batch <= 32.  Up to 32 sequences share the grid in
+// proportion to their candidate pages m_b: sequence b owns the consecutive
+// CTAs from start_b = b + floor((grid - batch) * (m_0 + ... + m_{b-1}) / M)
+// (at least one each), which split its pages evenly.  Up to `grid` sequences
+// own grid / batch CTAs each (+1 for the first grid % batch); with more
+// sequences than CTAs, CTA c scores sequences c, c + grid, ... whole.  Lane 0
+// writes (b, first page, end page) of each non-empty slice; returns their
+// count (at most kMaxScoreItems, which the launch guarantees).
+__device__ int my_slices(const StepParams& p, int lane, int2 v, int4* items) {
+    const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
     const int cap = p.kv.max_pages_per_seq * kPage;
     const bool pending = p.k_new != nullptr;
+    int cnt = 0;
+    if (p.batch <= 32 && p.batch <= grid) {
+        const int m = lane < p.batch ? seq_vals(v.x, v.y, cap, pending).m : 0;
+        const long long pre = warp_excl_scan(m, lane);
+        const long long M = __reduce_add_sync(0xffffffffu, m);
+        const int start = lane + (M > 0 ? (int)((long long)(grid - p.batch) * pre / M) : 0);
+        const unsigned own = __ballot_sync(0xffffffffu, lane < p.batch && start <= c);
+        const int b = 31 - __clz(own);                   // start_0 = 0 <= c
+        const int sb = __shfl_sync(0xffffffffu, start, b);
+        const int nx = __shfl_sync(0xffffffffu, start, min(b + 1, 31));
+        const int mb = __shfl_sync(0xffffffffu, m, b);
+        const int nb = (b + 1 < p.batch ? nx : grid) - sb, j = c - sb;
+        const int p0 = (int)((long long)mb * j / nb), p1 = (int)((long long)mb * (j + 1) / nb);
+        if (lane == 0 && p1 > p0) items[0] = make_int4(b, p0, p1, 0);
+        cnt = p1 > p0;
+    } else if (p.batch <= grid) {
+        const int per = grid / p.batch, extra = grid % p.batch;
+        const int b = c < extra * (per + 1) ? c / (per + 1) : extra + (c - extra * (per + 1)) / per;
+        const int sb = b < extra ? b * (per + 1) : extra * (per + 1) + (b - extra) * per;
+        const int nb = per + (b < extra ? 1 : 0), j = c - sb;
+        const int m = seq_vals(p.kv.ctx_len[b], p.budget[b], cap, pending).m;
+        const int p0 = (int)((long long)m * j / nb), p1 = (int)((long long)m * (j + 1) / nb);
+        if (lane == 0 && p1 > p0) items[0] = make_int4(b, p0, p1, 0);
+        cnt = p1 > p0;
+    } else {
+        // lane i looks at sequence c + i * grid
+        const int b = c + lane * grid;
+        const int m = lane < kMaxScoreItems && b < p.batch
+                          ? seq_vals(p.kv.ctx_len[b], p.budget[b], cap, pending).m
+                          : 0;
+        const unsigned has = __ballot_sync(0xffffffffu, m > 0);
+        if (m > 0) items[__popc(has & ((1u << lane) - 1))] = make_int4(b, 0, m, 0);
+        cnt = __popc(has);
+    }
+    __syncwarp();
+    return cnt;
+}
+
+// Sequence b's step values from its ctx_len and budget (L1-cached loads: both
+// stay unchanged until the last CTA commits the new lengths).
+__device__ __forceinline__ SeqVals seq_of(const StepParams& p, int b) {
+    return seq_vals(p.kv.ctx_len[b], p.budget[b], p.kv.max_pages_per_seq * kPage,
+                    p.k_new != nullptr);
+}
+
+// Where a unit's top-k keeps its keys: in the union area of shared memory when
+// no unit has more than kAreaKeys candidate pages (every selection of the CTA
+// then runs before its decodes, while the ring streams), else in the idle
+// stage ring, right before each piece's decode.  One warp.
+__device__ int keys_in_area(const StepParams& p, int lane) {
     int mx = 0;
 #pragma unroll 1
-    for (int b = lane; b < p.batch; b += 32) {
-        const int2 x = sseq[b];
-        mx = max(mx, seq_vals(x.x, x.y, cap, pending).m);
-    }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    *in_area = mx <= kAreaKeys;
-    return mx <= kAreaKeys ? p.groups : 1;
+    for (int b = lane; b < p.batch; b += 32) mx = max(mx, seq_of(p, b).m);
+    return __reduce_max_sync(0xffffffffu, mx) <= kAreaKeys;
 }
 
-// Score slices: in each group, every sequence's candidate pages are cut into
-// slices of P pages (the last one shorter), P = the option, else about the
-// group's candidates over the grid, doubled until the slices fit
-// kMaxScoreItems / groups rounds of the grid; slice t of a group (in sequence
-// order) is run by CTA t % grid.  Writes this CTA's slices (b, first page, end
-// page), group by group, and returns their count.
-__device__ int plan_score(const StepParams& p, const int2* sseq, int groups, int lane,
-                          int4* items, int* per_group) {
+// Decode pieces, the same in every CTA (one warp): unit u gets pieces_u =
+// max(1, min(max_splits, nc_u, floor(nc_u * share / total))) pieces of
+// nc_u * k / pieces_u chunks, share lowered from slots = grid * ceil(units /
+// grid) until the pieces fit the slots; piece t (in unit order) is run by CTA
+// t % grid and owns the partial slot t.  Writes this CTA's pieces (unit, first
+// chunk, end chunk, partial slot or -1) and their units' (first slot, pieces),
+// and returns their count.
+__device__ int plan_decode(const StepParams& p, int lane, int4* items, int2* uitems) {
     const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    const int cap = p.kv.max_pages_per_seq * kPage;
-    const bool pending = p.k_new != nullptr;
-    const int per_cta = kMaxScoreItems / groups;
-    auto m_of = [&](int b) {
-        const int2 x = sseq[b];
-        return seq_vals(x.x, x.y, cap, pending).m;
+    const int H = p.kv.num_kv_heads, units = p.units;
+    auto nc_of = [&](int u) { return seq_of(p, u / H).chunks; };
+    int total = 0;
+#pragma unroll 1
+    for (int base = 0; base < units; base += 32)
+        total += __reduce_add_sync(0xffffffffu, base + lane < units ? nc_of(base + lane) : 0);
+    const int tot = max(1, total);
+    const int slots = grid * ((units + grid - 1) / grid);
+    auto pieces_of = [&](int nc, int share) {
+        return nc == 0 ? 1
+                       : max(1, min(p.max_splits, min(nc, (int)((long long)nc * share / tot))));
     };
-    int cnt = 0;
+    int share = slots, run = 0;
 #pragma unroll 1
-    for (int g = 0; g < groups; ++g) {
-        const int b0 = group_begin(p, groups, g), b1 = group_begin(p, groups, g + 1);
-        long long M = 0;
+    for (int iter = 0; iter < 6; ++iter) {
+        run = 0;
 #pragma unroll 1
-        for (int base = b0; base < b1; base += 32)
-            M += __reduce_add_sync(0xffffffffu, base + lane < b1 ? m_of(base + lane) : 0);
-        if (lane == 0) per_group[g] = 0;
-        if (M == 0) continue;
-        int P = p.item_pages > 0 ? p.item_pages : max(kMinItemPages, (int)((M + grid - 1) / grid));
-#pragma unroll 1
-        for (int iter = 0; iter < 24; ++iter) {
-            int total = 0;
-#pragma unroll 1
-            for (int base = b0; base < b1; base += 32) {
-                const int m = base + lane < b1 ? m_of(base + lane) : 0;
-                total += __reduce_add_sync(0xffffffffu, (m + P - 1) / P);
-            }
-            if (total <= grid * per_cta) break;
-            P *= 2;
-        }
-        int run = 0;
-#pragma unroll 1
-        for (int base = b0; base < b1; base += 32) {
-            const int b = base + lane;
-            const int m = b < b1 ? m_of(b) : 0;
-            const int ni = (m + P - 1) / P;
-            const int off = run + warp_excl_scan(ni, lane);
-            // this CTA's slices c, c + grid, ... that fall in sequence b
-            for (int t = c; t < off + ni; t += grid) {
-                if (t >= off && (t - c) / grid < per_cta) {
-                    const int k = t - off;
-                    items[cnt + (t - c) / grid] = make_int4(b, k * P, min(m, (k + 1) * P), 0);
-                }
-            }
-            run += __reduce_add_sync(0xffffffffu, ni);
-        }
-        const int mine = min(per_cta, run > c ? (run - c + grid - 1) / grid : 0);
-        if (lane == 0) per_group[g] = mine;
-        cnt += mine;
-    }
-    return cnt;
-}
-
-// Decode pieces: in each group, unit u gets pieces_u = max(1, min(max_splits,
-// nc_u, floor(nc_u * share / total))) pieces of nc_u * k / pieces_u chunks,
-// share lowered from slots = grid * ceil(units / grid) until the pieces fit the
-// slots; piece t of a group (in unit order) is run by CTA t % grid and owns the
-// partial slot base + t.  Writes this CTA's pieces (unit, first chunk, end
-// chunk, partial slot or -1) and their units' (first slot, pieces), group by
-// group, and returns their count.
-__device__ int plan_decode(const StepParams& p, const int2* sseq, int groups, int lane,
-                           int4* items, int2* uitems, int* per_group) {
-    const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    const int H = p.kv.num_kv_heads;
-    const int cap = p.kv.max_pages_per_seq * kPage;
-    const bool pending = p.k_new != nullptr;
-    const int per_cta = kMaxPieces / groups;
-    auto nc_of = [&](int u) {
-        const int2 x = sseq[u / H];
-        return seq_vals(x.x, x.y, cap, pending).chunks;
-    };
-    int cnt = 0, base_slot = 0;
-#pragma unroll 1
-    for (int g = 0; g < groups; ++g) {
-        const int u0 = group_begin(p, groups, g) * H, u1 = group_begin(p, groups, g + 1) * H;
-        const int units = u1 - u0;
-        if (lane == 0) per_group[g] = 0;
-        if (units == 0) continue;
-        int total = 0;
-#pragma unroll 1
-        for (int base = u0; base < u1; base += 32)
-            total += __reduce_add_sync(0xffffffffu, base + lane < u1 ? nc_of(base + lane) : 0);
-        const int tot = max(1, total);
-        const int slots = grid * ((units + grid - 1) / grid);
-        auto pieces_of = [&](int nc, int share) {
-            return nc == 0 ? 1
-                           : max(1, min(p.max_splits, min(nc, (int)((long long)nc * share / tot))));
-        };
-        int share = slots, run = 0;
-#pragma unroll 1
-        for (int iter = 0; iter < 6; ++iter) {
-            run = 0;
-#pragma unroll 1
-            for (int base = u0; base < u1; base += 32) {
-                const int u = base + lane;
-                const int nc = u < u1 ? nc_of(u) : 0;
-                const int pc = u < u1 ? pieces_of(nc, share) : 0;
-                const int off = run + warp_excl_scan(pc, lane);
-                if (u < u1) {
-                    for (int t = c; t < off + pc; t += grid) {
-                        if (t >= off && (t - c) / grid < per_cta) {
-                            const int j = cnt + (t - c) / grid, k = t - off;
-                            items[j] = make_int4(u, (int)((long long)nc * k / pc),
-                                                 (int)((long long)nc * (k + 1) / pc),
-                                                 pc == 1 ? -1 : base_slot + t);
-                            uitems[j] = make_int2(base_slot + off, pc);
-                        }
+        for (int base = 0; base < units; base += 32) {
+            const int u = base + lane;
+            const int nc = u < units ? nc_of(u) : 0;
+            const int pc = u < units ? pieces_of(nc, share) : 0;
+            const int off = run + warp_excl_scan(pc, lane);
+            if (u < units) {
+                for (int t = c; t < off + pc; t += grid) {
+                    if (t >= off && (t - c) / grid < kMaxPieces) {
+                        const int j = (t - c) / grid, k = t - off;
+                        items[j] = make_int4(u, (int)((long long)nc * k / pc),
+                                             (int)((long long)nc * (k + 1) / pc), pc == 1 ? -1 : t);
+                        uitems[j] = make_int2(off, pc);
                     }
                 }
-                run += __reduce_add_sync(0xffffffffu, pc);
             }
-            __syncwarp();
-            if (run <= slots || share == 0) break;        // share 0: one piece per unit
-            share = iter == 4 ? 0 : max(0, share - (run - slots));
+            run += __reduce_add_sync(0xffffffffu, pc);
         }
-        const int mine = min(per_cta, run > c ? (run - c + grid - 1) / grid : 0);
-        if (lane == 0) per_group[g] = mine;
-        cnt += mine;
-        base_slot += run;
+        __syncwarp();
+        if (run <= slots || share == 0) break;            // share 0: one piece per unit
+        share = iter == 4 ? 0 : max(0, share - (run - slots));
     }
-    return cnt;
+    return min(kMaxPieces, run > c ? (run - c + grid - 1) / grid : 0);
 }
 
 template <int D, int NT, bool TWO_TERM>
@@ -637,22 +672,20 @@ __global__ void __launch_bounds__(kStepThreads, 2)
     uint8_t* ring = base;
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + NS * SS::kStageBytes);
     uint64_t* empty = full + NS;
-    uint64_t* planbar = empty + NS;                            // [0] slices, [1] pieces
+    uint64_t* planbar = empty + NS;                            // the pieces (+ 8 bytes pad)
     uint64_t* pready = planbar + 2;                            // [kMaxPieces] view rows written
     int* stage_ntok = reinterpret_cast<int*>(pready + kMaxPieces);
     int* misc = stage_ntok + NS;                               // 64 ints
     volatile int* abort_flag = misc;                           // [0]
     // [1] last-piece flag of the merge, [3] last CTA, [4] score slices,
-    // [5] pieces, [6] top-k in the union area, [8..12) slices per group,
-    // [12..16) pieces per group
+    // [5] pieces, [6] top-k in the union area
     int4* pitem = reinterpret_cast<int4*>(misc + 64);          // [kMaxPieces]
     int2* pseq = reinterpret_cast<int2*>(pitem + kMaxPieces);  // [kMaxPieces] held, budget
     int2* puit = pseq + kMaxPieces;                            // [kMaxPieces]
-    int4* sitem = reinterpret_cast<int4*>(puit + kMaxPieces);  // [kMaxScoreItems]
-    // the union area, in turn: the staged lengths, the query coefficients
-    // and the top-k (which never overlap), then the decode merge
+    int4* sitem = reinterpret_cast<int4*>(puit + kMaxPieces);  // [kMaxScoreItems] consumers'
+    int4* psitem = sitem + kMaxScoreItems;                     // [kMaxScoreItems] producer's
+    // the union area, in turn: the query coefficients, the top-k, the merge
     uint8_t* uni = base + p.off_union;
-    int2* sseq = reinterpret_cast<int2*>(uni);                 // [batch] (ctx_len, budget)
     float* coef = reinterpret_cast<float*>(uni);               // [H][2][D]
     float* merge = reinterpret_cast<float*>(uni);
 
@@ -661,44 +694,33 @@ __global__ void __launch_bounds__(kStepThreads, 2)
     const int cap = stride * kPage;
     const bool pending = p.k_new != nullptr;
     const int segs = D / 8;
+    // (ctx_len, budget) of sequence `lane` (producer) or `threadIdx.x`
+    // (consumers), loaded before anything waits on them
+    const int vb = warp == kProducerWarp ? lane : static_cast<int>(threadIdx.x);
+    const int2 v = vb < p.batch ? make_int2(p.kv.ctx_len[vb], p.budget[vb]) : make_int2(0, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(&planbar[0], 1);
-        mbar_init(&planbar[1], 1);
         for (int j = 0; j < kMaxPieces; ++j) mbar_init(&pready[j], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    // every sequence's (ctx_len, budget), one load each, all in flight
-    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
-        const int held = p.kv.ctx_len[b], bud = p.budget[b];
-        sseq[b] = make_int2(held, bud);
-        if (blockIdx.x == 0) {
-            if (held < 0 || held > cap) flag(p.status, SE_DEV_BAD_LENGTH);
-            else if (pending && held >= cap) flag(p.status, SE_DEV_CAPACITY);
-        }
-    }
     __syncthreads();
-    auto plan_wait = [&](int i) {
-        if (!*abort_flag && !mbar_wait(&planbar[i], 0, abort_flag)) give_up(p, abort_flag);
-    };
 
     if (warp == kProducerWarp) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
-            plan_wait(0);
         }
-        __syncwarp();
-        const int nscore = *abort_flag ? 0 : misc[4];
+        const int nscore = my_slices(p, lane, v, psitem);
         uint32_t seq = 0;
         // the score slices: each one contiguous block of summaries, 1-D bulk copies
         for (int i = 0; i < nscore; ++i) {
-            const int4 it = sitem[i];
+            const int4 it = psitem[i];
             const int64_t bytes = (int64_t)(it.z - it.y) * H * SS::kSumBytes;
             const uint8_t* src = static_cast<const uint8_t*>(p.kv.meta) +
                                  ((int64_t)it.x * stride + it.y) * H * SS::kSumBytes;
@@ -724,9 +746,9 @@ __global__ void __launch_bounds__(kStepThreads, 2)
         }
         // the decode pieces, each once the consumers have written its view
         // rows (and the new token's row)
-        if (lane == 0) plan_wait(1);
+        if (lane == 0 && !*abort_flag && !mbar_wait(&planbar[0], 0, abort_flag)) give_up(p, abort_flag);
         __syncwarp();
-        const int npieces = misc[5];
+        const int npieces = *abort_flag ? 0 : misc[5];
         const uint64_t kv_policy = l2_evict_first();
         for (int j = 0; j < npieces; ++j) {
             if (lane == 0 && !*abort_flag && !mbar_wait(&pready[j], 0, abort_flag))
@@ -789,41 +811,82 @@ __global__ void __launch_bounds__(kStepThreads, 2)
     } else {
         // -------------------------------- consumers --------------------------------
         const int ctid = threadIdx.x;
-        // the plans: the score slices by warp 0, the pieces by warp 1; each
-        // published through its own mbarrier (release / acquire in the CTA)
+        // the plans, while the first summaries are on their way: the score
+        // slices by warp 0, the decode pieces by warp 1 (published to the
+        // producer through the plan barrier)
         if (warp == 0) {
-            int in_area = 0;
-            const int groups = step_mode(p, sseq, lane, &in_area);
-            const int n = plan_score(p, sseq, groups, lane, sitem, misc + 8);
-            __syncwarp();
-            if (lane == 0) {
-                misc[4] = n;
-                misc[6] = in_area;
-                mbar_arrive(&planbar[0]);
-            }
+            const int n = my_slices(p, lane, v, sitem);
+            if (lane == 0) misc[4] = n;
         } else if (warp == 1) {
-            int in_area = 0;
-            const int groups = step_mode(p, sseq, lane, &in_area);
-            const int n = plan_decode(p, sseq, groups, lane, pitem, puit, misc + 12);
+            const int in_area = keys_in_area(p, lane);
+            const int n = plan_decode(p, lane, pitem, puit);
             __syncwarp();
-            for (int j = lane; j < n; j += 32) pseq[j] = sseq[pitem[j].x / H];
+            for (int j = lane; j < n; j += 32) {
+                const int b = pitem[j].x / H;
+                pseq[j] = make_int2(p.kv.ctx_len[b], p.budget[b]);
+            }
             __syncwarp();
             if (lane == 0) {
                 misc[5] = n;
-                mbar_arrive(&planbar[1]);
+                misc[6] = in_area;
+                mbar_arrive(&planbar[0]);
             }
         }
-        if (lane == 0) {
-            plan_wait(0);
-            plan_wait(1);
+        if (blockIdx.x == 0) {
+            for (int b = ctid; b < p.batch; b += kCThreads) {
+                const int held = b == ctid ? v.x : p.kv.ctx_len[b];
+                if (held < 0 || held > cap) flag(p.status, SE_DEV_BAD_LENGTH);
+                else if (pending && held >= cap) flag(p.status, SE_DEV_CAPACITY);
+            }
         }
-        __syncwarp();
-        consumer_bar();                                  // both plans seen before the first fold
-        const int nscore = *abort_flag ? 0 : misc[4];
+        consumer_bar();
+        const int nscore = misc[4];
+        const bool regs = coef_in_regs<D>(H);
+        const int lgH = 31 - __clz(H);
+        uint32_t seq = 0;
+        int folded = -1;
+        float cr[32];
+        for (int si = 0; si < nscore; ++si) {
+            const int4 it = sitem[si];
+            const int b = it.x;
+            if (b != folded) {
+                consumer_bar();                          // the previous reads of the union area
+                step_fold<D>(p, b, coef, ctid);
+                consumer_bar();
+                if (regs) coef_regs<D>(coef, H, lane, cr);
+                folded = b;
+            }
+            const int nsum_all = (it.z - it.y) * H;
+            const int nst = (nsum_all + SS::kSumsPerStage - 1) / SS::kSumsPerStage;
+            for (int j = 0; j < nst; ++j, ++seq) {
+                if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
+                const int s = seq % NS;
+                if (lane == 0 && !*abort_flag && !mbar_wait(&full[s], (seq / NS) & 1, abort_flag))
+                    give_up(p, abort_flag);
+                __syncwarp();
+                if (!*abort_flag) {
+                    const uint8_t* stg = ring + s * SS::kStageBytes;
+                    const int ns = min(SS::kSumsPerStage, nsum_all - j * SS::kSumsPerStage);
+                    if (regs) {
+                        const int t0 = j * SS::kSumsPerStage, sl = lane / (D / 16);
+                        uint32_t* krow = p.keys + ((int64_t)b * H + (sl & (H - 1))) * p.kstride +
+                                         it.y + (t0 >> lgH) + (sl >> lgH);
+                        score_stage_regs<D, SS::kSumsPerStage>(stg, ns, krow, lgH, cr, lane);
+                    } else
+                        score_stage<D>(p, stg, ns, j * SS::kSumsPerStage, b, it.y, coef, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            // every key of the slice is written: publish the slice's pages
+            consumer_bar();
+            if (ctid == 0) {
+                __threadfence();
+                atomicAdd(p.seq_scored + b, it.z - it.y);
+            }
+        }
         const int npieces = misc[5];
         const bool in_area = misc[6] != 0;
-        const int groups = in_area ? p.groups : 1;
-        uint32_t seq = 0;
         // the top-k of piece j (its ranks of the selection, its view rows, the
         // new token's row), then the producer is released for it
         auto select_piece = [&](int j, uint8_t* area) {
@@ -858,50 +921,11 @@ __global__ void __launch_bounds__(kStepThreads, 2)
             consumer_bar();
             if (ctid == 0) mbar_arrive(&pready[j]);
         };
-        int si = 0, pj = 0, folded = -1;
-        for (int g = 0; g < groups; ++g) {
-            const int ns_g = misc[8 + g];
-            for (int k = 0; k < ns_g && si < nscore; ++k, ++si) {
-                const int4 it = sitem[si];
-                const int b = it.x;
-                if (b != folded) {
-                    consumer_bar();                      // the previous reads of the union area
-                    step_fold<D>(p, b, coef, ctid);
-                    consumer_bar();
-                    folded = b;
-                }
-                const int nsum_all = (it.z - it.y) * H;
-                const int nst = (nsum_all + SS::kSumsPerStage - 1) / SS::kSumsPerStage;
-                for (int j = 0; j < nst; ++j, ++seq) {
-                    if ((seq % kConsumerWarps) != (uint32_t)warp) continue;
-                    const int s = seq % NS;
-                    if (lane == 0 && !*abort_flag && !mbar_wait(&full[s], (seq / NS) & 1, abort_flag))
-                        give_up(p, abort_flag);
-                    __syncwarp();
-                    if (!*abort_flag)
-                        score_stage<D>(p, ring + s * SS::kStageBytes,
-                                       min(SS::kSumsPerStage, nsum_all - j * SS::kSumsPerStage),
-                                       j * SS::kSumsPerStage, b, it.y, coef, lane);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[s]);
-                }
-                // every key of the slice is written: publish the slice's pages
-                consumer_bar();
-                if (ctid == 0) {
-                    __threadfence();
-                    atomicAdd(p.seq_scored + b, it.z - it.y);
-                }
-            }
-            if (in_area) {
-                // this group's selections, while the producer streams the next
-                // group's summaries (or the first group's chunks) into the ring
-                const int np_g = misc[12 + g];
-                for (int k = 0; k < np_g && pj < npieces; ++k, ++pj) {
-                    folded = -1;                         // the union area is reused
-                    select_piece(pj, uni);
-                }
-            }
-        }
+        // every selection of the CTA up front, in the union area, while the
+        // producer streams the first pieces' chunks; else each one in the idle
+        // ring right before its piece
+        if (in_area)
+            for (int j = 0; j < npieces; ++j) select_piece(j, uni);
         DecOut dout;
         dout.out = p.out;
         dout.out_f32 = p.out_f32;
@@ -912,7 +936,6 @@ __global__ void __launch_bounds__(kStepThreads, 2)
         dout.Hq = p.Hq;
         dout.G = p.G;
         for (int j = 0; j < npieces; ++j) {
-            // one group: the selection in the idle ring, right before the piece
             if (!in_area) select_piece(j, ring);
             const int4 it = pitem[j];
             const int u = it.x, c0 = it.y, c1 = it.z;
@@ -1013,15 +1036,14 @@ StepWs step_ws_carve(void* ws, int batch, int H, int G, int max_pages, int max_s
 }
 
 // Dynamic shared memory: the stage ring, the small areas, then the union area
-// (the sequences' staged lengths and budgets, then the query coefficients,
-// then the decode merge area).
+// (the query coefficients, the top-k, the decode merge area).
 template <int D, int NT>
-size_t step_smem(int batch, int H, int* off_union) {
+size_t step_smem(int H, int* off_union) {
     using SS = StepShape<D, NT>;
     const size_t ring = (size_t)SS::kStages * SS::kStageBytes;
     const size_t uni_off = (ring + SS::kFixed + 15) & ~static_cast<size_t>(15);
     const size_t uni = std::max({(size_t)DecShape<D, NT>::kMergeFloats * 4, (size_t)H * 2 * D * 4,
-                                 (size_t)batch * 8, (size_t)kAreaBytes});
+                                 (size_t)kAreaBytes});
     if (off_union) *off_union = static_cast<int>(uni_off);
     return 1024 + uni_off + uni;
 }
@@ -1029,7 +1051,7 @@ size_t step_smem(int batch, int H, int* off_union) {
 template <int D, int NT, bool TWO>
 cudaError_t run_step(const CUtensorMap& tk, const CUtensorMap& tv, StepParams p, cudaStream_t s) {
     auto kern = quest_step_kernel<D, NT, TWO>;
-    const size_t smem = step_smem<D, NT>(p.batch, p.kv.num_kv_heads, &p.off_union);
+    const size_t smem = step_smem<D, NT>(p.kv.num_kv_heads, &p.off_union);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -1038,8 +1060,9 @@ cudaError_t run_step(const CUtensorMap& tk, const CUtensorMap& tv, StepParams p,
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int grid = std::min(2048, num_sms() * per_sm);
-    // the pieces of a CTA must fit its list: groups * ceil(units / grid) <= kMaxPieces
-    if (p.groups * ((p.units + grid - 1) / grid) > kMaxPieces) return cudaErrorInvalidConfiguration;
+    // a CTA's pieces and score slices must fit its lists
+    if ((p.units + grid - 1) / grid > kMaxPieces || (p.batch + grid - 1) / grid > kMaxScoreItems)
+        return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kStepThreads);
@@ -1062,11 +1085,10 @@ size_t quest_step_ws_bytes(int batch, int H, int G, int D, int max_pages, int ma
            a256(slots * G * sizeof(float)) + a256(slots * G * (size_t)D * sizeof(float));
 }
 
-size_t quest_step_smem_bytes(int batch, int H, int D, int G) {
+size_t quest_step_smem_bytes(int H, int D, int G) {
     const int NT = G > 8 ? 2 : 1;
-    if (D == 64) return NT == 1 ? step_smem<64, 1>(batch, H, nullptr)
-                                : step_smem<64, 2>(batch, H, nullptr);
-    return NT == 1 ? step_smem<128, 1>(batch, H, nullptr) : step_smem<128, 2>(batch, H, nullptr);
+    if (D == 64) return NT == 1 ? step_smem<64, 1>(H, nullptr) : step_smem<64, 2>(H, nullptr);
+    return NT == 1 ? step_smem<128, 1>(H, nullptr) : step_smem<128, 2>(H, nullptr);
 }
 
 size_t quest_step_ring_bytes(int D, int G) {
@@ -1077,9 +1099,8 @@ size_t quest_step_ring_bytes(int D, int G) {
 
 cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const void* v_new,
                               const void* q, int batch, int num_q_heads, const int32_t* budget,
-                              float scale, int out_dtype, int max_splits, int item_pages,
-                              int groups, unsigned long long wait_ns, int32_t* sel_pages,
-                              int32_t* n_sel,
+                              float scale, int out_dtype, int max_splits,
+                              unsigned long long wait_ns, int32_t* sel_pages, int32_t* n_sel,
                               const se_view& view, void* out, float* lse, void* ws,
                               cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t s) {
     const int H = kv.num_kv_heads, D = kv.head_dim, G = num_q_heads / H;
@@ -1117,8 +1138,6 @@ cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const vo
     p.o_part = w.o_part;
     p.lse_part = w.lse_part;
     p.max_splits = max_splits;
-    p.item_pages = item_pages;
-    p.groups = std::max(1, std::min(groups > 0 ? groups : 1, std::min(kMaxGroups, batch)));
     p.off_union = 0;
     p.total_rows = total_rows;
     p.wait_ns = wait_ns;

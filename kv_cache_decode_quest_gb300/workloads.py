@@ -48,8 +48,7 @@ class QuestRun:
                         faster path on the bench workloads, the default);
           "step"     -- se_quest_step: append, select and decode in one kernel;
           "separate" -- se_kv_append, se_quest_select, se_sparse_decode.
-    step_tuning: se_quest_step_opts fields (mode "step"): slice_pages,
-    wait_limit_ns."""
+    step_tuning: se_quest_step_opts fields (mode "step"): wait_limit_ns."""
 
     MODES = ("step", "fused", "separate")
 

@@ -137,11 +137,9 @@ def test_quest_step_workspace_and_host_validation(lib):
     big = binding.ViewC(1 << 20, 1 << 20, 1025 * 4, 8)
     assert call(batch=1025, view_=big) == -2        # batch limit
     O = binding.QuestStepOptsC
-    assert call(opts=O(0, 65, None, None, 0, 0, 0)) == -1            # max_splits
-    assert call(opts=O(2, 0, None, None, 0, 0, 0)) == -1             # out_dtype
-    assert call(opts=O(0, 0, None, None, -1, 0, 0)) == -1            # slice_pages
-    assert call(opts=O(0, 0, None, None, 0, -5, 0)) == -1            # wait_limit_ns
-    assert call(opts=O(0, 0, None, None, 0, 0, 5)) == -1             # groups
+    assert call(opts=O(0, 65, None, None, 0)) == -1                  # max_splits
+    assert call(opts=O(2, 0, None, None, 0)) == -1                   # out_dtype
+    assert call(opts=O(0, 0, None, None, -5)) == -1                  # wait_limit_ns
     many = binding.ViewC(1 << 20, 1 << 20, 1024 * 8, 8)
     kv8 = binding.PagedKVC(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 10, 4, 8, 128, 16)
     assert call(batch=1024, hq=64, view_=many, kv_=kv8) == -2        # more than 4096 units

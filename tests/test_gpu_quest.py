@@ -145,18 +145,18 @@ def test_one_kernel_step_matches_two_calls():
     view, lengths, cache rows and page summaries bit for bit, outputs within
     the rounding of their different split pieces; steps open new pages
     (contexts 15, 16, 31, 1000 and 2047 tokens at the start, one sequence with
-    every page selected), and the scoring slice size and the number of
-    sequence groups are varied from step to step."""
+    every page selected), and the split limit of the step's decode plan is
+    varied from step to step."""
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name="quest_step_eq", batch=5, ctx=(15, 16, 31, 1000, 2047),
                      budget=(64, 64, 256, 128, U32), steps=12)
     inputs = synth.quest_inputs(w)
     a = QuestRun(w, inputs, mode="step", out_dtype=1)
     b = QuestRun(w, inputs, mode="fused", out_dtype=1)
-    knobs = [{}, {"slice_pages": 1}, {"slice_pages": 3, "groups": 1}, {"slice_pages": 40},
-             {"slice_pages": 7, "groups": 3}, {"slice_pages": 2, "groups": 4}, {"groups": 1}]
+    top = a.max_splits                                   # the workspace's split count
+    splits = [top, 1, 3, 7, 2, top, 5]
     for s in range(w.steps):
-        a.step_tuning = knobs[s % len(knobs)]
+        a.max_splits = min(top, splits[s % len(splits)])
         a.step(s)
         b.step(s)
         torch.cuda.synchronize()
@@ -207,8 +207,7 @@ def test_split_count_does_not_change_results(max_splits, mode):
     base = synth.workloads()["quest_32k"]
     w = synth.scaled(base, name="quest_splits", batch=2, ctx=(3000, 1234), budget=(U32, 1024),
                      steps=1)
-    run_and_check(w, out_dtype=1, max_splits=max_splits, mode=mode,
-                  step_tuning={"slice_pages": 5} if mode == "step" else None)
+    run_and_check(w, out_dtype=1, max_splits=max_splits, mode=mode)
 
 
 def test_many_units_block_plan():
@@ -220,6 +219,18 @@ def test_many_units_block_plan():
     w = synth.scaled(base, name="quest_many_units", batch=B, ctx=ctx, budget=(256,) * B, steps=1)
     run_and_check(w, units=range(0, B * 4, 7), mode="fused")
     run_and_check(w, units=range(0, B * 4, 7), mode="step")
+
+
+def test_more_sequences_than_blocks():
+    """1024 sequences x 4 KV heads (the step's batch and unit limits), more
+    sequences than resident blocks: each block scores several whole
+    sequences; short ragged contexts, a 4-page budget."""
+    base = synth.workloads()["quest_32k"]
+    B = 1024
+    ctx = tuple(int(x) for x in (np.arange(B) * 53 % 700 + 5))
+    w = synth.scaled(base, name="quest_max_batch", batch=B, ctx=ctx, budget=(64,) * B, steps=1)
+    run_and_check(w, units=range(0, B * 4, 37), mode="step")
+    run_and_check(w, units=range(3, B * 4, 41), mode="fused")
 
 
 def test_stream_k_plan():
@@ -261,13 +272,17 @@ def test_full_size_ragged_128k_sampled():
 
 
 def test_step_wait_that_runs_out_reports_timeout_and_resets():
-    """A bounded wait that runs out (a limit of 1 ns: a block whose sequence is
-    still being scored by other blocks gives up at once) sets SE_DEV_TIMEOUT,
-    leaves ctx_len unchanged and the control words at zero; the next call,
-    with the default limit and the status word cleared, matches the oracle."""
+    """A bounded wait that runs out sets SE_DEV_TIMEOUT, leaves ctx_len
+    unchanged and the control words at zero; the next call, with the default
+    limit and the status word cleared, matches the oracle.  The wait is made
+    to run out by a limit of 1 ns and a skewed batch: 40 sequences take an
+    equal share of the blocks each, so the blocks that score one page of a
+    20-token sequence reach the pieces of the 30000-token one long before the
+    few blocks that score it are done."""
     base = synth.workloads()["quest_32k"]
-    w = synth.scaled(base, name="quest_timeout", batch=4, ctx=(20000, 15000, 9000, 30000),
-                     budget=(512, 1024, 256, 2048), steps=2)
+    B = 40
+    w = synth.scaled(base, name="quest_timeout", batch=B, ctx=(30000,) + (20,) * (B - 1),
+                     budget=(2048,) + (16,) * (B - 1), steps=2)
     inputs = synth.quest_inputs(w)
     run = QuestRun(w, inputs, mode="step", step_tuning={"wait_limit_ns": 1})
     ctx0 = run.kv.ctx_len.clone()
