@@ -342,7 +342,7 @@ int se_sparse_decode_noalloc(const void* k_rows, const void* v_rows, int64_t tot
  * unchanged and the results invalid.  The last block to finish commits the new
  * lengths and clears the workspace's control words.
  * Limits: batch <= 1024, batch * num_kv_heads <= 4096, max_pages_per_seq <=
- * 16384 (15296 with 16 query heads per KV head at head_dim 128), else
+ * 16384 (14833 with 16 query heads per KV head at head_dim 128), else
  * SE_ERR_UNSUPPORTED.  A device that cannot hold the whole grid at once fails
  * the launch (SE_ERR_CUDA).
  * Workspace: se_quest_step_workspace(batch, num_kv_heads, num_q_heads, head_dim,

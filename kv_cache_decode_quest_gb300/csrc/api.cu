@@ -279,10 +279,7 @@ int se_quest_step(const se_paged_kv* kv, const void* k_new, const void* v_new, c
     const int G = num_q_heads / kv->num_kv_heads;
     if (quest_step_smem_bytes(kv->num_kv_heads, kv->head_dim, G) > 227 * 1024)
         return SE_ERR_UNSUPPORTED;
-    // a unit with more than 2048 candidate pages is selected by the consumer
-    // warps, which stage its keys in the idle stage ring
-    if ((size_t)kv->max_pages_per_seq * 4 + 4352 > quest_step_ring_bytes(kv->head_dim, G))
-        return SE_ERR_UNSUPPORTED;
+    if (kv->max_pages_per_seq > quest_step_max_pages(kv->head_dim, G)) return SE_ERR_UNSUPPORTED;
     if ((rc = check_ws(ws, ws_bytes,
                        se_quest_step_workspace(batch, kv->num_kv_heads, num_q_heads, kv->head_dim,
                                                kv->max_pages_per_seq, o.max_splits))))

@@ -67,7 +67,7 @@ constexpr int kStepMaxBatch = 1024;
 constexpr int kStepMaxUnits = 4096;
 size_t quest_step_ws_bytes(int batch, int H, int G, int D, int max_pages, int max_splits);
 size_t quest_step_smem_bytes(int H, int D, int G);
-size_t quest_step_ring_bytes(int D, int G);
+int quest_step_max_pages(int D, int G);
 cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const void* v_new,
                               const void* q, int batch, int num_q_heads, const int32_t* budget,
                               float scale, int out_dtype, int max_splits,

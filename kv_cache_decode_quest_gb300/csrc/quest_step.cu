@@ -57,10 +57,21 @@ constexpr int kStepThreads = (kConsumerWarps + 1) * 32;
 constexpr int kDigit = 10, kStepBins = 1 << kDigit;     // top-k: 10-bit radix digits
 constexpr int kMaxPieces = 32;                          // decode pieces per CTA at most
 constexpr int kMaxScoreItems = 8;                       // score slices per CTA at most
-constexpr int kAreaKeys = 2048;                         // keys a unit's top-k holds outside the ring
+// The top-k runs once per piece, so its instructions come cold from the
+// instruction caches every step: its passes are short rolled loops (code
+// fetched once, then reused) rather than unrolled runs.  A unit's keys sit in
+// shared memory with one pad word per 32 keys, so that consumer thread t can
+// walk its own kKeysPerThread consecutive keys [16t, 16t + 16) of a batch of
+// kAreaKeys without bank conflicts; ranks in page order then come from block
+// scans of per-thread counts.
+constexpr int kKeysPerThread = 16;
+constexpr int kAreaKeys = kKeysPerThread * kCThreads;   // 2048
+constexpr int kSmallInts = 64;
+__host__ __device__ constexpr int key_slots(int m) { return m + (m >> 5); }
+__device__ __forceinline__ int kidx(int i) { return i + (i >> 5); }
 // the top-k's shared memory: histogram, small ints, keys
-constexpr int kSelectBytes = kStepBins * 4 + 64 * 4;
-constexpr int kAreaBytes = kSelectBytes + kAreaKeys * 4;
+constexpr int kSelectBytes = kStepBins * 4 + kSmallInts * 4;
+constexpr int kAreaBytes = kSelectBytes + key_slots(kAreaKeys) * 4;
 
 struct StepParams {
     se_paged_kv kv;
@@ -110,6 +121,9 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -177,73 +191,85 @@ __device__ __forceinline__ int scan128(int v, int* tmp, int warp, int lane) {
     return x + before;
 }
 
-// Threshold of the top K of m order-preserving keys in shared memory, on the
-// 128 consumer threads: bits above the highest bit in which the largest and
-// smallest key differ are common to all keys, so the radix digits start there,
-// and a pass ends the search when the boundary digit is kept whole.  On
-// return: keys above *T (under *mask) are kept, and so are the first *need keys
-// equal to *T.
-__device__ void step_threshold(const uint32_t* sk, int m, int K, int* hist, int* tmp,
-                               uint32_t* red, int* sel, uint32_t* T, uint32_t* mask, int* need,
-                               int warp, int lane) {
+// The float an order-preserving key was made from (float_key inverted).
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Descending scan of a 1024-bin histogram on the 128 consumer threads (thread
+// t owns bins 1023-8t .. 1016-8t): the bin holding the remaining-th largest
+// key.  Writes sel[0] = that bin, sel[1] = keys in the bins above it, sel[2] =
+// keys in it.
+__device__ __forceinline__ void find_bin(const int* hist, int remaining, int* tmp, int* sel,
+                                         int warp, int lane) {
+    constexpr int NB = kStepBins;
+    constexpr int kPer = NB / kCThreads;                  // 8 bins per thread
     const int ctid = warp * 32 + lane;
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int i = ctid; i < m; i += kCThreads) {
-        const uint32_t k = sk[i];
-        lo = min(lo, k);
-        hi = max(hi, k);
+    int vv[kPer], v = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        vv[j] = hist[NB - 1 - (ctid * kPer + j)];
+        v += vv[j];
     }
-    lo = __reduce_min_sync(0xffffffffu, lo);
-    hi = __reduce_max_sync(0xffffffffu, hi);
-    if (lane == 0) {
-        red[warp] = lo;
-        red[4 + warp] = hi;
+    int run = scan128(v, tmp, warp, lane) - v;            // keys in the bins above this thread's
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        if (run < remaining && run + vv[j] >= remaining) {
+            sel[0] = NB - 1 - (ctid * kPer + j);
+            sel[1] = run;
+            sel[2] = vv[j];
+        }
+        run += vv[j];
     }
     consumer_bar();
-    lo = min(min(red[0], red[1]), min(red[2], red[3]));
-    hi = max(max(red[4], red[5]), max(red[6], red[7]));
-    const uint32_t diff = lo ^ hi;
-    if (diff == 0u) {                                     // every key is equal
-        *T = hi;
-        *mask = 0xffffffffu;
-        *need = K;
-        return;
+}
+
+// Exclusive scan over the 128 consumer threads; *total gets the sum.
+__device__ __forceinline__ int scan128_excl(int v, int* tmp, int warp, int lane, int* total) {
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-    const int top = 31 - __clz(diff);                     // highest differing bit
+    if (lane == 31) tmp[warp] = x;
+    consumer_bar();
+    int before = 0;
+#pragma unroll
+    for (int i = 0; i < kConsumerWarps; ++i) before += i < warp ? tmp[i] : 0;
+    *total = tmp[0] + tmp[1] + tmp[2] + tmp[3];
+    consumer_bar();
+    return x - v + before;
+}
+
+// Radix threshold (the general case): bits above the highest bit in which the
+// largest and smallest key differ are common to all keys, so the 10-bit radix
+// digits start there, and a pass ends the search when the boundary digit is
+// kept whole.
+__device__ void radix_threshold(const uint32_t* sk, int m, int K, uint32_t lo, uint32_t hi,
+                                int* hist, int* tmp, int* sel, uint32_t* T, uint32_t* mask,
+                                int* need, int warp, int lane) {
+    constexpr int kPer = kStepBins / kCThreads;
+    const int ctid = warp * 32 + lane;
+    const int top = 31 - __clz(lo ^ hi);                  // highest differing bit
     uint32_t msk = top == 31 ? 0u : ~((2u << top) - 1u);
     uint32_t prefix = hi & msk;
     int remaining = K;
     int low = top + 1;                                    // bits [low, 32) are decided
-    constexpr int kPer = kStepBins / kCThreads;           // 8 bins per thread
+#pragma unroll 1
     while (low > 0) {
-        // thread t owns bins 1023 - 8t .. 1016 - 8t (descending)
         const int w = min(kDigit, low), shift = low - w;
         const uint32_t dm = (1u << w) - 1u;
 #pragma unroll
         for (int j = 0; j < kPer; ++j) hist[ctid * kPer + j] = 0;
         consumer_bar();
+#pragma unroll 2
         for (int i = ctid; i < m; i += kCThreads) {
-            const uint32_t k = sk[i];
+            const uint32_t k = sk[kidx(i)];
             if ((k & msk) == prefix) atomicAdd(&hist[(k >> shift) & dm], 1);
         }
         consumer_bar();
-        int vv[kPer], v = 0;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            vv[j] = hist[kStepBins - 1 - (ctid * kPer + j)];
-            v += vv[j];
-        }
-        int run = scan128(v, tmp, warp, lane) - v;        // digits above this thread's
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            if (run < remaining && run + vv[j] >= remaining) {
-                sel[0] = kStepBins - 1 - (ctid * kPer + j);
-                sel[1] = run;
-                sel[2] = vv[j];
-            }
-            run += vv[j];
-        }
-        consumer_bar();
+        find_bin(hist, remaining, tmp, sel, warp, lane);
         prefix |= static_cast<uint32_t>(sel[0]) << shift;
         msk |= dm << shift;
         remaining -= sel[1];
@@ -257,91 +283,192 @@ __device__ void step_threshold(const uint32_t* sk, int m, int K, int* hist, int*
     *need = remaining;
 }
 
+// Threshold of the top K of m order-preserving keys in shared memory (lo /
+// hi: the smallest and largest), on the 128 consumer threads.  On return:
+// keys above *T (under *mask) are kept, and so are the first *need keys equal
+// to *T.  One histogram pass over 1024 equal-width bins of the score VALUES
+// between the smallest and the largest (weakly monotone in the key, so every
+// bin above the boundary bin is kept whole and every bin below it dropped),
+// then the keys of the boundary bin, when it holds at most kBinCap, are
+// gathered and ranked exactly by (key desc, page asc); a larger boundary bin
+// (many equal or clustered scores, or a range that overflows) takes the
+// radix passes.
+constexpr int kBinCap = 128;
+__device__ void step_threshold(const uint32_t* sk, int m, int K, uint32_t lo, uint32_t hi,
+                               int* hist, int* tmp, int* sel, int* cnt, uint32_t* T,
+                               uint32_t* mask, int* need, int warp, int lane) {
+    constexpr int kPer = kStepBins / kCThreads;
+    const int ctid = warp * 32 + lane;
+    if (lo == hi) {                                       // every key is equal
+        *T = hi;
+        *mask = 0xffffffffu;
+        *need = K;
+        return;
+    }
+    const float flo = key_float(lo);
+    const float scale = static_cast<float>(kStepBins) / (key_float(hi) - flo);
+    auto bin_of = [&](uint32_t k) {
+        const int b = static_cast<int>((key_float(k) - flo) * scale);   // NaN -> 0
+        return min(kStepBins - 1, max(0, b));
+    };
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) hist[ctid * kPer + j] = 0;
+    if (ctid == 0) *cnt = 0;
+    consumer_bar();
+#pragma unroll 2
+    for (int i = ctid; i < m; i += kCThreads) atomicAdd(&hist[bin_of(sk[kidx(i)])], 1);
+    consumer_bar();
+    find_bin(hist, K, tmp, sel, warp, lane);
+    const int bstar = sel[0], R = K - sel[1], E = sel[2];
+    if (E > kBinCap) {
+        consumer_bar();                                   // sel is rewritten
+        radix_threshold(sk, m, K, lo, hi, hist, tmp, sel, T, mask, need, warp, lane);
+        return;
+    }
+    // the boundary bin's keys and pages, gathered into the free histogram
+    uint32_t* bk = reinterpret_cast<uint32_t*>(hist);
+    int* bp = hist + kBinCap;
+#pragma unroll 2
+    for (int i = ctid; i < m; i += kCThreads) {
+        const uint32_t k = sk[kidx(i)];
+        if (bin_of(k) == bstar) {
+            const int at = atomicAdd(cnt, 1);
+            bk[at] = k;
+            bp[at] = i;
+        }
+    }
+    consumer_bar();
+    if (ctid < E) {
+        const uint32_t k = bk[ctid];
+        const int pg = bp[ctid];
+        int rank = 0, above = 0;
+#pragma unroll 1
+        for (int j = 0; j < E; ++j) {
+            const uint32_t kj = bk[j];
+            rank += kj > k || (kj == k && bp[j] < pg);
+            above += kj > k;
+        }
+        if (rank == R - 1) {                              // the last kept key of the bin
+            sel[3] = static_cast<int>(k);
+            sel[4] = R - above;
+        }
+    }
+    consumer_bar();
+    *T = static_cast<uint32_t>(sel[3]);
+    *mask = 0xffffffffu;
+    *need = sel[4];
+    consumer_bar();                                       // hist and sel are rewritten next
+}
+
 // The selection of unit u = (b, h) restricted to ranks [c0, c1) on the four
-// consumer warps (used when a unit has more than 2048 candidate pages): exact top-(k-1)
-// of the candidate pages 0..n-2 by (score desc, page asc) in ascending page
-// order, then the last page (always selected, never scored) at rank k-1; all
-// pages when n <= k.  Writes sel_pages[u][rank] for the ranks of the range.
-// The keys were written by the scoring slices of other CTAs (read through
-// L2); `area` is the idle stage ring (hist, small ints, keys).
-__device__ void piece_select(const StepParams& p, int u, const SeqVals& s, int c0, int c1,
-                             uint8_t* area, int warp, int lane) {
+// consumer warps: exact top-(k-1) of the candidate pages 0..n-2 by (score
+// desc, page asc) in ascending page order, then the last page (always
+// selected, never scored) at rank k-1; all pages when n <= k.  Writes
+// sel_pages[u][rank] for the ranks of the range.  The keys were written by
+// the scoring slices of other CTAs (read through L2); `area` holds the
+// histogram, small ints and the keys (key_slots(m) words).  Returns where in
+// the area the range's pages are also left (page of rank c at [c - c0]), or
+// null.
+__device__ const int* piece_select(const StepParams& p, int u, const SeqVals& s, int c0, int c1,
+                                   uint8_t* area, int warp, int lane) {
     const int ctid = warp * 32 + lane;
     const int stride = p.kv.max_pages_per_seq;
     int32_t* selp = p.sel_pages + (int64_t)u * stride;
-    if (s.m == 0) {
-        for (int c = c0 + ctid; c < c1; c += kCThreads) selp[c] = c;
-        return;
-    }
     int* hist = reinterpret_cast<int*>(area);                    // [1024]
-    int* small = hist + kStepBins;                               // 64 ints
+    int* small = hist + kStepBins;                               // kSmallInts
     int* tmp = small;                                            // [4]
     uint32_t* red = reinterpret_cast<uint32_t*>(small + 4);      // [8]
-    int* sel = small + 12;                                       // [4]
-    int* wgt = small + 16;                                       // [4]
-    int* weq = small + 20;                                       // [4]
-    uint32_t* skeys = reinterpret_cast<uint32_t*>(small + 64);   // [m]
+    int* sel = small + 12;                                       // [8]
+    int* cnt = small + 20;                                       // [1]
+    uint32_t* sk = reinterpret_cast<uint32_t*>(small + kSmallInts);   // [key_slots(m)]
+    int* spage = hist;                                           // [c1 - c0] at the end
+    const bool keep = c1 - c0 <= kStepBins;
+    if (s.m == 0) {
+#pragma unroll 1
+        for (int c = c0 + ctid; c < c1; c += kCThreads) {
+            selp[c] = c;
+            if (keep) spage[c - c0] = c;
+        }
+        return keep ? spage : nullptr;
+    }
     const int m = s.m, K = s.k - 1;
-    if (c1 == s.k && ctid == 0) selp[K] = s.n - 1;
-    if (K == 0 || c0 >= K) return;                                // only the last page here
-    {
+    if (K > 0 && c0 < K) {
+        // the keys into shared memory, with their smallest and largest
         const uint32_t* keys = p.keys + (int64_t)u * p.kstride;
-        constexpr int kU = 8;
-        for (int base = ctid; base < m; base += kCThreads * kU) {
-            uint32_t kv2[kU];
+        uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll 1
+        for (int base = ctid; base < m; base += kCThreads * 4) {
+            uint32_t kk[4];
 #pragma unroll
-            for (int j = 0; j < kU; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const int i = base + j * kCThreads;
-                kv2[j] = i < m ? __ldcg(keys + i) : 0u;
+                kk[j] = i < m ? __ldcg(keys + i) : 0u;
             }
 #pragma unroll
-            for (int j = 0; j < kU; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const int i = base + j * kCThreads;
-                if (i < m) skeys[i] = kv2[j];
+                if (i < m) {
+                    sk[kidx(i)] = kk[j];
+                    lo = min(lo, kk[j]);
+                    hi = max(hi, kk[j]);
+                }
             }
         }
+        lo = __reduce_min_sync(0xffffffffu, lo);
+        hi = __reduce_max_sync(0xffffffffu, hi);
+        if (lane == 0) {
+            red[warp] = lo;
+            red[4 + warp] = hi;
+        }
         consumer_bar();
+        lo = min(min(red[0], red[1]), min(red[2], red[3]));
+        hi = max(max(red[4], red[5]), max(red[6], red[7]));
+        int need = 0;
+        uint32_t T = 0, msk = 0;
+        step_threshold(sk, m, K, lo, hi, hist, tmp, sel, cnt, &T, &msk, &need, warp, lane);
+        // ranks in page order: thread t walks its keys [16t, 16t + 16) of each
+        // batch of kAreaKeys, so block scans of the per-thread counts of
+        // equal and of kept keys place each kept key
+        int eq_carry = 0, take_carry = 0;
+#pragma unroll 1
+        for (int base = 0; base < m && take_carry < c1; base += kAreaKeys) {
+            const int first = base + ctid * kKeysPerThread;
+            const int nv = max(0, min(kKeysPerThread, m - first));
+            int gt = 0, eq = 0;
+#pragma unroll 2
+            for (int t = 0; t < nv; ++t) {
+                const uint32_t x = sk[kidx(first + t)] & msk;
+                gt += x > T;
+                eq += x == T;
+            }
+            int eq_tot = 0, take_tot = 0;
+            const int eq_before = eq_carry + scan128_excl(eq, tmp, warp, lane, &eq_tot);
+            const int take_eq = max(0, min(eq, need - eq_before));
+            int rank = take_carry + scan128_excl(gt + take_eq, tmp, warp, lane, &take_tot);
+            int used = 0;
+#pragma unroll 2
+            for (int t = 0; t < nv; ++t) {
+                const uint32_t x = sk[kidx(first + t)] & msk;
+                const bool is_eq = x == T;
+                const bool tk = x > T || (is_eq && used < take_eq);
+                used += is_eq;
+                if (tk) {
+                    if (rank >= c0 && rank < c1) {
+                        selp[rank] = first + t;
+                        if (keep) spage[rank - c0] = first + t;
+                    }
+                    ++rank;
+                }
+            }
+            eq_carry += eq_tot;
+            take_carry += take_tot;
+        }
     }
-    int need_eq = 0;
-    uint32_t T = 0, msk = 0;
-    step_threshold(skeys, m, K, hist, tmp, red, sel, &T, &msk, &need_eq, warp, lane);
-    // pages in ascending order: warp w owns a contiguous range read with a lane
-    // stride; ballots rank the kept pages inside the warp and the counts of the
-    // warps before it place its run
-    const int chunk = ((m + kConsumerWarps - 1) / kConsumerWarps + 31) & ~31;
-    const int r0 = min(m, warp * chunk), r1 = min(m, r0 + chunk);
-    int gt = 0, eq = 0;
-    for (int i = r0 + lane; i < r1; i += 32) {
-        const uint32_t kk = skeys[i] & msk;
-        gt += kk > T;
-        eq += kk == T;
+    if (c1 == s.k && ctid == 0) {                       // the last page
+        selp[K] = s.n - 1;
+        if (keep) spage[K - c0] = s.n - 1;
     }
-    gt = __reduce_add_sync(0xffffffffu, gt);
-    eq = __reduce_add_sync(0xffffffffu, eq);
-    if (lane == 0) {
-        wgt[warp] = gt;
-        weq[warp] = eq;
-    }
-    consumer_bar();
-    int eq_seen = 0, out = 0;
-    for (int w = 0; w < warp; ++w) {
-        const int take_w = max(0, min(weq[w], need_eq - eq_seen));
-        out += wgt[w] + take_w;
-        eq_seen += weq[w];
-    }
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int i0 = r0; i0 < r1 && out < c1; i0 += 32) {
-        const int i = i0 + lane;
-        const uint32_t kk = i < r1 ? skeys[i] & msk : 0u;
-        const bool is_eq = i < r1 && kk == T;
-        const uint32_t meq = __ballot_sync(0xffffffffu, is_eq);
-        const bool take = (i < r1 && kk > T) || (is_eq && eq_seen + __popc(meq & lt) < need_eq);
-        const uint32_t mt = __ballot_sync(0xffffffffu, take);
-        const int rank = out + __popc(mt & lt);
-        if (take && rank >= c0 && rank < c1) selp[rank] = i;
-        out += __popc(mt);
-        eq_seen += __popc(meq);
-    }
+    return keep ? spage : nullptr;
 }
 
 __device__ __forceinline__ int warp_excl_scan(int v, int lane) {
@@ -355,9 +482,11 @@ __device__ __forceinline__ int warp_excl_scan(int v, int lane) {
 }
 
 // The view rows of ranks [c0, c1) of unit u: the physical chunk of each
-// selected page (from sel_pages, written by the calling threads), `nt`
-// threads t = 0..nt-1, eight block-table lookups of a thread in flight together.
-__device__ void view_rows(const StepParams& p, int u, int c0, int c1, int t, int nt) {
+// selected page (from spage when not null, page of rank c at [c - c0], else
+// from sel_pages, written by the calling threads), `nt` threads t = 0..nt-1,
+// eight block-table lookups of a thread in flight together.
+__device__ void view_rows(const StepParams& p, int u, int c0, int c1, const int* spage, int t,
+                          int nt) {
     const int H = p.kv.num_kv_heads, h = u % H, b = u / H;
     const int stride = p.kv.max_pages_per_seq;
     const int32_t* selp = p.sel_pages + (int64_t)u * stride;
@@ -368,7 +497,7 @@ __device__ void view_rows(const StepParams& p, int u, int c0, int c1, int t, int
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = c00 + e * nt + t;
-            page[e] = c < c1 ? __ldcg(selp + c) : -1;
+            page[e] = c < c1 ? (spage ? spage[c - c0] : __ldcg(selp + c)) : -1;
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) phys[e] = (page[e] >= 0 && page[e] < stride) ? btr[page[e]] : -1;
@@ -831,6 +960,14 @@ __global__ void __launch_bounds__(kStepThreads, 2)
                 misc[6] = in_area;
                 mbar_arrive(&planbar[0]);
             }
+            // the block-table rows the pieces' view rows will read, into L2
+            // while the summaries stream
+            for (int j = 0; j < n; ++j) {
+                const int b = pitem[j].x / H;
+                const int np = min(stride, seq_vals(pseq[j].x, pseq[j].y, cap, pending).n);
+                const int32_t* row = p.kv.block_table + (int64_t)b * stride;
+                for (int e = lane * 32; e < np; e += 32 * 32) prefetch_l2(row + e);
+            }
         }
         if (blockIdx.x == 0) {
             for (int b = ctid; b < p.batch; b += kCThreads) {
@@ -903,9 +1040,9 @@ __global__ void __launch_bounds__(kStepThreads, 2)
                 !wait_count(p, p.seq_scored + b, sv.m, abort_flag))
                 give_up(p, abort_flag);
             consumer_bar();
-            piece_select(p, u, sv, c0, c1, area, warp, lane);
+            const int* spage = piece_select(p, u, sv, c0, c1, area, warp, lane);
             consumer_bar();
-            view_rows(p, u, c0, c1, ctid, kCThreads);
+            view_rows(p, u, c0, c1, spage, ctid, kCThreads);
             if (c0 == 0 && ctid == 0) {
                 p.n_sel[u] = sv.chunks;
                 p.view.n_tokens[u] = sv.tokens;
@@ -1091,10 +1228,17 @@ size_t quest_step_smem_bytes(int H, int D, int G) {
     return NT == 1 ? step_smem<128, 1>(H, nullptr) : step_smem<128, 2>(H, nullptr);
 }
 
-size_t quest_step_ring_bytes(int D, int G) {
-    if (D == 64) return (size_t)StepShape<64, 1>::kStages * StepShape<64, 1>::kStageBytes;
-    return G > 8 ? (size_t)StepShape<128, 2>::kStages * StepShape<128, 2>::kStageBytes
-                 : (size_t)StepShape<128, 1>::kStages * StepShape<128, 1>::kStageBytes;
+// A unit with more than kAreaKeys candidate pages keeps its keys in the idle
+// stage ring, after the top-k's histogram and small ints.
+int quest_step_max_pages(int D, int G) {
+    const size_t ring =
+        D == 64 ? (size_t)StepShape<64, 1>::kStages * StepShape<64, 1>::kStageBytes
+        : G > 8 ? (size_t)StepShape<128, 2>::kStages * StepShape<128, 2>::kStageBytes
+                : (size_t)StepShape<128, 1>::kStages * StepShape<128, 1>::kStageBytes;
+    // the largest m with key_slots(m) words after the histogram and small ints
+    size_t words = (ring - kSelectBytes) / 4, m = words * 32 / 33;
+    while (m > 0 && (size_t)key_slots(static_cast<int>(m)) > words) --m;
+    return static_cast<int>(std::min<size_t>(16384, m + 1));
 }
 
 cudaError_t launch_quest_step(const se_paged_kv& kv, const void* k_new, const void* v_new,

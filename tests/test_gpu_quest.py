@@ -221,6 +221,65 @@ def test_many_units_block_plan():
     run_and_check(w, units=range(0, B * 4, 7), mode="step")
 
 
+def _tied_inputs(w):
+    """Sequences 0 and 1: their best-scoring page (KV head 0, step 0) copied
+    over pages [40, 200) and [30, 70), so that 161 and 41 candidate pages tie
+    at the top score, more than the budget keeps; sequence 3: its page of the
+    54th best score copied over pages [300, 320), so that the budget's
+    boundary falls inside the 21 tied pages; sequence 2: one page repeated
+    throughout (every score equal).  Returns the inputs and the tied page
+    groups."""
+    inputs = synth.quest_inputs(w)
+    groups = {}
+    for b, (lo, hi), nth in ((0, (40, 200), 0), (1, (30, 70), 0), (3, (300, 320), 53)):
+        U = oracle_unit(w, inputs, b, 0, 0)[0]
+        src = int(oracle.rank_order(U[:len(U) - 1])[nth])
+        k = inputs["k"][b]
+        for pg in range(lo, hi):
+            k[:, pg * 16:(pg + 1) * 16] = k[:, src * 16:(src + 1) * 16]
+        groups[b] = sorted(set(range(lo, hi)) | {src})
+    k = inputs["k"][2]
+    for pg in range(1, (w.ctx[2] + w.steps) // 16):
+        k[:, pg * 16:(pg + 1) * 16] = k[:, 0:16]
+    return inputs, groups
+
+
+@pytest.mark.parametrize("mode", ["step", "fused"])
+def test_tied_scores_keep_page_order(mode):
+    """Exact ties at the selection boundary are broken by page order: 161 tied
+    pages at the top (more than one boundary bin holds, so the radix passes
+    decide), 41 tied pages at the top (ranked inside the boundary bin), 21
+    tied pages across the boundary of a 750-page sequence, and all-equal
+    scores."""
+    base = synth.workloads()["quest_32k"]
+    w = synth.scaled(base, name="quest_ties", batch=4, ctx=(4000, 3000, 2500, 12000),
+                     budget=(1024, 512, 256, 1024), steps=1)
+    inputs, groups = _tied_inputs(w)
+    run = QuestRun(w, inputs, mode=mode, out_dtype=1)
+    run.step(0)
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    check_step(run, inputs, 0)
+    Hkv = w.num_kv_heads
+    sel = run.sel.cpu().numpy()
+    n_sel = run.n_sel.cpu().numpy()
+    for b, grp in groups.items():
+        u = b * Hkv                                       # head 0: the group's scores
+        pages = set(sel[u, :n_sel[u]].tolist())
+        k = w.budget[b] // 16
+        taken = [pg for pg in grp if pg in pages]
+        if b < 2:                                         # the group is the top
+            assert taken == grp[:k - 1], f"sequence {b}: tied pages not taken in page order"
+        else:                                             # the boundary is inside it
+            assert 0 < len(taken) < len(grp), f"sequence {b}: boundary not inside the group"
+            assert taken == grp[:len(taken)], f"sequence {b}: tied pages not taken in page order"
+    n = (w.ctx[2] + 1 + 15) // 16
+    k = w.budget[2] // 16
+    for h in range(Hkv):
+        u = 2 * Hkv + h
+        assert sel[u, :n_sel[u]].tolist() == list(range(k - 1)) + [n - 1]
+
+
 def test_more_sequences_than_blocks():
     """1024 sequences x 4 KV heads (the step's batch and unit limits), more
     sequences than resident blocks: each block scores several whole
