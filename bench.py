@@ -59,6 +59,22 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """(dense bf16 TFLOP/s of a GEMM timed alone, SM clock MHz, kind)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("sm_max_mhz", 2070.0)), "measured"
+    return 1900.0, 2070.0, "fallback"
+
+
+# Exponentials per clock per SM: the special-function rate of this GPU
+# generation (twice the previous one's 16); with the SM count and the
+# maximum SM clock it gives the ex2 roof of the SnapKV scoring passes.
+EX2_PER_CLOCK_PER_SM = 32
+
+
 def file_sha(path):
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -821,11 +837,25 @@ def snapkv(out, device, peak, flush):
     kept = min(w.keep, L - w.window) + w.window
     c_bytes = Bh * (L * D * 2 + 2 * kept * D * 2 * 2)       # K read once, kept K/V read + written
     c_flops = 2 * 2 * Bh * w.window * G * L * D              # two passes of S = Q K^T
+    c_s = sum(c_ms) / len(c_ms) / 1e3
+    tf_peak, sm_mhz, tf_kind = tensor_peak()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    ex2 = 2 * Bh * w.window * G * L                           # one exp2 per (row, key) per pass
+    ex2_peak = EX2_PER_CLOCK_PER_SM * sms * sm_mhz * 1e6
     out["snapkv_32k_compaction"] = {
-        "ms_per_batch": round(sum(c_ms) / len(c_ms), 4),
-        "prefill_tokens_per_s": round(w.batch * L / (sum(c_ms) / len(c_ms) / 1e3), 1),
-        "algorithmic_gbs": round(c_bytes / (sum(c_ms) / len(c_ms) / 1e3) / 1e9, 1),
-        "tensor_tflops": round(c_flops / (sum(c_ms) / len(c_ms) / 1e3) / 1e12, 1),
+        "ms_per_batch": round(c_s * 1e3, 4),
+        "prefill_tokens_per_s": round(w.batch * L / c_s, 1),
+        "algorithmic_gbs": round(c_bytes / c_s / 1e9, 1),
+        "tensor_tflops": round(c_flops / c_s / 1e12, 1),
+        "roofs": {
+            "hbm_frac": round(c_bytes / c_s / 1e9 / peak, 4),
+            "tensor_frac": round(c_flops / c_s / 1e12 / tf_peak, 4),
+            "tensor_peak_tflops": tf_peak, "tensor_peak_kind": tf_kind + " bf16 burst",
+            "ex2_per_s": round(ex2 / c_s, 1),
+            "ex2_frac": round(ex2 / c_s / ex2_peak, 4),
+            "ex2_peak_per_s": round(ex2_peak, 1),
+            "ex2_peak": f"{EX2_PER_CLOCK_PER_SM} per clock per SM x {sms} SMs x {sm_mhz:.0f} MHz",
+            "scope": "whole compaction call (both scoring passes, pool + top-k, gather)"},
         "batch": w.batch, "ctx": L}
     K2 = min(32, w.steps - 3)
     s_ms, s_k = timed_steps(lambda i, a, b: sr.step(i, a, b), K2, 3, flush)
