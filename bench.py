@@ -323,7 +323,10 @@ def oracle_rates(seconds=2.0):
     """Single-threaded oracle rates per workload, in one spawned process."""
     import multiprocessing as mp
     with mp.get_context("spawn").Pool(1) as pool:
-        return pool.apply(_oracle_rates_worker, (seconds,))
+        res = pool.apply(_oracle_rates_worker, (seconds,))
+        pool.close()
+        pool.join()
+    return res
 
 
 def cpu_baseline(name, seconds=12.0, cores=None, single=None):
@@ -335,6 +338,8 @@ def cpu_baseline(name, seconds=12.0, cores=None, single=None):
     t0 = time.perf_counter()
     with ctx.Pool(cores) as pool:
         res = pool.map(_oracle_worker, [(name, i % B, seconds) for i in range(cores)])
+        pool.close()
+        pool.join()
     wall = time.perf_counter() - t0
     q = sum(r[0] for r in res)
     per_worker = [r[0] / r[1] for r in res]
@@ -598,13 +603,6 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
 
-    # oracle baselines first (spawned workers), rank 0 only: every workload's
-    # single-threaded oracle rate, then the headline's on all host cores
-    rates = oracle_rates(args.oracle_seconds) if (rank == 0 and args.oracle_seconds > 0) else {}
-    cpu = (cpu_baseline(HEADLINE, seconds=args.cpu_seconds,
-                        single=rates.get(HEADLINE, {}).get("queries_per_s"))
-           if (rank == 0 and args.cpu_seconds > 0) else None)
-
     peak, peak_kind = peaks()
     qb = QuestBench(HEADLINE, device, mode=HEADLINE_MODE)
     B = qb.w.batch
@@ -632,9 +630,18 @@ def run_ours(args):
     extra = {}
     if args.extras:
         extra = run_extras(args, device, peak)
-        for key, val in extra.items():
-            if key in rates:
-                val["oracle_single_core"] = rates[key]
+
+    # oracle baselines last (spawned workers on the host cores, rank 0 only),
+    # so that no GPU timing, the end-to-end one above all, runs on a host
+    # that the workers still load: every workload's single-threaded oracle
+    # rate, then the headline's on all host cores
+    rates = oracle_rates(args.oracle_seconds) if (rank == 0 and args.oracle_seconds > 0) else {}
+    cpu = (cpu_baseline(HEADLINE, seconds=args.cpu_seconds,
+                        single=rates.get(HEADLINE, {}).get("queries_per_s"))
+           if (rank == 0 and args.cpu_seconds > 0) else None)
+    for key, val in extra.items():
+        if key in rates:
+            val["oracle_single_core"] = rates[key]
 
     if rank != 0:
         return
