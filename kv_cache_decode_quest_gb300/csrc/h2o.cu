@@ -33,27 +33,29 @@ struct EvictParams {
 };
 
 // 512 threads: two blocks per SM, so one block per unit runs in a single wave.
-// STAGED: the unit's positions and scores are read once into shared memory
-// (all loads in flight), every later pass reads them there, and the updated
-// scores go back in one pass; used when 8 * seg_cap bytes fit kEvictStageMax.
+// One pass over the unit's tokens does the usual step whole: the score update
+// (written in place), the count of the recent window and the victim among the
+// others (lowest score, then the higher position) with its slot, reduced
+// over the block once.  Only when the newest `recent` positions are not all
+// held does a second, exact pass select the recent window (a radix selection
+// of the `recent` largest positions) and look for the victim again.
 constexpr int kEvictThreads = 512;
-constexpr int kEvictStageMax = 96 * 1024;
 // G4 = G / 4 (a compile-time count of 16-byte logit vectors per token, so a
 // thread's loads for several tokens are issued together), or 0 for G = 1, 2.
-template <bool STAGED, int G4>
+template <int G4>
 __global__ void __launch_bounds__(kEvictThreads) h2o_evict_kernel(const EvictParams p) {
     pdl_wait();
     pdl_trigger();
-    extern __shared__ int32_t stage[];                  // STAGED: [seg_cap] pos, [seg_cap] score
     __shared__ float s_lse[16];
     __shared__ int hist[256];
     __shared__ int tmp[33];
     __shared__ int sel[2];
     __shared__ unsigned long long s_best[32];
-    __shared__ int s_cnt;
+    __shared__ int s_slot[32], s_cnt[32];
     const int H = p.kv.num_kv_heads, segs = p.kv.head_dim / 8;
     const int u = blockIdx.x, b = u / H, h = u % H;
     const int G = p.G;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
     int n = p.kv.seg_len[u];
     const int off = p.kv.seg_off[u];
     if (n < 0 || n > p.kv.seg_cap || off < 0 || (int64_t)off + n > p.kv.total_rows) {
@@ -64,16 +66,26 @@ __global__ void __launch_bounds__(kEvictThreads) h2o_evict_kernel(const EvictPar
         return;
     }
     if (threadIdx.x < G) s_lse[threadIdx.x] = p.lse[(int64_t)b * p.Hq + h * G + threadIdx.x];
-    if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
 
-    float* gscore = p.kv.score + off;
-    int32_t* gpos = p.kv.pos + off;
-    int32_t* pos = STAGED ? stage : gpos;
-    float* score = STAGED ? reinterpret_cast<float*>(stage + p.kv.seg_cap) : gscore;
+    float* score = p.kv.score + off;
+    int32_t* pos = p.kv.pos + off;
+    const bool evict = n > p.budget;
+    // the recent window when its newest `recent` positions are all held (the
+    // usual case): positions above new_pos - recent
+    const int new_pos = p.kv.seq_len[b] - 1;
+    int thr = new_pos - p.recent;
+    // the victim key: float_key(score) high, then the higher position first
+    auto victim_key = [](float sc, int ps) {
+        return (static_cast<unsigned long long>(float_key(sc)) << 32) |
+               static_cast<unsigned long long>(0x7fffffffu - static_cast<uint32_t>(ps));
+    };
     // 1. score update with this step's normalised probabilities (a token's G
-    //    logits as 16-byte vectors when G % 4 == 0), positions staged alongside
+    //    logits as 16-byte vectors when G % 4 == 0), the recent count and the
+    //    thread's victim candidate, all in one pass
     const float* lg = p.logits + (int64_t)u * p.stride * G;
+    int c = 0, best_slot = -1;
+    unsigned long long best = ~0ull;
 #pragma unroll 4
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
         float pr = 0.f;
@@ -88,79 +100,96 @@ __global__ void __launch_bounds__(kEvictThreads) h2o_evict_kernel(const EvictPar
         } else {
             for (int g = 0; g < G; ++g) pr += __expf(lg[(int64_t)t * G + g] - s_lse[g]);
         }
-        score[t] = gscore[t] + pr;
-        if (STAGED) pos[t] = gpos[t];
+        const float sc = score[t] + pr;
+        score[t] = sc;
+        if (evict) {
+            const int ps = pos[t];
+            c += ps > thr;
+            if (ps <= thr) {
+                const unsigned long long key = victim_key(sc, ps);
+                if (key < best) {
+                    best = key;
+                    best_slot = t;
+                }
+            }
+        }
     }
-    __syncthreads();
-    // the updated scores go back to the cache (STAGED), after any move
-    auto write_back = [&](int count) {
-        if (STAGED)
-            for (int t = threadIdx.x; t < count; t += blockDim.x) gscore[t] = score[t];
-    };
-    if (n <= p.budget) {
-        write_back(n);
+    if (!evict) {
         if (threadIdx.x == 0) p.evicted_pos[u] = -1;
         return;
     }
-    // 2. the recent window: positions above new_pos - recent when the newest
-    //    `recent` positions are all held (the usual case), else an exact
-    //    selection of the `recent` largest positions.
-    const int new_pos = p.kv.seq_len[b] - 1;
-    int thr = new_pos - p.recent;            // candidates: pos <= thr
-    int c = 0;
-#pragma unroll 4
-    for (int t = threadIdx.x; t < n; t += blockDim.x) c += pos[t] > thr;
-    atomicAdd(&s_cnt, c);
-    __syncthreads();
-    if (s_cnt != p.recent) {
+    // the block's recent count and victim (key, slot)
+    auto reduce = [&](int cnt) {
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+            const int ys = __shfl_xor_sync(0xffffffffu, best_slot, o);
+            if (y < best) {
+                best = y;
+                best_slot = ys;
+            }
+        }
+        if (lane == 0) {
+            s_best[wid] = best;
+            s_slot[wid] = best_slot;
+            s_cnt[wid] = cnt;
+        }
+        __syncthreads();                                  // every score is written too
+        if (wid == 0) {
+            best = lane < nw ? s_best[lane] : ~0ull;
+            best_slot = lane < nw ? s_slot[lane] : -1;
+            cnt = __reduce_add_sync(0xffffffffu, lane < nw ? s_cnt[lane] : 0);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+                const int ys = __shfl_xor_sync(0xffffffffu, best_slot, o);
+                if (y < best) {
+                    best = y;
+                    best_slot = ys;
+                }
+            }
+            if (lane == 0) {
+                s_best[0] = best;
+                s_slot[0] = best_slot;
+                s_cnt[0] = cnt;
+            }
+        }
+        __syncthreads();
+        best = s_best[0];
+        best_slot = s_slot[0];
+        return s_cnt[0];
+    };
+    const int held_recent = reduce(c);
+    __syncthreads();                                      // s_* are rewritten below
+    if (held_recent != p.recent) {
+        // 2. the exact recent window: the `recent` largest positions
         int need_eq;
         const uint32_t T = block_radix_select(
             [&](int i) { return static_cast<uint32_t>(pos[i]) ^ 0x80000000u; }, n,
             min(p.recent, n), hist, tmp, sel, &need_eq);
-        thr = static_cast<int>(T ^ 0x80000000u) - 1;   // positions are unique
-    }
-    // 3. victim: lowest score, then the higher position
-    unsigned long long best = ~0ull;
+        thr = static_cast<int>(T ^ 0x80000000u) - 1;     // positions are unique
+        best = ~0ull;
+        best_slot = -1;
 #pragma unroll 4
-    for (int t = threadIdx.x; t < n; t += blockDim.x) {
-        const int ps = pos[t];
-        if (ps > thr) continue;
-        const unsigned long long key =
-            (static_cast<unsigned long long>(float_key(score[t])) << 32) |
-            static_cast<unsigned long long>(0x7fffffffu - static_cast<uint32_t>(ps));
-        best = key < best ? key : best;
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-        best = y < best ? y : best;
-    }
-    if ((threadIdx.x & 31) == 0) s_best[threadIdx.x >> 5] = best;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        best = threadIdx.x < (blockDim.x >> 5) ? s_best[threadIdx.x] : ~0ull;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-            best = y < best ? y : best;
+        for (int t = threadIdx.x; t < n; t += blockDim.x) {
+            const int ps = pos[t];
+            if (ps > thr) continue;
+            const unsigned long long key = victim_key(score[t], ps);
+            if (key < best) {
+                best = key;
+                best_slot = t;
+            }
         }
-        if (threadIdx.x == 0) s_best[0] = best;
+        reduce(0);
     }
-    __syncthreads();
-    best = s_best[0];
     if (best == ~0ull) {   // no candidate (recent >= n): nothing can be evicted
-        write_back(n);
         if (threadIdx.x == 0) p.evicted_pos[u] = -1;
         return;
     }
     const int victim_pos = static_cast<int>(0x7fffffffu - static_cast<uint32_t>(best & 0xffffffffu));
-    // 4. find the victim's slot, then move the last slot into it
-    __shared__ int s_slot;
-#pragma unroll 4
-    for (int t = threadIdx.x; t < n; t += blockDim.x)
-        if (pos[t] == victim_pos) s_slot = t;
-    __syncthreads();
-    const int v = s_slot, last = n - 1;
+    // 3. move the last slot into the victim's
+    const int v = best_slot, last = n - 1;
     if (v != last) {
         uint4* K = static_cast<uint4*>(p.kv.k) + (int64_t)off * segs;
         uint4* V = static_cast<uint4*>(p.kv.v) + (int64_t)off * segs;
@@ -171,11 +200,8 @@ __global__ void __launch_bounds__(kEvictThreads) h2o_evict_kernel(const EvictPar
         if (threadIdx.x == 0) {
             pos[v] = pos[last];
             score[v] = score[last];
-            if (STAGED) gpos[v] = pos[last];
         }
     }
-    __syncthreads();
-    write_back(n - 1);
     if (threadIdx.x == 0) {
         p.evicted_pos[u] = victim_pos;
         p.kv.seg_len[u] = n - 1;
@@ -242,21 +268,15 @@ cudaError_t launch_h2o_step(const se_h2o_state& st, const void* q, const void* k
     p.lse = lse_used;
     p.evicted_pos = evicted_pos;
     p.status = status;
-    const size_t stage_bytes = (size_t)8 * kv.seg_cap;
-    const bool staged = stage_bytes <= kEvictStageMax;
     auto go = [&](auto kern) -> cudaError_t {
-        const size_t smem = staged ? stage_bytes : 0;
-        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              static_cast<int>(smem));
-        if (e2 != cudaSuccess) return e2;
-        kern<<<units, kEvictThreads, smem, s>>>(p);
+        kern<<<units, kEvictThreads, 0, s>>>(p);
         return cudaGetLastError();
     };
     switch (G) {
-        case 4:  return staged ? go(h2o_evict_kernel<true, 1>) : go(h2o_evict_kernel<false, 1>);
-        case 8:  return staged ? go(h2o_evict_kernel<true, 2>) : go(h2o_evict_kernel<false, 2>);
-        case 16: return staged ? go(h2o_evict_kernel<true, 4>) : go(h2o_evict_kernel<false, 4>);
-        default: return staged ? go(h2o_evict_kernel<true, 0>) : go(h2o_evict_kernel<false, 0>);
+        case 4:  return go(h2o_evict_kernel<1>);
+        case 8:  return go(h2o_evict_kernel<2>);
+        case 16: return go(h2o_evict_kernel<4>);
+        default: return go(h2o_evict_kernel<0>);
     }
 }
 
