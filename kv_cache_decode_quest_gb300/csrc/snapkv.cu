@@ -350,12 +350,106 @@ struct SkSelParams {
 };
 constexpr int kGatherRows = 128;                // kept rows per gather CTA
 constexpr int kSelSmemMax = 200 * 1024;         // shared-memory key budget of the select
+constexpr int kPoolRegs = 32;                    // scores per thread of the one-round pooling
+
+// The float an order-preserving key was made from (float_key inverted).
+__device__ __forceinline__ float sel_key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Threshold of the top K of m keys in ky (lo / hi: the smallest and largest),
+// one block of 1024 threads: one histogram pass over kValBins equal-width
+// bins of the key VALUES between the smallest and the largest (weakly
+// monotone in the key, so every bin above the boundary bin is kept whole and
+// every bin below it dropped), then the boundary bin's keys are gathered and
+// ranked exactly by (key desc, position asc).  Returns the K-th largest key T
+// and in *need_eq how many keys equal to T belong to the top K; a boundary bin
+// of more than kValCap keys (many equal or clustered values) takes the radix
+// passes instead.  vh: kValBins ints of shared memory.
+constexpr int kValBins = 2048, kValCap = 1024;
+template <typename KeyAt>
+__device__ uint32_t value_select(KeyAt key_at, int m, int K, uint32_t lo, uint32_t hi, int* vh,
+                                 int* hist, int* tmp, int* sel, int* need_eq) {
+    if (lo == hi) {                                       // every key is equal
+        *need_eq = K;
+        return hi;
+    }
+    const int tid = threadIdx.x;
+    const float flo = sel_key_float(lo);
+    const float scale = static_cast<float>(kValBins) / (sel_key_float(hi) - flo);
+    auto bin_of = [&](uint32_t k) {
+        const int b = static_cast<int>((sel_key_float(k) - flo) * scale);   // NaN -> 0
+        return min(kValBins - 1, max(0, b));
+    };
+    constexpr int kPer = kValBins / 1024;                 // bins per thread
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) vh[tid * kPer + j] = 0;
+    if (tid == 0) sel[0] = 0;
+    __syncthreads();
+    for (int i = tid; i < m; i += blockDim.x) atomicAdd(&vh[bin_of(key_at(i))], 1);
+    __syncthreads();
+    // the boundary bin, scanning from the top (thread t owns bins
+    // kValBins-1-kPer*t ..)
+    int vv[kPer], v = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        vv[j] = vh[kValBins - 1 - (tid * kPer + j)];
+        v += vv[j];
+    }
+    int total = 0;
+    int run = block_exclusive_scan(v, tmp, &total);
+    __shared__ int s_bin[3];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        if (run < K && run + vv[j] >= K) {
+            s_bin[0] = kValBins - 1 - (tid * kPer + j);
+            s_bin[1] = run;
+            s_bin[2] = vv[j];
+        }
+        run += vv[j];
+    }
+    __syncthreads();
+    const int bstar = s_bin[0], R = K - s_bin[1], E = s_bin[2];
+    if (E > kValCap) return block_radix_select(key_at, m, K, hist, tmp, sel, need_eq);
+    // the boundary bin's keys and positions, gathered into the free histogram
+    uint32_t* bk = reinterpret_cast<uint32_t*>(vh);
+    int* bp = vh + kValCap;
+    for (int i = tid; i < m; i += blockDim.x) {
+        const uint32_t k = key_at(i);
+        if (bin_of(k) == bstar) {
+            const int at = atomicAdd(&sel[0], 1);
+            bk[at] = k;
+            bp[at] = i;
+        }
+    }
+    __syncthreads();
+    __shared__ uint32_t s_T;
+    __shared__ int s_need;
+    for (int t = tid; t < E; t += blockDim.x) {
+        const uint32_t k = bk[t];
+        const int ps = bp[t];
+        int rank = 0, above = 0;
+        for (int j = 0; j < E; ++j) {
+            const uint32_t kj = bk[j];
+            rank += kj > k || (kj == k && bp[j] < ps);
+            above += kj > k;
+        }
+        if (rank == R - 1) {                              // the last kept key of the bin
+            s_T = k;
+            s_need = R - above;
+        }
+    }
+    __syncthreads();
+    *need_eq = s_need;
+    return s_T;
+}
 
 // One CTA (1024 threads) per unit (candidates: SnapKV's prefix before the
 // recent window, or a caller's span with every position outside it kept):
 // max-pooled candidate scores -> keys (in
 // shared memory when they fit), exact top-`keep` by (pooled desc, position
-// asc) with four 8-bit radix passes, then the kept positions in ascending
+// asc) from one value histogram and the boundary bin's ranks (value_select),
+// then the kept positions in ascending
 // order (each thread owns a contiguous run of candidates: two block scans
 // place them) followed by the recent window.  The rows are gathered by
 // snapkv_gather_kernel.
@@ -365,6 +459,8 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
     __shared__ int tmp[33];
     __shared__ int sel[2];
     __shared__ int wgt[32], weq[32];
+    __shared__ int vh[kValBins];
+    __shared__ uint32_t s_lo[32], s_hi[32];
     const int H = p.kv.num_kv_heads;
     const int u = blockIdx.x, b = u / H, h = u % H;
     int L = p.kv.ctx_len[b];
@@ -388,39 +484,101 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
     const float* A = p.colsum + (int64_t)u * p.max_ctx + s0;
     uint32_t* ky = p.keys_in_smem ? skeys : p.keys + (int64_t)u * p.max_ctx;
     const int nw = blockDim.x >> 5, wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // max-pool over [j-rad, j+rad] clipped to the candidates: a warp takes 32
-    // consecutive positions, one per lane, and its 2*rad neighbours by shuffle
-    // (lanes < rad also hold the halo on either side; rad <= 31)
-    constexpr int kPB = 8;                        // chunks whose loads are in flight together
-    for (int jb = wid * 32; jb < ncand; jb += nw * 32 * kPB) {
-        float x[kPB], hl[kPB], hr[kPB];
+    // max-pool over [j-rad, j+rad] clipped to the candidates (rad <= 31)
+    uint32_t klo = 0xffffffffu, khi = 0u;         // the keys' smallest and largest
+    if (p.keys_in_smem && ncand <= kPoolRegs * 1024) {
+        // every score of the unit in flight at once (32 coalesced loads per
+        // thread, one latency round), staged in the key area; each thread
+        // pools its positions from there into registers, then the keys
+        // overwrite the scores in place
+        float* sa = reinterpret_cast<float*>(skeys);
+        float v[kPoolRegs];
 #pragma unroll
-        for (int q = 0; q < kPB; ++q) {
-            const int j0 = jb + q * nw * 32, j = j0 + lane;
-            x[q] = j < ncand ? A[j] : -INFINITY;
-            hl[q] = -INFINITY;
-            hr[q] = -INFINITY;
-            if (lane < rad) {
-                const int jl = j0 - rad + lane, jr = j0 + 32 + lane;
-                if (jl >= 0 && jl < ncand) hl[q] = A[jl];
-                if (jr < ncand) hr[q] = A[jr];
-            }
+        for (int q = 0; q < kPoolRegs; ++q) {
+            const int j = q * 1024 + threadIdx.x;
+            v[q] = j < ncand ? A[j] : -INFINITY;
         }
 #pragma unroll
-        for (int q = 0; q < kPB; ++q) {
-            const int j = jb + q * nw * 32 + lane;
-            float mx = x[q];
-            for (int t = 1; t <= rad; ++t) {
-                const float li = __shfl_sync(0xffffffffu, x[q], (lane - t) & 31);
-                const float lh = __shfl_sync(0xffffffffu, hl[q], (lane - t + rad) & 31);
-                const float ri = __shfl_sync(0xffffffffu, x[q], (lane + t) & 31);
-                const float rh = __shfl_sync(0xffffffffu, hr[q], (lane + t - 32) & 31);
-                mx = fmaxf(mx, fmaxf(lane >= t ? li : lh, lane + t < 32 ? ri : rh));
+        for (int q = 0; q < kPoolRegs; ++q) {
+            const int j = q * 1024 + threadIdx.x;
+            if (j < ncand) sa[j] = v[q];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < kPoolRegs; ++q) {
+            const int j = q * 1024 + threadIdx.x;
+            float mx = v[q];
+            const int t0 = max(0, j - rad), t1 = min(ncand - 1, j + rad);
+            for (int t = t0; t <= t1; ++t) mx = fmaxf(mx, sa[t]);
+            v[q] = mx;
+        }
+        __syncthreads();                                  // every window is read
+#pragma unroll
+        for (int q = 0; q < kPoolRegs; ++q) {
+            const int j = q * 1024 + threadIdx.x;
+            if (j < ncand) {
+                const uint32_t k = float_key(v[q]);
+                ky[j] = k;
+                klo = min(klo, k);
+                khi = max(khi, k);
             }
-            if (j < ncand) ky[j] = float_key(mx);
+        }
+    } else {
+        // a warp takes 32 consecutive positions, one per lane, and its 2*rad
+        // neighbours by shuffle (lanes < rad also hold the halo on either side)
+        constexpr int kPB = 8;                    // chunks whose loads are in flight together
+        for (int jb = wid * 32; jb < ncand; jb += nw * 32 * kPB) {
+            float x[kPB], hl[kPB], hr[kPB];
+#pragma unroll
+            for (int q = 0; q < kPB; ++q) {
+                const int j0 = jb + q * nw * 32, j = j0 + lane;
+                x[q] = j < ncand ? A[j] : -INFINITY;
+                hl[q] = -INFINITY;
+                hr[q] = -INFINITY;
+                if (lane < rad) {
+                    const int jl = j0 - rad + lane, jr = j0 + 32 + lane;
+                    if (jl >= 0 && jl < ncand) hl[q] = A[jl];
+                    if (jr < ncand) hr[q] = A[jr];
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kPB; ++q) {
+                const int j = jb + q * nw * 32 + lane;
+                float mx = x[q];
+                for (int t = 1; t <= rad; ++t) {
+                    const float li = __shfl_sync(0xffffffffu, x[q], (lane - t) & 31);
+                    const float lh = __shfl_sync(0xffffffffu, hl[q], (lane - t + rad) & 31);
+                    const float ri = __shfl_sync(0xffffffffu, x[q], (lane + t) & 31);
+                    const float rh = __shfl_sync(0xffffffffu, hr[q], (lane + t - 32) & 31);
+                    mx = fmaxf(mx, fmaxf(lane >= t ? li : lh, lane + t < 32 ? ri : rh));
+                }
+                if (j < ncand) {
+                    const uint32_t k = float_key(mx);
+                    ky[j] = k;
+                    klo = min(klo, k);
+                    khi = max(khi, k);
+                }
+            }
+        }
+    }
+    klo = __reduce_min_sync(0xffffffffu, klo);
+    khi = __reduce_max_sync(0xffffffffu, khi);
+    if (lane == 0) {
+        s_lo[wid] = klo;
+        s_hi[wid] = khi;
+    }
+    __syncthreads();
+    if (wid == 0) {
+        klo = __reduce_min_sync(0xffffffffu, lane < nw ? s_lo[lane] : 0xffffffffu);
+        khi = __reduce_max_sync(0xffffffffu, lane < nw ? s_hi[lane] : 0u);
+        if (lane == 0) {
+            s_lo[0] = klo;
+            s_hi[0] = khi;
         }
     }
     __syncthreads();
+    klo = s_lo[0];
+    khi = s_hi[0];
 
     const int off = p.out.seg_off[u];
     const int cap = p.out.seg_cap;
@@ -437,8 +595,8 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
             for (int j = threadIdx.x; j < ncand && j + s0 < cap; j += blockDim.x) pos[j] = s0 + j;
         } else if (K > 0) {
             int need_eq;
-            const uint32_t T = block_radix_select([&](int i) { return ky[i]; }, ncand, K, hist, tmp,
-                                                  sel, &need_eq);
+            const uint32_t T = value_select([&](int i) { return ky[i]; }, ncand, K, klo, khi, vh,
+                                            hist, tmp, sel, &need_eq);
             // emit in ascending position: warp w owns a contiguous chunk read
             // with a lane stride; ballots rank the kept keys inside the warp and
             // a scan over the warps places each warp's run.
@@ -504,8 +662,13 @@ __global__ void __launch_bounds__(1024) snapkv_select_kernel(const SkSelParams p
 }
 
 // grid (row blocks, units): copies the kept rows of K and V (and their
-// unpooled scores) into the unit's varlen segment, in kept order.
-__global__ void __launch_bounds__(256) snapkv_gather_kernel(const SkSelParams p) {
+// unpooled scores) into the unit's varlen segment, in kept order.  The block's
+// rows are resolved first (position, then its physical page: two dependent
+// round trips per block, not per copy) into shared memory; then each thread
+// issues all of its 16-byte K and V loads before its stores.
+constexpr int kGatherThreads = 256;
+__global__ void __launch_bounds__(kGatherThreads) snapkv_gather_kernel(const SkSelParams p) {
+    __shared__ int64_t s_src[kGatherRows];                // source row, -1 when invalid
     const int H = p.kv.num_kv_heads, D = p.kv.head_dim, segs = D / 8;
     const int u = blockIdx.y, b = u / H, h = u % H;
     const int n = p.out.seg_len[u];
@@ -516,24 +679,50 @@ __global__ void __launch_bounds__(256) snapkv_gather_kernel(const SkSelParams p)
     const int32_t* bt = p.kv.block_table + (int64_t)b * p.kv.max_pages_per_seq;
     const int32_t* pos = p.out.pos + off;
     const float* A = p.colsum + (int64_t)u * p.max_ctx;
+    for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+        const int ps = pos[r];
+        const int page = ps / kPage;
+        const int phys = (ps >= 0 && page < p.kv.max_pages_per_seq) ? bt[page] : -1;
+        int64_t src = -1;
+        if (phys < 0 || phys >= p.kv.num_pages) {
+            flag(p.status, SE_DEV_BAD_INDEX);
+        } else {
+            src = ((int64_t)phys * H + h) * kPage + ps % kPage;
+            if (p.out.score) p.out.score[(int64_t)off + r] = A[ps];
+        }
+        s_src[r - r0] = src;
+    }
+    __syncthreads();
     const uint4* Ks = static_cast<const uint4*>(p.kv.k);
     const uint4* Vs = static_cast<const uint4*>(p.kv.v);
     uint4* Kd = static_cast<uint4*>(p.out.k);
     uint4* Vd = static_cast<uint4*>(p.out.v);
-    for (int i = threadIdx.x; i < (r1 - r0) * segs; i += blockDim.x) {
-        const int r = r0 + i / segs, sg = i % segs;
-        const int ps = pos[r];
-        const int page = ps / kPage;
-        const int phys = (ps >= 0 && page < p.kv.max_pages_per_seq) ? bt[page] : -1;
-        if (phys < 0 || phys >= p.kv.num_pages) {
-            if (sg == 0) flag(p.status, SE_DEV_BAD_INDEX);
-            continue;
+    const int total = (r1 - r0) * segs;
+    constexpr int kU = 4;                                 // copies of a thread in flight together
+    for (int i0 = threadIdx.x; i0 < total; i0 += kGatherThreads * kU) {
+        uint4 kv4[kU], vv4[kU];
+        int64_t dst[kU];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            const int i = i0 + q * kGatherThreads;
+            dst[q] = -1;
+            if (i < total) {
+                const int r = i / segs, sg = i % segs;
+                const int64_t src = s_src[r];
+                if (src >= 0) {
+                    kv4[q] = Ks[src * segs + sg];
+                    vv4[q] = Vs[src * segs + sg];
+                    dst[q] = ((int64_t)off + r0 + r) * segs + sg;
+                }
+            }
         }
-        const int64_t src = ((int64_t)phys * H + h) * kPage + ps % kPage;
-        const int64_t dst = (int64_t)off + r;
-        Kd[dst * segs + sg] = Ks[src * segs + sg];
-        Vd[dst * segs + sg] = Vs[src * segs + sg];
-        if (sg == 0 && p.out.score) p.out.score[dst] = A[ps];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            if (dst[q] >= 0) {
+                Kd[dst[q]] = kv4[q];
+                Vd[dst[q]] = vv4[q];
+            }
+        }
     }
 }
 
@@ -624,7 +813,7 @@ cudaError_t launch_snapkv_compact(const se_paged_kv& kv, const void* q_win, int 
     if (e != cudaSuccess) return e;
     const int max_rows = min(out.seg_cap, max_ctx);
     dim3 g((max_rows + kGatherRows - 1) / kGatherRows, units);
-    snapkv_gather_kernel<<<g, 256, 0, s>>>(q);
+    snapkv_gather_kernel<<<g, kGatherThreads, 0, s>>>(q);
     return cudaGetLastError();
 }
 
