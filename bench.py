@@ -37,7 +37,7 @@ PROFILE_DIR = os.path.join(ROOT, "profiles")
 CSRC = os.path.join(ROOT, "kv_cache_decode_quest_gb300", "csrc")
 # the Quest step as the bench runs it: "step" = append, select and decode in one
 # kernel (se_quest_step); "fused" = se_quest_select_append + se_sparse_decode
-HEADLINE_MODE = "fused"
+HEADLINE_MODE = "step"
 RAGGED_MODE = "step"
 # per mode: the dominant kernel, its source and its committed ncu traffic record
 KERNEL_OF_MODE = {
