@@ -45,8 +45,9 @@ class QuestRun:
     """Paged KV + Quest selection + split-K decode, one appended token per step.
 
     mode: "fused"    -- se_quest_select_append, then se_sparse_decode (the
-                        faster path on the bench workloads, the default);
-          "step"     -- se_quest_step: append, select and decode in one kernel;
+                        default here; the faster path for a single query);
+          "step"     -- se_quest_step: append, select and decode in one kernel
+                        (the faster path on the multi-sequence workloads);
           "separate" -- se_kv_append, se_quest_select, se_sparse_decode.
     step_tuning: se_quest_step_opts fields (mode "step"): wait_limit_ns."""
 
